@@ -1,0 +1,463 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated DeltaNet token mixer on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+  * prefill: one sequence of T=8192 tokens, H_k=16 tiled to H_v=48, bf16
+    activations, zero initial state (gdn_prefill_chunked, chunk = 64);
+  * decode: B=64 sequences, one token each, H_k=16 / H_v=32, bf16, fp32 state
+    updated in place (gdn_decode_step);
+  * speculative verify: the same B=64 sequences, K=3 tokens each, with
+    per-position checkpoints (gdn_verify_k), then gdn_commit of a seeded
+    accept length in {1,2,3}.
+value = tokens processed per second over the step (8192 + 64 + 192 tokens);
+the per-part figures (tokens/s, ms, roofline) are under "parts".
+
+Timing: CUDA events on the launching stream, W >= 3 warm-up steps, L2 flushed
+(a 256 MiB write) before every timed step, outside the timed region; every
+input is also larger than L2.  e2e: the same step through the C ABI with the
+step's inputs copied from pinned host memory and its outputs read back, inside
+the timed region.  Under torchrun (N > 1) each rank runs its own replica (no
+collective on the data path: the layer shards by sequence and head) and the
+slowest rank's time is used.
+
+--impl reference times the CPU oracle (fp64, OpenMP) on the host cores on a
+bounded sample of the same step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gdn_inputs  # noqa: E402
+
+METRIC = "GDN layer tokens/s: prefill T=8192 & decode B=64; % of roofline"
+WORKLOAD = ("prefill T=8192 H_k=16 H_v=48 bf16 (chunk 64) + decode B=64 H_k=16 H_v=32 bf16 "
+            "+ verify B=64 K=3 + commit")
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------------ algorithmic work
+def prefill_bytes(T, Hk, Hv, out_bytes=2, act_bytes=2, init_state=False):
+    C = 128 * (2 * Hk + Hv)
+    HvD = Hv * 128
+    b = T * C * act_bytes + T * HvD * act_bytes + 2 * T * Hv * act_bytes + T * HvD * out_bytes
+    b += Hv * 128 * 128 * 4 + 3 * C * act_bytes                 # final S and conv state written
+    if init_state:
+        b += Hv * 128 * 128 * 4 + 3 * C * act_bytes             # initial state read
+    b += C * 16 + Hv * 8 + 128 * 4                              # weights
+    return b
+
+
+def decode_bytes(B, Hk, Hv, K=1, act_bytes=2, out_bytes=2, ckpt=False):
+    C = 128 * (2 * Hk + Hv)
+    per_seq = 2 * Hv * 128 * 128 * 4 if not ckpt else Hv * 128 * 128 * 4 * (1 + K)
+    per_seq += (3 * C * act_bytes) * (2 if not ckpt else 1 + K)
+    per_seq += K * (C + Hv * 128 + 2 * Hv) * act_bytes + K * Hv * 128 * out_bytes
+    return B * per_seq + C * 16 + Hv * 8 + 128 * 4
+
+
+def prefill_flops(T, Hv):
+    # chunk-64 form, triangles counted once: 1.41e5 flop per token per v-head
+    C_, d = 64, 128
+    per = (C_ * (C_ - 1) * d / C_ + C_ * C_ / 3 + 2 * (C_ + 1) * d + 2 * d * d + (C_ + 1) * d
+           + 2 * d * d + (C_ + 1) * d + 2 * d * d + 2 * d)
+    return per * T * Hv
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.lines = []
+        self.bus = None
+        try:
+            pr = torch.cuda.get_device_properties(device_index)
+            if hasattr(pr, "pci_bus_id"):
+                self.bus = f"{getattr(pr, 'pci_domain_id', 0):08X}:{pr.pci_bus_id:02X}:{getattr(pr, 'pci_device_id', 0):02X}.0"
+        except Exception:
+            pass
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.bus:
+            cmd.insert(1, f"--id={self.bus}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ the GPU arm
+class Workload:
+    """Device-resident inputs/outputs of one step, plus pinned host copies for e2e."""
+
+    def __init__(self, device):
+        import gated_deltanet_linear_decode_gb300 as gdn
+        self.gdn = gdn
+        dev = device
+        self.pc = gdn_inputs.prefill_t8192()
+        self.dc = gdn_inputs.decode_b64()
+        self.vc = gdn_inputs.verify_b64_k3()
+        pc, dc, vc = self.pc, self.dc, self.vc
+        self.p_dims = gdn.make_dims(pc.Hk, pc.Hv, torch.bfloat16, torch.bfloat16)
+        self.d_dims = gdn.make_dims(dc.Hk, dc.Hv, torch.bfloat16, torch.bfloat16)
+        self.p_w = gdn.make_weights(pc.conv_w, pc.dt_bias, pc.ssm_a, pc.norm_w, device=dev)
+        self.d_w = gdn.make_weights(dc.conv_w, dc.dt_bias, dc.ssm_a, dc.norm_w, device=dev)
+        # host (pinned) inputs for the e2e leg
+        pin = lambda t: t.contiguous().pin_memory()
+        self.h = {k: pin(getattr(pc, k)) for k in ("x", "z", "a_raw", "b_raw")}
+        self.hd = {k: pin(getattr(dc, k)) for k in ("x", "z", "a_raw", "b_raw")}
+        self.hv = {k: pin(getattr(vc, k)) for k in ("x", "z", "a_raw", "b_raw")}
+        # device copies
+        self.p_in = {k: v.to(dev, non_blocking=True) for k, v in self.h.items()}
+        self.d_in = {k: v.to(dev, non_blocking=True) for k, v in self.hd.items()}
+        self.v_in = {k: v.to(dev, non_blocking=True) for k, v in self.hv.items()}
+        self.cu_h = pc.cu_seqlens.to(torch.int32)
+        self.cu_d = self.cu_h.to(dev)
+        self.p_conv = torch.zeros(1, 3, pc.C, device=dev, dtype=torch.bfloat16)
+        self.p_S = torch.zeros(1, pc.Hv, 128, 128, device=dev)
+        self.p_out = torch.empty(pc.T, pc.Hv * 128, device=dev, dtype=torch.bfloat16)
+        nws = gdn.gdn_prefill_workspace_bytes(self.p_dims, 1, pc.T)
+        self.p_ws = torch.empty(max(nws, 16), device=dev, dtype=torch.uint8) if nws else None
+        self.d_conv = dc.conv0.to(dev)
+        self.d_S = dc.S0.to(dev)
+        self.d_out = torch.empty(dc.N, dc.Hv * 128, device=dev, dtype=torch.bfloat16)
+        B, K = vc.N, vc.K
+        self.v_ckc = torch.empty(B, K, 3, vc.C, device=dev, dtype=torch.bfloat16)
+        self.v_ckS = torch.empty(B, K, vc.Hv, 128, 128, device=dev)
+        self.v_out = torch.empty(B * K, vc.Hv * 128, device=dev, dtype=torch.bfloat16)
+        self.acc = vc.accept_len.to(dev)
+        self.h_pout = torch.empty(self.p_out.shape, dtype=torch.bfloat16).pin_memory()
+        self.h_dout = torch.empty(self.d_out.shape, dtype=torch.bfloat16).pin_memory()
+        self.h_vout = torch.empty(self.v_out.shape, dtype=torch.bfloat16).pin_memory()
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+        self.launches_per_step = 0
+
+    # each call returns the number of library kernels it launched
+    def prefill(self):
+        g, i = self.gdn, self.p_in
+        g.gdn_prefill_chunked(self.p_dims, self.p_w, self.cu_h, self.cu_d, i["x"], i["z"], i["a_raw"], i["b_raw"],
+                              self.p_conv, self.p_S, self.p_out, zero_init=True, workspace=self.p_ws)
+        return 2
+
+    def decode(self):
+        g, i = self.gdn, self.d_in
+        g.gdn_decode_step(self.d_dims, self.d_w, i["x"], i["z"], i["a_raw"], i["b_raw"], self.d_conv, self.d_S,
+                          self.d_out)
+        return 1
+
+    def verify(self):
+        g, i = self.gdn, self.v_in
+        g.gdn_verify_k(self.d_dims, self.d_w, self.vc.K, i["x"], i["z"], i["a_raw"], i["b_raw"], self.d_conv,
+                       self.d_S, self.v_ckc, self.v_ckS, self.v_out)
+        g.gdn_commit(self.d_dims, self.vc.K, self.acc, self.v_ckc, self.v_ckS, self.d_conv, self.d_S)
+        return 2
+
+    def h2d(self):
+        for src, dst in ((self.h, self.p_in), (self.hd, self.d_in), (self.hv, self.v_in)):
+            for k in src:
+                dst[k].copy_(src[k], non_blocking=True)
+
+    def d2h(self):
+        self.h_pout.copy_(self.p_out, non_blocking=True)
+        self.h_dout.copy_(self.d_out, non_blocking=True)
+        self.h_vout.copy_(self.v_out, non_blocking=True)
+
+    def io_bytes(self):
+        h2d = sum(t.numel() * t.element_size() for d in (self.h, self.hd, self.hv) for t in d.values())
+        d2h = sum(t.numel() * t.element_size() for t in (self.h_pout, self.h_dout, self.h_vout))
+        return h2d, d2h
+
+    def flush_l2(self):
+        self.flush.fill_(1.0)
+
+
+def run_gpu(args, rank, world):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    import gated_deltanet_linear_decode_gb300 as gdn
+    gdn.library()
+    wl = Workload(dev)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        wl.flush_l2()
+        wl.prefill(); wl.decode(); wl.verify()
+    torch.cuda.synchronize()
+
+    parts = {"prefill": [], "decode": [], "verify": []}
+    launches = 0
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    _barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    step_ms = []
+    for _ in range(args.steps):
+        wl.flush_l2()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record(stream)
+        launches += wl.prefill()
+        ev[1].record(stream)
+        launches += wl.decode()
+        ev[2].record(stream)
+        launches += wl.verify()
+        ev[3].record(stream)
+        torch.cuda.synchronize()
+        parts["prefill"].append(ev[0].elapsed_time(ev[1]))
+        parts["decode"].append(ev[1].elapsed_time(ev[2]))
+        parts["verify"].append(ev[2].elapsed_time(ev[3]))
+        step_ms.append(ev[0].elapsed_time(ev[3]))
+    torch.cuda.synchronize()
+    _barrier(world)
+    wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+
+    # e2e: host buffers in, results out, inside the timed region
+    e2e_ms = []
+    for _ in range(max(1, args.steps)):
+        wl.flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        wl.h2d()
+        wl.prefill(); wl.decode(); wl.verify()
+        wl.d2h()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+
+    tot_ms = sum(step_ms)
+    tot_ms = _max_over_ranks(tot_ms, world)
+    e2e_tot = _max_over_ranks(sum(e2e_ms), world)
+    pc, dc, vc = wl.pc, wl.dc, wl.vc
+    tok_step = pc.T + dc.N + vc.N * vc.K
+    value = world * tok_step * args.steps / (tot_ms / 1e3)
+    hbm, tf, peak_src = peaks()
+    pm = statistics.mean(parts["prefill"])
+    dm = statistics.mean(parts["decode"])
+    vm = statistics.mean(parts["verify"])
+    pb = prefill_bytes(pc.T, pc.Hk, pc.Hv)
+    db = decode_bytes(dc.N, dc.Hk, dc.Hv)
+    vb = decode_bytes(vc.N, vc.Hk, vc.Hv, K=vc.K, ckpt=True)
+    pf = prefill_flops(pc.T, pc.Hv)
+    p_roof = {"bound": "hbm", "achieved": pb / (pm / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+              "frac": pb / (pm / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes": pb,
+              "tensor_tflops_algorithmic": pf / (pm / 1e3) / 1e12, "peak_source": peak_src}
+    d_roof = {"bound": "hbm", "achieved": db / (dm / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+              "frac": db / (dm / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes": db, "peak_source": peak_src}
+    v_roof = {"bound": "hbm", "achieved": vb / (vm / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+              "frac": vb / (vm / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes_verify_only": vb,
+              "note": "time includes the commit copy"}
+    dominant = max((pm, "prefill", p_roof), (dm, "decode", d_roof), (vm, "verify", v_roof))[1:]
+    h2d, d2h = wl.io_bytes()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (bf16 activations in/out, fp32 state)",
+        "data": "synthetic (seeded; no weights or dataset)",
+        "config": {"workload": WORKLOAD, "tokens_per_step": tok_step, "l2": "flushed (256 MiB write) before each "
+                   "timed step; inputs also exceed L2", "parallelism": f"replicas x{world}"},
+        "roofline": {**dominant[1], "kernel": dominant[0]},
+        "parts": {
+            "prefill_T8192": {"tokens_per_s": pc.T / (pm / 1e3), "ms": pm, "roofline": p_roof},
+            "decode_B64": {"tokens_per_s": dc.N / (dm / 1e3), "ms": dm, "roofline": d_roof},
+            "verify_B64_K3_commit": {"tokens_per_s": vc.N * vc.K / (vm / 1e3), "ms": vm, "roofline": v_roof},
+        },
+        "e2e": {"value": world * tok_step * len(e2e_ms) / (e2e_tot / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+    }
+    return line
+
+
+def run_part(args):
+    """Warm-up then timed launches of one part only (profiling aid)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = Workload(dev)
+    fn = {"prefill": wl.prefill, "decode": wl.decode, "verify": wl.verify}[args.only]
+    for _ in range(args.warmup + args.steps):
+        wl.flush_l2()
+        fn()
+    torch.cuda.synchronize()
+    print(f"ran {args.only}: {args.warmup} warm-up + {args.steps} launches", flush=True)
+
+
+def _barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(v, world):
+    if world <= 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ the oracle (CPU)
+def oracle_step_sample(prefill_tokens=64, seed_cases=None):
+    """One bounded sample of the step on the host cores: the prefill's first
+    `prefill_tokens` tokens (all 48 heads), the full B=64 decode step and the
+    full B=64 K=3 verify walk (with checkpoints).  Returns (seconds, seconds
+    extrapolated to the whole step)."""
+    import oracle
+    pc, dc, vc = seed_cases
+    n = prefill_tokens
+    t0 = time.perf_counter()
+    oracle.forward(pc.Hk, pc.Hv, pc.x[:n], pc.z[:n], pc.a_raw[:n], pc.b_raw[:n], pc.conv_w, pc.dt_bias, pc.ssm_a,
+                   pc.norm_w, pc.conv0, pc.S0, cu_seqlens=[0, n])
+    t1 = time.perf_counter()
+    oracle.forward(dc.Hk, dc.Hv, dc.x, dc.z, dc.a_raw, dc.b_raw, dc.conv_w, dc.dt_bias, dc.ssm_a, dc.norm_w,
+                   dc.conv0, dc.S0, cu_seqlens=np.arange(dc.N + 1))
+    t2 = time.perf_counter()
+    oracle.verify_checkpoints(vc.Hk, vc.Hv, vc.x, vc.z, vc.a_raw, vc.b_raw, vc.conv_w, vc.dt_bias, vc.ssm_a,
+                              vc.norm_w, vc.conv0, vc.S0, vc.K)
+    t3 = time.perf_counter()
+    full = (t1 - t0) * pc.T / n + (t2 - t1) + (t3 - t2)
+    return t3 - t0, full
+
+
+def cpu_baseline(target_s=15.0):
+    import oracle
+    oracle.build()
+    cases = (gdn_inputs.prefill_t8192(), gdn_inputs.decode_b64(), gdn_inputs.verify_b64_k3())
+    tok = cases[0].T + cases[1].N + cases[2].N * cases[2].K
+    used, full = oracle_step_sample(64, cases)          # calibrate
+    n = int(min(cases[0].T, max(64, 64 * target_s / max(used, 1e-3))))
+    used, full = oracle_step_sample(n, cases)
+    return {"value": tok / full, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"fp64 C oracle on the host: prefill tokens 0..{n - 1} of T=8192 (48 heads) + the full "
+                      f"B=64 decode step + the full B=64 K=3 verify walk; the prefill part scaled by 8192/{n} "
+                      f"({used:.1f} s of CPU work)", "seconds": used}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    cases = (gdn_inputs.prefill_t8192(), gdn_inputs.decode_b64(), gdn_inputs.verify_b64_k3())
+    tok = cases[0].T + cases[1].N + cases[2].N * cases[2].K
+    n = 32
+    for _ in range(args.warmup):
+        oracle_step_sample(n, cases)
+    fulls, used = [], 0.0
+    for _ in range(args.steps):
+        u, f = oracle_step_sample(n, cases)
+        fulls.append(f)
+        used += u
+    tot = sum(fulls)
+    value = tok * len(fulls) / tot
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(fulls),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "tokens_per_step": tok},
+        "cpu_baseline": {"kind": "oracle", "cores": oracle.max_threads(), "value": value, "unit": "tokens/s",
+                         "sample": f"each step: prefill tokens 0..{n - 1} of T=8192 scaled by 8192/{n}, full B=64 "
+                                   f"decode, full B=64 K=3 verify ({used:.1f} s of CPU work in total)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode", "verify"], default=None,
+                    help="run only one part of the step (for profiling); no JSON line")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if args.only:
+        run_part(args)
+        return
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl")
+    line = run_gpu(args, rank, world)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,85 @@
+// gdn_internal.h -- launch parameter blocks shared by the host API and the
+// kernels of libgdn.so (not installed; the public surface is include/gdn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr uint32_t kFlagCheckFinite = 1u;
+
+// Recurrent walk (decode step when K == 1 and the outputs alias the states;
+// speculative verify when the outputs are the checkpoint planes).
+struct RecParams {
+    int B, K, Hk, Hv, C;
+    int CS;    // CTAs per cluster = (H_v/H_k) * SPH
+    int SPH;   // CTAs per v-head = 128 / rows-per-CTA
+    float eps;
+    uint32_t flags;
+    const void* x;          // [B*K][C]
+    const void* z;          // [B*K][Hv*128]
+    const void* a_raw;      // [B*K][Hv]
+    const void* b_raw;      // [B*K][Hv]
+    const float* conv_w;    // [C][4]
+    const float* dt_bias;   // [Hv]
+    const float* ssm_a;     // [Hv]
+    const float* norm_w;    // [128]
+    const void* conv_in;    // [B][3][C]
+    const float* S_in;      // [B][Hv][128][128]
+    void* conv_out;         // element (b, t) at conv_out + b*conv_out_b + t*conv_out_p
+    float* S_out;           // state (b, t) at S_out + b*S_out_b + t*S_out_p
+    long long conv_out_b, conv_out_p;
+    long long S_out_b, S_out_p;
+    void* out;              // [B*K][Hv*128]
+    float* prenorm;         // optional, [B*K][Hv*128]
+    int* dev_status;        // optional, [B*Hv]
+};
+
+struct CommitParams {
+    int B, K;
+    const int* accept_len;  // [B]
+    const void* conv_ckpt;  // [B][K][3][C]
+    const float* S_ckpt;    // [B][K][Hv][128][128]
+    void* conv_state;       // [B][3][C]
+    float* S;               // [B][Hv][128][128]
+    size_t S_elems;         // Hv*128*128
+    size_t conv_bytes;      // 3*C*sizeof(act)
+};
+
+// Chunked prefill over packed sequences.
+struct PrefillParams {
+    int n_seq;
+    long long T;
+    int max_len;
+    int Hk, Hv, C;
+    float eps;
+    uint32_t flags;
+    bool zero_init;
+    const int* cu_seqlens;   // device [n_seq+1]
+    const void* x;
+    const void* z;
+    const void* a_raw;
+    const void* b_raw;
+    const float* conv_w;
+    const float* dt_bias;
+    const float* ssm_a;
+    const float* norm_w;
+    void* conv_state;        // [n_seq][3][C] in/out
+    float* S;                // [n_seq][Hv][128][128] in/out
+    void* out;
+    float* prenorm;
+    int* dev_status;
+    void* workspace;
+};
+
+size_t prefill_workspace_bytes(int Hk, int Hv, int n_seq, long long T);
+cudaError_t launch_prefill(const PrefillParams& p, int act_dtype, int out_dtype, cudaStream_t stream);
+
+cudaError_t launch_recurrent(const RecParams& p, int act_dtype, int out_dtype, int rows_per_cta,
+                             cudaStream_t stream);
+cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream);
+cudaError_t launch_conv_init(void* dst, const void* src, size_t bytes, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,191 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) gated DeltaNet token mixer library
+ * (libgdn.so).
+ *
+ * The operation is the gated DeltaNet layer of the Qwen 3.6 hybrid models, as
+ * defined on the xwen CLAUDE.md page, "Architecture cheat sheet (Qwen 3.6,
+ * ggml-org GGUF)", paragraph "Gated DeltaNet layer", taken from the fused
+ * attn_qkv stream onward:
+ *
+ *   1. causal depthwise conv1d, kernel 4, no bias, over the full fused width
+ *      C = 128*(2*H_k + H_v); left context from a per-sequence conv state of
+ *      the last 3 raw rows (oldest first); tap 3 multiplies the current token;
+ *   2. SiLU over the whole fused stream;
+ *   3. split q = channels [0, 128*H_k), k = [128*H_k, 256*H_k), v = the rest,
+ *      head-major inside each block (channel = head*128 + i);
+ *   4. L2 norm of q and k in clamp form x / max(||x||, eps);
+ *   5. q/k heads tiled to H_v (v-head j reads q/k head j mod H_k -- the page's
+ *      "GGUF facts" section: V-head order is tiled, not interleaved);
+ *   6. beta = sigmoid(b_raw), g = ssm_a * softplus(a_raw + dt_bias), with
+ *      ssm_a = -exp(A_log) pre-baked;
+ *   7. delta rule on an fp32 state S per (sequence, v-head):
+ *        S = S*exp(g);  d = (v - S.k)*beta;  S += k (x) d;  o = S.q/sqrt(128)
+ *   8. gated RMSNorm over each head's 128 outputs:
+ *        y = o / sqrt(mean(o^2) + eps) * norm_w * silu(z).
+ *
+ * Two forms compute it: a per-token recurrent step (gdn_decode_step and the
+ * speculative-verify walk gdn_verify_k) and the chunked form with chunk = 64
+ * (gdn_prefill_chunked; the page's "Ground truth" list names both forms).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument except the gdn_dims / gdn_weights structs and the
+ *     cu_seqlens_host array is DEVICE memory, allocated and owned by the
+ *     caller.  The library allocates nothing and keeps no state between calls.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  A non-GDN_OK return from argument validation means
+ *     nothing was enqueued.  GDN_E_CUDA reports a launch error.
+ *   - Every device pointer must be 16-byte aligned (GDN_E_ALIGNMENT).
+ *   - Errors are returned, never printed; the library never exits.
+ *   - Layouts are dense row-major, innermost index last, in elements:
+ *       x           [T][C]                act dtype
+ *       z, out      [T][H_v*128]          act dtype / out dtype
+ *       a_raw,b_raw [T][H_v]              act dtype
+ *       conv_state  [N][3][C]             act dtype (raw rows, oldest first)
+ *       S           [N][H_v][128][128]    fp32, S[j][i]: j the v-row, i the
+ *                                         k-index; "S.k" = sum_i S[j][i] k_i
+ *       conv_w      [C][4] fp32; dt_bias, ssm_a [H_v] fp32; norm_w [128] fp32
+ *   - prenorm_out (optional, may be NULL) receives o before the gated norm,
+ *     fp32 with out's layout.
+ *   - dev_status (optional, may be NULL) is int32 [N*H_v].  When
+ *     GDN_FLAG_CHECK_FINITE is set, the kernels OR bit 0 into
+ *     dev_status[n*H_v + h] if the updated state of (n, h) holds a non-finite
+ *     value and bit 1 if its output does.  The caller zeroes it and reads it
+ *     after synchronising (the production failure mode the home-server page
+ *     records: non-finite GDN state that persists in cached state).
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the CUDA runtime's stream handle). */
+typedef struct CUstream_st* gdn_stream_t;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_E_INVALID_ARG = 1,   /* null pointer, bad size, bad enum, aliasing */
+    GDN_E_UNSUPPORTED = 2,   /* valid but not supported (e.g. H_v/H_k > 16) */
+    GDN_E_ALIGNMENT = 3,     /* a device pointer is not 16-byte aligned */
+    GDN_E_CUDA = 4,          /* a CUDA launch or query failed */
+    GDN_E_WORKSPACE = 5      /* workspace missing or too small */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+#define GDN_HEAD_DIM 128
+#define GDN_CONV_KERNEL 4
+#define GDN_CHUNK 64
+#define GDN_MAX_VERIFY_K 16
+#define GDN_FLAG_CHECK_FINITE 1u
+
+typedef struct {
+    int32_t H_k;        /* q/k heads (16 in both model sizes on the page)       */
+    int32_t H_v;        /* v heads, H_v % H_k == 0, H_v/H_k <= 16 (32 or 48)   */
+    float eps;          /* L2 clamp and RMSNorm eps (the page: 1e-6)            */
+    int32_t act_dtype;  /* gdn_dtype of x, z, a_raw, b_raw, conv_state         */
+    int32_t out_dtype;  /* gdn_dtype of out                                     */
+    uint32_t flags;     /* GDN_FLAG_*                                           */
+} gdn_dims;
+
+typedef struct {
+    const float* conv_w;   /* [C][4]   conv1d taps (F32 in the GGUF)           */
+    const float* dt_bias;  /* [H_v]    ssm_dt.bias                             */
+    const float* ssm_a;    /* [H_v]    ssm_a = -exp(A_log), pre-baked          */
+    const float* norm_w;   /* [128]    ssm_norm.weight, multiply-ready          */
+} gdn_weights;
+
+/* Text of a status code (static storage; never NULL). */
+const char* gdn_status_string(gdn_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t gdn_version(void);
+
+/*
+ * gdn_conv_state_init -- set conv_state [n_seq][3][C] to `prefix` (same
+ * layout; copied bit-exactly), or to zeros when prefix is NULL.  A fresh
+ * sequence has no left context, so its conv state is zero; a caller with
+ * fewer than 3 earlier rows left-pads them with zeros in `prefix`.
+ * (The page's definition: conv state = last 3 columns of the fused stream.)
+ */
+gdn_status gdn_conv_state_init(const gdn_dims* dims, int32_t n_seq, void* conv_state,
+                               const void* prefix, gdn_stream_t stream);
+
+/*
+ * gdn_decode_step -- one recurrent step (steps 1-8) for B independent
+ * sequences, one token each.
+ *   x [B][C], z [B][H_v*128], a_raw/b_raw [B][H_v]         (read)
+ *   conv_state [B][3][C], S [B][H_v][128][128]             (read, updated in place)
+ *   out [B][H_v*128], prenorm_out [B][H_v*128] or NULL     (written)
+ * B == 0 is a no-op.  Inputs must not overlap outputs (other than the two
+ * in/out states).
+ */
+gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, int32_t B,
+                           const void* x, const void* z, const void* a_raw, const void* b_raw,
+                           void* conv_state, float* S, void* out, float* prenorm_out,
+                           int32_t* dev_status, gdn_stream_t stream);
+
+/*
+ * gdn_verify_k -- speculative verify: B sequences, K tokens each (1 <= K <=
+ * GDN_MAX_VERIFY_K), token p of sequence b at row b*K + p.  Walks the
+ * recurrence through the K tokens and keeps a state checkpoint after every
+ * position (the page's "Drafting" section: verify-walk rollback from
+ * per-position state planes; the NEXTN.md page's "GDN rollback").
+ *   conv_state [B][3][C], S [B][H_v][128][128]             (read only)
+ *   conv_ckpt [B][K][3][C], S_ckpt [B][K][H_v][128][128]   (written)
+ *   out, prenorm_out [B*K][H_v*128]                        (written)
+ * Checkpoint p is the state after consuming position p; it is bit-identical
+ * to the state that p+1 calls of gdn_decode_step would leave.
+ */
+gdn_status gdn_verify_k(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t K,
+                        const void* x, const void* z, const void* a_raw, const void* b_raw,
+                        const void* conv_state, const float* S, void* conv_ckpt, float* S_ckpt,
+                        void* out, float* prenorm_out, int32_t* dev_status, gdn_stream_t stream);
+
+/*
+ * gdn_commit -- after a verify, make checkpoint accept_len[b]-1 the live state
+ * of sequence b (bit-exact copy into conv_state[b] and S[b]).
+ *   accept_len [B] int32 on the device, each in 1..K; a value outside that
+ *   range leaves the sequence's state untouched.
+ */
+gdn_status gdn_commit(const gdn_dims* dims, int32_t B, int32_t K, const int32_t* accept_len,
+                      const void* conv_ckpt, const float* S_ckpt, void* conv_state, float* S,
+                      gdn_stream_t stream);
+
+/*
+ * gdn_prefill_workspace_bytes -- device scratch that gdn_prefill_chunked needs
+ * for n_seq sequences totalling T_total tokens (0 if none).
+ */
+size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t n_seq, int64_t T_total);
+
+/*
+ * gdn_prefill_chunked -- the layer over n_seq packed sequences in chunked
+ * form (chunk = 64; a sequence's last chunk may be partial).  Mathematically
+ * equal to running gdn_decode_step token by token.
+ *   cu_seqlens_host [n_seq+1]   HOST int32, non-decreasing, [0] = 0
+ *   cu_seqlens_dev  [n_seq+1]   the same values on the device
+ *   x [T][C], z [T][H_v*128], a_raw/b_raw [T][H_v]          (read)
+ *   conv_state [n_seq][3][C], S [n_seq][H_v][128][128]      (updated in place;
+ *                                   read only when zero_init == 0)
+ *   zero_init != 0: the initial conv state and S are taken as zero (fresh
+ *                   sequences) and are not read
+ *   out, prenorm_out [T][H_v*128]                           (written)
+ *   workspace of at least gdn_prefill_workspace_bytes() bytes (may be NULL
+ *   when that is 0).
+ */
+gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, int32_t n_seq,
+                               const int32_t* cu_seqlens_host, const int32_t* cu_seqlens_dev,
+                               const void* x, const void* z, const void* a_raw, const void* b_raw,
+                               void* conv_state, float* S, int32_t zero_init, void* out,
+                               float* prenorm_out, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, gdn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

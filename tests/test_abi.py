@@ -1,0 +1,145 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/gdn.h declares, and its host-side validation rejects bad arguments
+before anything reaches a device (CPU only: no call here launches a kernel)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import gated_deltanet_linear_decode_gb300 as gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("gdn_conv_state_init", "gdn_decode_step", "gdn_prefill_chunked", "gdn_verify_k",
+                     "gdn_commit", "gdn_status_string", "gdn_prefill_workspace_bytes"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib_path = gdn._build.build()
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    lib = gdn.library()
+    for n in declared_functions():
+        assert hasattr(lib, n)
+    assert set(gdn.EXPORTED_SYMBOLS) <= set(declared_functions())
+
+
+def test_header_compiles_as_c():
+    """The header is plain C (no CUDA or C++ types needed)."""
+    src = '#include "gdn.h"\nint main(void){ gdn_dims d; (void)d; return (int)GDN_OK; }\n'
+    r = subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.dirname(HEADER),
+                        "-x", "c", "-"], input=src, text=True, capture_output=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_status_strings_and_version():
+    assert gdn.gdn_status_string(0) == "ok"
+    assert "align" in gdn.gdn_status_string(3)
+    assert gdn.gdn_status_string(99) == "unknown status"
+    assert gdn.gdn_version() >= 100
+
+
+# --- validation paths: every one returns before any CUDA call -------------------------------
+FAKE = 0x10000          # a 16-byte aligned non-null address; never dereferenced on these paths
+
+
+def _call(fn, *args):
+    return getattr(gdn.library(), fn)(*args)
+
+
+def _dims(Hk=16, Hv=32, act=1, out=0, eps=1e-6, flags=0):
+    return gdn.GdnDims(Hk, Hv, eps, act, out, flags)
+
+
+def _w(ptr=FAKE):
+    return gdn.GdnWeights(ptr, ptr + 0x100000, ptr + 0x200000, ptr + 0x300000)
+
+
+def _decode(d, w, B=4, x=FAKE, **kw):
+    args = dict(z=FAKE + 0x1000000, a=FAKE + 0x2000000, b=FAKE + 0x3000000, cs=FAKE + 0x4000000,
+                S=FAKE + 0x5000000, out=FAKE + 0x6000000, pre=None, st=None)
+    args.update(kw)
+    return _call("gdn_decode_step", ctypes.byref(d), ctypes.byref(w) if w is not None else None, B, x,
+                 args["z"], args["a"], args["b"], args["cs"], args["S"], args["out"], args["pre"], args["st"], None)
+
+
+@pytest.mark.parametrize("dims,status", [
+    (None, 1),
+    (_dims(Hk=0), 1), (_dims(Hv=0), 1), (_dims(Hk=16, Hv=40), 1),   # H_v % H_k != 0
+    (_dims(eps=0.0), 1), (_dims(eps=float("nan")), 1), (_dims(act=7), 1), (_dims(out=-1), 1),
+    (_dims(flags=0x80), 1), (_dims(Hk=1, Hv=17), 2),                 # ratio > 16: unsupported
+])
+def test_decode_rejects_bad_dims(dims, status):
+    if dims is None:
+        st = _call("gdn_decode_step", None, ctypes.byref(_w()), 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                   None, None, None)
+    else:
+        st = _decode(dims, _w())
+    assert st == status
+
+
+def test_decode_validation():
+    d = _dims()
+    assert _decode(d, _w(), B=-1) == 1
+    assert _decode(d, _w(), B=0) == 0                 # no-op
+    assert _decode(d, None) == 1                      # no weights
+    assert _decode(d, _w(), x=None) == 1              # null input
+    assert _decode(d, _w(), x=FAKE + 8) == 3          # misaligned
+    assert _decode(d, _w(FAKE + 4)) == 3              # misaligned weights
+    assert _decode(d, _w(), out=FAKE) == 1            # output overlaps x
+    assert _decode(d, _w(), pre=FAKE + 0x6000000) == 1   # prenorm overlaps out
+
+
+def test_verify_and_commit_validation():
+    d = _dims()
+    w = _w()
+    L = gdn.library()
+    base = [FAKE * (i + 1) * 0x100 for i in range(12)]
+    # K out of range
+    for K in (0, 17):
+        assert L.gdn_verify_k(ctypes.byref(d), ctypes.byref(w), 2, K, *base[:10], None, None) == 1
+    # S_ckpt overlapping S
+    args = base[:10]
+    args[7] = args[5]
+    assert L.gdn_verify_k(ctypes.byref(d), ctypes.byref(w), 2, 3, *args, None, None) == 1
+    assert L.gdn_commit(ctypes.byref(d), 2, 0, *base[:5], None) == 1
+    assert L.gdn_commit(ctypes.byref(d), 0, 3, *base[:5], None) == 0
+    assert L.gdn_commit(ctypes.byref(d), 2, 3, base[0], base[1], base[2], base[3] + 4, base[4], None) == 3
+
+
+def test_prefill_validation():
+    d = _dims(Hk=16, Hv=48)
+    w = _w()
+    L = gdn.library()
+    P = [FAKE * (i + 1) * 0x1000 for i in range(12)]
+
+    def call(cu, n=None, **kw):
+        arr = (ctypes.c_int32 * len(cu))(*cu)
+        n = len(cu) - 1 if n is None else n
+        a = dict(cu_dev=P[0], x=P[1], z=P[2], a=P[3], b=P[4], cs=P[5], S=P[6], out=P[7])
+        a.update(kw)
+        return L.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(w), n, arr, a["cu_dev"], a["x"], a["z"], a["a"],
+                                     a["b"], a["cs"], a["S"], 0, a["out"], None, None, 0, None, None)
+    assert call([0, 5], n=-1) == 1
+    assert call([0, 5], n=0) == 0
+    assert call([1, 5]) == 1                 # must start at 0
+    assert call([0, 5, 3]) == 1              # decreasing
+    assert call([0, 5], x=None) == 1
+    assert call([0, 5], x=P[1] + 2) == 3
+    assert call([0, 5], cu_dev=None) == 1
+    assert gdn.gdn_prefill_workspace_bytes(d, 1, 8192) >= 0
