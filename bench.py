@@ -362,14 +362,14 @@ def _max_over_ranks(v, world):
 
 
 # ------------------------------------------------------------------ the oracle (CPU)
-def oracle_step_sample(prefill_tokens=64, seed_cases=None):
-    """One bounded sample of the step on the host cores: the prefill's first
-    `prefill_tokens` tokens (all 48 heads), the full B=64 decode step and the
-    full B=64 K=3 verify walk (with checkpoints).  Returns (seconds, seconds
-    extrapolated to the whole step)."""
+def oracle_step(cases, prefill_tokens=None):
+    """One step of the workload through the CPU oracle (fp64, OpenMP): the
+    prefill (all 48 heads; its first `prefill_tokens` tokens when given), the
+    B=64 decode step and the B=64 K=3 verify walk with checkpoints.
+    Returns (seconds used, seconds extrapolated to the whole step)."""
     import oracle
-    pc, dc, vc = seed_cases
-    n = prefill_tokens
+    pc, dc, vc = cases
+    n = pc.T if prefill_tokens is None else prefill_tokens
     t0 = time.perf_counter()
     oracle.forward(pc.Hk, pc.Hv, pc.x[:n], pc.z[:n], pc.a_raw[:n], pc.b_raw[:n], pc.conv_w, pc.dt_bias, pc.ssm_a,
                    pc.norm_w, pc.conv0, pc.S0, cu_seqlens=[0, n])
@@ -380,22 +380,24 @@ def oracle_step_sample(prefill_tokens=64, seed_cases=None):
     oracle.verify_checkpoints(vc.Hk, vc.Hv, vc.x, vc.z, vc.a_raw, vc.b_raw, vc.conv_w, vc.dt_bias, vc.ssm_a,
                               vc.norm_w, vc.conv0, vc.S0, vc.K)
     t3 = time.perf_counter()
-    full = (t1 - t0) * pc.T / n + (t2 - t1) + (t3 - t2)
-    return t3 - t0, full
+    return t3 - t0, (t1 - t0) * pc.T / n + (t2 - t1) + (t3 - t2)
 
 
-def cpu_baseline(target_s=15.0):
+def cpu_baseline(min_seconds=10.0):
+    """The oracle, as it stands, on the host cores: whole steps of the workload,
+    repeated until at least `min_seconds` of CPU work."""
     import oracle
     oracle.build()
     cases = (gdn_inputs.prefill_t8192(), gdn_inputs.decode_b64(), gdn_inputs.verify_b64_k3())
     tok = cases[0].T + cases[1].N + cases[2].N * cases[2].K
-    used, full = oracle_step_sample(64, cases)          # calibrate
-    n = int(min(cases[0].T, max(64, 64 * target_s / max(used, 1e-3))))
-    used, full = oracle_step_sample(n, cases)
-    return {"value": tok / full, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"fp64 C oracle on the host: prefill tokens 0..{n - 1} of T=8192 (48 heads) + the full "
-                      f"B=64 decode step + the full B=64 K=3 verify walk; the prefill part scaled by 8192/{n} "
-                      f"({used:.1f} s of CPU work)", "seconds": used}
+    reps, used = 0, 0.0
+    while used < min_seconds or reps == 0:
+        u, _ = oracle_step(cases)
+        used += u
+        reps += 1
+    return {"value": tok * reps / used, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"fp64 C oracle, whole steps of the workload (prefill T=8192 all 48 heads + B=64 decode + "
+                      f"B=64 K=3 verify) x{reps}, {used:.1f} s of CPU work", "seconds": used}
 
 
 def run_reference(args, rank, world):
@@ -405,12 +407,12 @@ def run_reference(args, rank, world):
     oracle.build()
     cases = (gdn_inputs.prefill_t8192(), gdn_inputs.decode_b64(), gdn_inputs.verify_b64_k3())
     tok = cases[0].T + cases[1].N + cases[2].N * cases[2].K
-    n = 32
+    n = 512
     for _ in range(args.warmup):
-        oracle_step_sample(n, cases)
+        oracle_step(cases, n)
     fulls, used = [], 0.0
     for _ in range(args.steps):
-        u, f = oracle_step_sample(n, cases)
+        u, f = oracle_step(cases, n)
         fulls.append(f)
         used += u
     tot = sum(fulls)

@@ -41,7 +41,7 @@ __device__ __forceinline__ float conv4(float4 w, float x0, float x1, float x2, f
 }
 
 #ifndef GDN_REC_MIN_BLOCKS
-#define GDN_REC_MIN_BLOCKS 1
+#define GDN_REC_MIN_BLOCKS 8   // 8 CTAs of 128 threads per SM (64 registers)
 #endif
 
 template <typename Tact, typename Tout, int RPC>
