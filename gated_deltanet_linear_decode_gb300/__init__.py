@@ -30,6 +30,7 @@ __all__ = [
 HEAD_DIM = 128
 GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_CHECK_FINITE = 1
+GDN_FLAG_PREFILL_FP32 = 2
 
 EXPORTED_SYMBOLS = (
     "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step",
@@ -109,8 +110,9 @@ def _dt(t: torch.dtype) -> int:
 
 
 def make_dims(Hk: int, Hv: int, act_dtype=torch.bfloat16, out_dtype=torch.float32, eps: float = 1e-6,
-              check_finite: bool = False) -> GdnDims:
-    return GdnDims(Hk, Hv, eps, _dt(act_dtype), _dt(out_dtype), GDN_FLAG_CHECK_FINITE if check_finite else 0)
+              check_finite: bool = False, prefill_fp32: bool = False) -> GdnDims:
+    flags = (GDN_FLAG_CHECK_FINITE if check_finite else 0) | (GDN_FLAG_PREFILL_FP32 if prefill_fp32 else 0)
+    return GdnDims(Hk, Hv, eps, _dt(act_dtype), _dt(out_dtype), flags)
 
 
 @dataclass

@@ -49,7 +49,7 @@ gdn_status check_dims(const gdn_dims* d) {
     if ((d->act_dtype != GDN_F32 && d->act_dtype != GDN_BF16) ||
         (d->out_dtype != GDN_F32 && d->out_dtype != GDN_BF16))
         return GDN_E_INVALID_ARG;
-    if (d->flags & ~GDN_FLAG_CHECK_FINITE) return GDN_E_INVALID_ARG;
+    if (d->flags & ~(GDN_FLAG_CHECK_FINITE | GDN_FLAG_PREFILL_FP32)) return GDN_E_INVALID_ARG;
     if (d->H_v / d->H_k > 16) return GDN_E_UNSUPPORTED;
     return GDN_OK;
 }

@@ -33,6 +33,12 @@ __device__ __forceinline__ float softplusf_(float x) {
 }
 __device__ __forceinline__ float siluf_(float x) { return x / (1.0f + expf(-x)); }
 
+// Non-finite test on the bit pattern (exponent all ones): integer-only, so no
+// floating-point assumption of the compiler can fold it away.
+__device__ __forceinline__ bool nonfinite_bits(float v) {
+    return (__float_as_uint(v) & 0x7f800000u) == 0x7f800000u;
+}
+
 // ---------------------------------------------------------------- warp reductions
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -9,6 +9,7 @@
 namespace gdn {
 
 constexpr uint32_t kFlagCheckFinite = 1u;
+constexpr uint32_t kFlagForceSimt = 2u;   // GDN_FLAG_PREFILL_FP32
 
 // Recurrent walk (decode step when K == 1 and the outputs alias the states;
 // speculative verify when the outputs are the checkpoint planes).

@@ -232,7 +232,7 @@ prefill_simt_kernel(const PrefillParams p) {
                 const float y = o[u] * rs * p.norm_w[j] * siluf_(zz);
                 st_out(static_cast<Tout*>(p.out) + oi, y);
                 if (p.prenorm) p.prenorm[oi] = o[u];
-                if (p.flags & kFlagCheckFinite) bad |= !isfinite(y);
+                if (p.flags & kFlagCheckFinite) bad |= nonfinite_bits(y);
             }
         }
     }
@@ -241,7 +241,7 @@ prefill_simt_kernel(const PrefillParams p) {
     for (int e = tid; e < kD * kD; e += kThreads) {
         const float v = Ss[(e >> 7) * kLd + (e & 127)];
         Sg[e] = v;
-        if (p.flags & kFlagCheckFinite) bad_s |= !isfinite(v);
+        if (p.flags & kFlagCheckFinite) bad_s |= nonfinite_bits(v);
     }
     if (p.dev_status && (p.flags & kFlagCheckFinite)) {
         const int st = (__any_sync(0xffffffffu, bad_s) ? 1 : 0) | (__any_sync(0xffffffffu, bad) ? 2 : 0);
@@ -279,8 +279,6 @@ cudaError_t launch_prefill_simt_t(const PrefillParams& p, cudaStream_t stream) {
                                          static_cast<int>(kSimtSmemBytes));
     if (e != cudaSuccess) return e;
     k<<<static_cast<unsigned>(p.n_seq) * p.Hv, kThreads, kSimtSmemBytes, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    conv_state_finalize_kernel<Tact><<<dim3((p.C + 255) / 256, p.n_seq), 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -292,10 +290,23 @@ cudaError_t launch_prefill_simt(const PrefillParams& p, int act_dtype, int out_d
                           : launch_prefill_simt_t<float, float>(p, stream);
 }
 
+cudaError_t launch_prefill_tc(const PrefillParams& p, int out_dtype, cudaStream_t stream);
+
 size_t prefill_workspace_bytes(int, int, int, long long) { return 0; }
 
+// bf16 activations take the tensor-core kernel; fp32 activations (whose 1e-5
+// tolerance needs fp32 products) take the CUDA-core kernel.  Either is
+// followed by the conv-state update, which must run after every CTA has read
+// the old rows.
 cudaError_t launch_prefill(const PrefillParams& p, int act_dtype, int out_dtype, cudaStream_t stream) {
-    return launch_prefill_simt(p, act_dtype, out_dtype, stream);
+    cudaError_t e = act_dtype == 1 && !(p.flags & kFlagForceSimt) ? launch_prefill_tc(p, out_dtype, stream)
+                                                                   : launch_prefill_simt(p, act_dtype, out_dtype, stream);
+    if (e != cudaSuccess) return e;
+    if (act_dtype == 1)
+        conv_state_finalize_kernel<__nv_bfloat16><<<dim3((p.C + 255) / 256, p.n_seq), 256, 0, stream>>>(p);
+    else
+        conv_state_finalize_kernel<float><<<dim3((p.C + 255) / 256, p.n_seq), 256, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace gdn

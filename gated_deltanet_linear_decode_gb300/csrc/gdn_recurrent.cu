@@ -170,7 +170,8 @@ recurrent_kernel(const RecParams p) {
             for (int rr = 0; rr < 8; ++rr) {
                 st_f4(Sout + static_cast<size_t>(warp * 8 + rr) * kD + 4 * lane, s[rr]);
                 if (p.flags & kFlagCheckFinite)
-                    bad_state |= !(isfinite(s[rr].x) && isfinite(s[rr].y) && isfinite(s[rr].z) && isfinite(s[rr].w));
+                    bad_state |= nonfinite_bits(s[rr].x) | nonfinite_bits(s[rr].y) | nonfinite_bits(s[rr].z) |
+                                 nonfinite_bits(s[rr].w);
             }
         }
         float ps = 0.f;
@@ -198,7 +199,7 @@ recurrent_kernel(const RecParams p) {
             const size_t oi = row * HvD + h * kD + j0 + tid;
             st_out(static_cast<Tout*>(p.out) + oi, y);
             if (p.prenorm) p.prenorm[oi] = ov;
-            if (p.flags & kFlagCheckFinite) bad_out |= !isfinite(y);
+            if (p.flags & kFlagCheckFinite) bad_out |= nonfinite_bits(y);
         }
         // ---- conv state after token t: window (w1, w2, x_t); raw values, bit-exact
         Tact* cout = static_cast<Tact*>(p.conv_out) + static_cast<size_t>(b) * p.conv_out_b +

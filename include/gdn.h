@@ -82,6 +82,10 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 #define GDN_CHUNK 64
 #define GDN_MAX_VERIFY_K 16
 #define GDN_FLAG_CHECK_FINITE 1u
+/* gdn_prefill_chunked with bf16 activations: use the fp32 CUDA-core chunk
+ * kernel instead of the tensor-core kernel (fp32 products end to end; slower).
+ * fp32 activations always take that kernel. */
+#define GDN_FLAG_PREFILL_FP32 2u
 
 typedef struct {
     int32_t H_k;        /* q/k heads (16 in both model sizes on the page)       */

@@ -22,8 +22,9 @@ def weights(case):
     return gdn.make_weights(case.conv_w, case.dt_bias, case.ssm_a, case.norm_w)
 
 
-def dims(case, out_dtype=torch.float32, check_finite=False):
-    return gdn.make_dims(case.Hk, case.Hv, case.act_dtype, out_dtype, check_finite=check_finite)
+def dims(case, out_dtype=torch.float32, check_finite=False, prefill_fp32=False):
+    return gdn.make_dims(case.Hk, case.Hv, case.act_dtype, out_dtype, check_finite=check_finite,
+                         prefill_fp32=prefill_fp32)
 
 
 def half_ulp_bf16(ref):

@@ -15,8 +15,9 @@ from tests import gpu_util as G
 pytestmark = pytest.mark.gpu
 
 
-def run_prefill(c, zero_init=False, out_dtype=torch.float32, conv=None, S=None, check_finite=False):
-    d, w = G.dims(c, out_dtype, check_finite), G.weights(c)
+def run_prefill(c, zero_init=False, out_dtype=torch.float32, conv=None, S=None, check_finite=False,
+                prefill_fp32=False):
+    d, w = G.dims(c, out_dtype, check_finite, prefill_fp32), G.weights(c)
     cu = c.cu_seqlens.to(torch.int32).contiguous()
     conv = G.dev(c.conv0 if conv is None else conv)
     S = G.dev(c.S0 if S is None else S)
@@ -62,10 +63,12 @@ def test_tiny_fp32_both_forms():
     assert G.conv_bits_equal(conv_d, ref.conv_state, torch.float32)
 
 
-def test_prefill_t8192_full_size():
-    """The prefill workload at full size (T=8192, 16/48, bf16, zero state)."""
+@pytest.mark.parametrize("fp32_path", [False, True], ids=["tensor_core", "cuda_core"])
+def test_prefill_t8192_full_size(fp32_path):
+    """The prefill workload at full size (T=8192, 16/48, bf16, zero state),
+    through the tensor-core kernel and the fp32 CUDA-core kernel."""
     c = gdn_inputs.prefill_t8192()
-    out, pre, conv, S, _ = run_prefill(c, zero_init=True)
+    out, pre, conv, S, _ = run_prefill(c, zero_init=True, prefill_fp32=fp32_path)
     ref = oracle_run(c)
     G.assert_out_close(out, ref.out, c.act_dtype)
     G.assert_state_close(S, ref.S, c.act_dtype)
@@ -126,6 +129,19 @@ def test_varlen_t65536_sampled_sequences():
         G.assert_out_close(out[t0:t1], ref.out, c.act_dtype)
         G.assert_state_close(S[s:s + 1], ref.S, c.act_dtype)
         assert G.conv_bits_equal(conv[s:s + 1], ref.conv_state, c.act_dtype)
+
+
+@pytest.mark.parametrize("Hk,Hv,lengths", [(1, 1, [64]), (1, 3, [1]), (4, 8, [127, 65]), (2, 32, [300]),
+                                            (3, 3, [5, 200, 64, 63])])
+def test_tensor_core_prefill_shapes(Hk, Hv, lengths):
+    """Tensor-core prefill across head ratios 1..16, one-token and
+    whole-chunk sequences, against the oracle."""
+    c = gdn_inputs.make_case("tcs", Hk=Hk, Hv=Hv, lengths=lengths, seed=Hk * 31 + Hv + sum(lengths))
+    out, pre, conv, S, _ = run_prefill(c)
+    ref = oracle_run(c)
+    G.assert_out_close(out, ref.out, c.act_dtype)
+    G.assert_state_close(S, ref.S, c.act_dtype)
+    assert G.conv_bits_equal(conv, ref.conv_state, c.act_dtype)
 
 
 def test_prefill_bf16_output():
