@@ -85,6 +85,22 @@ int rows_per_cta(int r) {
 
 gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_E_CUDA; }
 
+// Streaming (persistent, one CTA per SM) recurrent kernel when there are at
+// least two (sequence, q/k-group) items per SM and its stages fit in shared
+// memory; the cluster kernel otherwise.  The choice depends on B, H_k and K
+// only, never on the data.
+bool use_stream_kernel(int B, int Hk, int K, int act_dtype, int* grid) {
+    int dev = 0, sms = 0, smem = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
+    const long long items = static_cast<long long>(B) * Hk;
+    if (items < 2LL * sms) return false;
+    if (gdn::recurrent_stream_smem(K, act_dtype) > static_cast<size_t>(smem)) return false;
+    *grid = sms;
+    return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -162,6 +178,10 @@ static gdn_status recurrent_common(const gdn_dims* dims, const gdn_weights* w, i
         p.S_out_b = static_cast<long long>(Hv) * kD * kD; p.S_out_p = 0;
     }
     p.out = out; p.prenorm = prenorm_out; p.dev_status = dev_status;
+    int grid = 0;
+    if (use_stream_kernel(B, Hk, K, dims->act_dtype, &grid))
+        return cuda_status(gdn::launch_recurrent_stream(p, dims->act_dtype, dims->out_dtype, grid,
+                                                        reinterpret_cast<cudaStream_t>(stream)));
     return cuda_status(gdn::launch_recurrent(p, dims->act_dtype, dims->out_dtype, rpc,
                                              reinterpret_cast<cudaStream_t>(stream)));
 }

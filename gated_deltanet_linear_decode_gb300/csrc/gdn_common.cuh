@@ -46,6 +46,24 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Transposed butterfly reduction: each lane holds 32 partial sums v[0..31];
+// afterwards v[0] of lane l is the sum over all 32 lanes of partial l
+// (31 shuffles for 32 sums instead of 5 per sum).
+__device__ __forceinline__ float reduce32_transposed(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float send = up ? v[i] : v[i + o];
+            const float keep = up ? v[i + o] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
+}
+
 // ---------------------------------------------------------------- clusters (PTX ISA: barrier.cluster, mapa, ld.shared::cluster)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

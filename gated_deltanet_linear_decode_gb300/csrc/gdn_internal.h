@@ -80,6 +80,8 @@ cudaError_t launch_prefill(const PrefillParams& p, int act_dtype, int out_dtype,
 
 cudaError_t launch_recurrent(const RecParams& p, int act_dtype, int out_dtype, int rows_per_cta,
                              cudaStream_t stream);
+size_t recurrent_stream_smem(int K, int act_dtype);
+cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_dtype, int grid, cudaStream_t stream);
 cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream);
 cudaError_t launch_conv_init(void* dst, const void* src, size_t bytes, cudaStream_t stream);
 

@@ -26,7 +26,8 @@
 // blocked forward substitution on the CUDA cores in fp32; Gam is accumulated
 // in fp64 so the decay weights keep fp32 relative accuracy.
 //
-// One CTA (4 warps, thread j <-> tensor-memory lane j) per (sequence, v-head);
+// One CTA of 8 warps per (sequence, v-head): warp w reads TMEM lane quarter
+// w%4 (thread <-> state row j) and the column half w/4;
 // the phases of a chunk run in order, each MMA group retired through one
 // mbarrier (waits are bounded and report a timeout through dev_status bit 4).
 #include "gdn_common.cuh"
@@ -37,7 +38,7 @@ namespace gdn {
 
 namespace {
 
-constexpr int kTcThreads = 128;
+constexpr int kTcThreads = 256;   // 8 warps; warps w and w+4 share TMEM lane quarter w%4
 
 // shared memory map (bytes)
 constexpr uint32_t kQKs = 0;            // [Q;K] hi at +0, lo at +32768   (128 rows x 128, canonical)
@@ -71,6 +72,10 @@ constexpr int kWaitLimit = 1 << 22;
 __device__ __forceinline__ float conv4(float4 w, float x0, float x1, float x2, float cur) {
     return fmaf(w.w, cur, fmaf(w.z, x2, fmaf(w.y, x1, w.x * x0)));
 }
+
+// SiLU with the fast exponential and a correctly rounded reciprocal (relative
+// error ~1e-6, far inside the output tolerance).
+__device__ __forceinline__ float silu_fast(float x) { return x * __frcp_rn(1.0f + __expf(-x)); }
 
 __device__ __forceinline__ void bf16x8_to_f32(uint4 u, float* f) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -144,7 +149,10 @@ prefill_tc_kernel(const PrefillParams p) {
 
     float* beta_s = reinterpret_cast<float*>(sm + kMisc);
     float* g_s = beta_s + 64;
-    double* gam_s = reinterpret_cast<double*>(sm + kMisc + 512);
+    // Gam_t as an unevaluated sum ghi + glo of two floats (formed from an fp64
+    // scan), so Gam_t - Gam_r keeps fp32 relative accuracy with fp32 arithmetic.
+    float* ghi_s = reinterpret_cast<float*>(sm + kMisc + 512);
+    float* glo_s = reinterpret_cast<float*>(sm + kMisc + 768);
     float* egam_s = reinterpret_cast<float*>(sm + kMisc + 1024);
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sm + kMisc + 1280);
     uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + kMisc + 1288);
@@ -161,7 +169,10 @@ prefill_tc_kernel(const PrefillParams p) {
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_base_s;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);   // this warp's lane quarter
+    const int quarter = warp & 3, chalf = warp >> 2;
+    const int row = quarter * 32 + lane;                                          // TMEM lane = state row j
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);      // this warp's lane quarter
+    auto dgam = [&](int t, int r) { return (ghi_s[t] - ghi_s[r]) + (glo_s[t] - glo_s[r]); };
     uint32_t phase = 0;
     bool abort = false;
 
@@ -177,11 +188,12 @@ prefill_tc_kernel(const PrefillParams p) {
     {
         float v[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * chalf + cc;
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
                 float4 f = p.zero_init ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                       : *reinterpret_cast<const float4*>(Sg + tid * kD + 32 * c + i);
+                                       : *reinterpret_cast<const float4*>(Sg + row * kD + 32 * c + i);
                 v[i] = f.x; v[i + 1] = f.y; v[i + 2] = f.z; v[i + 3] = f.w;
             }
             tc::tmem_st32(tl + kColS + 32 * c, v);
@@ -246,12 +258,16 @@ prefill_tc_kernel(const PrefillParams p) {
                 if (lane >= o) run += up;
             }
             const double base = run - (g0 + g1);
-            gam_s[2 * lane] = base + g0;
-            gam_s[2 * lane + 1] = run;
-            egam_s[2 * lane] = expf(static_cast<float>(base + g0));
-            egam_s[2 * lane + 1] = expf(static_cast<float>(run));
+            const double G0 = base + g0, G1 = run;
+            const float h0 = static_cast<float>(G0), h1 = static_cast<float>(G1);
+            ghi_s[2 * lane] = h0;
+            glo_s[2 * lane] = static_cast<float>(G0 - static_cast<double>(h0));
+            ghi_s[2 * lane + 1] = h1;
+            glo_s[2 * lane + 1] = static_cast<float>(G1 - static_cast<double>(h1));
+            egam_s[2 * lane] = __expf(h0);
+            egam_s[2 * lane + 1] = __expf(h1);
         }
-        for (int t = warp; t < kChunk; t += 4) {
+        for (int t = warp; t < kChunk; t += 8) {
             const uint32_t qrow = is_q ? t : 64 + t;
             if (t < n) {
                 float win[4][8], winv[4][4];
@@ -264,7 +280,7 @@ prefill_tc_kernel(const PrefillParams p) {
                 float val[8], ss = 0.f;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    val[i] = siluf_(conv4(wqk[i], win[0][i], win[1][i], win[2][i], win[3][i]));
+                    val[i] = silu_fast(conv4(wqk[i], win[0][i], win[1][i], win[2][i], win[3][i]));
                     ss = fmaf(val[i], val[i], ss);
                 }
 #pragma unroll
@@ -279,7 +295,7 @@ prefill_tc_kernel(const PrefillParams p) {
                 *reinterpret_cast<uint4*>(sm + kQKs + 32768 + o) = lo;
                 float vv[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) vv[i] = siluf_(conv4(wv[i], winv[0][i], winv[1][i], winv[2][i], winv[3][i]));
+                for (int i = 0; i < 4; ++i) vv[i] = silu_fast(conv4(wv[i], winv[0][i], winv[1][i], winv[2][i], winv[3][i]));
                 uint2 vh, vl;
                 tc::split4(vv, vh, vl);
                 const uint32_t ov = tc::cl_off(t, 4 * lane, 64);
@@ -296,7 +312,7 @@ prefill_tc_kernel(const PrefillParams p) {
         }
         tc::fence_proxy_async();
         __syncthreads();
-        const double gl = gam_s[n - 1];
+        const int nl = n - 1;   // last token of the chunk
 
         // ===== phase b: [Q;K] K^T  (3 passes, K = 128)
         if (tid == 0) {
@@ -319,40 +335,38 @@ prefill_tc_kernel(const PrefillParams p) {
             float* Tf = reinterpret_cast<float*>(sm + kTf);
             float* Xf = reinterpret_cast<float*>(sm + kXf);
             float v[32];
-            const int t = tid & 63;
-            for (int half = 0; half < 2; ++half) {
-                tc::tmem_ld32(tl + kColQK + 32 * half, v);
-                if (tid < 64) {           // rows of Q K^T -> P
+            const int t = row & 63;
+            tc::tmem_ld32(tl + kColQK + 32 * chalf, v);
+            if (row < 64) {           // rows of Q K^T -> P
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
                     float pv[8];
 #pragma unroll
-                    for (int g8 = 0; g8 < 4; ++g8) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int r = 32 * half + 8 * g8 + i;
-                            pv[i] = r <= t ? expf(static_cast<float>(gam_s[t] - gam_s[r])) * v[8 * g8 + i] : 0.f;
-                        }
-                        uint4 hi, lo;
-                        tc::split8(pv, hi, lo);
-                        const uint32_t o = tc::cl_off(t, 32 * half + 8 * g8, 64);
-                        *reinterpret_cast<uint4*>(sm + kPs + o) = hi;
-                        *reinterpret_cast<uint4*>(sm + kPs + 8192 + o) = lo;
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = 32 * chalf + 8 * g8 + i;
+                        pv[i] = r <= t ? __expf(dgam(t, r)) * v[8 * g8 + i] : 0.f;
                     }
-                } else {                  // rows of K K^T -> A
+                    uint4 hi, lo;
+                    tc::split8(pv, hi, lo);
+                    const uint32_t o = tc::cl_off(t, 32 * chalf + 8 * g8, 64);
+                    *reinterpret_cast<uint4*>(sm + kPs + o) = hi;
+                    *reinterpret_cast<uint4*>(sm + kPs + 8192 + o) = lo;
+                }
+            } else {                  // rows of K K^T -> A
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int r = 32 * half + i;
-                        Af[t * 65 + r] = r < t ? beta_s[t] * expf(static_cast<float>(gam_s[t] - gam_s[r])) * v[i] : 0.f;
-                    }
+                for (int i = 0; i < 32; ++i) {
+                    const int r = 32 * chalf + i;
+                    Af[t * 65 + r] = r < t ? beta_s[t] * __expf(dgam(t, r)) * v[i] : 0.f;
                 }
             }
             tc::fence_before_sync();
             __syncthreads();
             unit_lower_inverse(Af, Tf, Xf);
-            // T diag(beta) and T diag(beta e^Gam): thread -> row tid/2, 32 columns
+            // T diag(beta) and T diag(beta e^Gam): thread -> row tid/4, 16 columns
             {
-                const int tr = tid >> 1, r0 = (tid & 1) * 32;
+                const int tr = tid >> 2, r0 = (tid & 3) * 16;
 #pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
+                for (int g8 = 0; g8 < 2; ++g8) {
                     float a8[8], b8[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
@@ -395,23 +409,22 @@ prefill_tc_kernel(const PrefillParams p) {
         // ===== phase e: W^T -> fp16 operand; S -> fp16 hi/lo operand and S <- e^{Gam_n} S
         {
             float v[32];
-            for (int half = 0; half < 2; ++half) {
-                tc::tmem_ld32(tl + kColW + 32 * half, v);
+            tc::tmem_ld32(tl + kColW + 32 * chalf, v);
 #pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
-                    uint4 hi, lo;
-                    tc::split8(v + 8 * g8, hi, lo);
-                    *reinterpret_cast<uint4*>(sm + kWh + tc::cl_off(tid, 32 * half + 8 * g8, 128)) = hi;
-                }
+            for (int g8 = 0; g8 < 4; ++g8) {
+                uint4 hi, lo;
+                tc::split8(v + 8 * g8, hi, lo);
+                *reinterpret_cast<uint4*>(sm + kWh + tc::cl_off(row, 32 * chalf + 8 * g8, 128)) = hi;
             }
-            const float egl = expf(static_cast<float>(gl));
-            for (int c = 0; c < 4; ++c) {
+            const float egl = egam_s[nl];
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * chalf + cc;
                 tc::tmem_ld32(tl + kColS + 32 * c, v);
 #pragma unroll
                 for (int g8 = 0; g8 < 4; ++g8) {
                     uint4 hi, lo;
                     tc::split8(v + 8 * g8, hi, lo);
-                    const uint32_t o = tc::cl_off(tid, 32 * c + 8 * g8, 128);
+                    const uint32_t o = tc::cl_off(row, 32 * c + 8 * g8, 128);
                     *reinterpret_cast<uint4*>(sm + kSs + o) = hi;
                     *reinterpret_cast<uint4*>(sm + kSs + 32768 + o) = lo;
                 }
@@ -446,25 +459,23 @@ prefill_tc_kernel(const PrefillParams p) {
         // ===== phase g: D^T -> fp16 operands (plain and scaled by e^{Gam_n - Gam_t})
         {
             float v[32];
-            for (int half = 0; half < 2; ++half) {
-                tc::tmem_ld32(tl + kColDU + 32 * half, v);
+            tc::tmem_ld32(tl + kColDU + 32 * chalf, v);
 #pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
-                    float sc[8];
+            for (int g8 = 0; g8 < 4; ++g8) {
+                float sc[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int t = 32 * half + 8 * g8 + i;
-                        sc[i] = v[8 * g8 + i] * expf(static_cast<float>(gl - gam_s[t]));
-                    }
-                    uint4 hi, lo;
-                    const uint32_t o = tc::cl_off(tid, 32 * half + 8 * g8, 128);
-                    tc::split8(v + 8 * g8, hi, lo);
-                    *reinterpret_cast<uint4*>(sm + kA1 + o) = hi;
-                    *reinterpret_cast<uint4*>(sm + kA1 + 16384 + o) = lo;
-                    tc::split8(sc, hi, lo);
-                    *reinterpret_cast<uint4*>(sm + kA2 + o) = hi;
-                    *reinterpret_cast<uint4*>(sm + kA2 + 16384 + o) = lo;
+                for (int i = 0; i < 8; ++i) {
+                    const int t = 32 * chalf + 8 * g8 + i;
+                    sc[i] = v[8 * g8 + i] * __expf(dgam(nl, t));
                 }
+                uint4 hi, lo;
+                const uint32_t o = tc::cl_off(row, 32 * chalf + 8 * g8, 128);
+                tc::split8(v + 8 * g8, hi, lo);
+                *reinterpret_cast<uint4*>(sm + kA1 + o) = hi;
+                *reinterpret_cast<uint4*>(sm + kA1 + 16384 + o) = lo;
+                tc::split8(sc, hi, lo);
+                *reinterpret_cast<uint4*>(sm + kA2 + o) = hi;
+                *reinterpret_cast<uint4*>(sm + kA2 + 16384 + o) = lo;
             }
             tc::fence_proxy_async();
             tc::fence_before_sync();
@@ -499,20 +510,18 @@ prefill_tc_kernel(const PrefillParams p) {
                                                                   static_cast<size_t>(t0 + c0 + t) * HvD + h * kD + off);
             }
             float v1[32], v2[32];
-            for (int half = 0; half < 2; ++half) {
-                tc::tmem_ld32(tl + kColO1 + 32 * half, v1);
-                tc::tmem_ld32(tl + kColO2 + 32 * half, v2);
+            tc::tmem_ld32(tl + kColO1 + 32 * chalf, v1);
+            tc::tmem_ld32(tl + kColO2 + 32 * chalf, v2);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int t = 32 * half + i;
-                    OT[t * kLdO + tid] = fmaf(egam_s[t], v1[i], v2[i]) * kInvSqrtD;
-                }
+            for (int i = 0; i < 32; ++i) {
+                const int t = 32 * chalf + i;
+                OT[t * kLdO + row] = fmaf(egam_s[t], v1[i], v2[i]) * kInvSqrtD;
             }
             tc::cp_async_drain();
             tc::fence_before_sync();
             __syncthreads();
             if (*err_s) abort = true;
-            for (int t = warp; t < n; t += 4) {
+            for (int t = warp; t < n; t += 8) {
                 const float4 o4 = *reinterpret_cast<const float4*>(OT + t * kLdO + 4 * lane);
                 float ss = o4.x * o4.x + o4.y * o4.y + o4.z * o4.z + o4.w * o4.w;
                 ss = warp_sum(ss);
@@ -521,8 +530,8 @@ prefill_tc_kernel(const PrefillParams p) {
                 float zf[4];
                 bf16x4_to_f32(*reinterpret_cast<const uint2*>(sm + kZs + t * 256 + 8 * lane), zf);
                 const float4 w4 = *reinterpret_cast<const float4*>(p.norm_w + 4 * lane);
-                const float y[4] = {o4.x * rs * w4.x * siluf_(zf[0]), o4.y * rs * w4.y * siluf_(zf[1]),
-                                    o4.z * rs * w4.z * siluf_(zf[2]), o4.w * rs * w4.w * siluf_(zf[3])};
+                const float y[4] = {o4.x * rs * w4.x * silu_fast(zf[0]), o4.y * rs * w4.y * silu_fast(zf[1]),
+                                    o4.z * rs * w4.z * silu_fast(zf[2]), o4.w * rs * w4.w * silu_fast(zf[3])};
                 Tout* out = static_cast<Tout*>(p.out) + oi;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -539,11 +548,12 @@ prefill_tc_kernel(const PrefillParams p) {
     bool bad_s = false;
     {
         float v[32];
-        for (int c = 0; c < 4; ++c) {
+        for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * chalf + cc;
             tc::tmem_ld32(tl + kColS + 32 * c, v);
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
-                *reinterpret_cast<float4*>(Sg + tid * kD + 32 * c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                *reinterpret_cast<float4*>(Sg + row * kD + 32 * c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
                 if (p.flags & kFlagCheckFinite)
                     bad_s |= nonfinite_bits(v[i]) | nonfinite_bits(v[i + 1]) | nonfinite_bits(v[i + 2]) |
                              nonfinite_bits(v[i + 3]);

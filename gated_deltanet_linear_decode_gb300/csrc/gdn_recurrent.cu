@@ -102,7 +102,7 @@ recurrent_kernel(const RecParams p) {
     }
     const float a_dt = p.dt_bias[h];
     const float a_ssm = p.ssm_a[h];
-    bool bad_state = false, bad_out = false;
+    int* const status = (p.dev_status && (p.flags & kFlagCheckFinite)) ? p.dev_status + b * p.Hv + h : nullptr;
 
     for (int t = 0; t < p.K; ++t) {
         const size_t row = static_cast<size_t>(b) * p.K + t;      // token row
@@ -169,9 +169,9 @@ recurrent_kernel(const RecParams p) {
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr) {
                 st_f4(Sout + static_cast<size_t>(warp * 8 + rr) * kD + 4 * lane, s[rr]);
-                if (p.flags & kFlagCheckFinite)
-                    bad_state |= nonfinite_bits(s[rr].x) | nonfinite_bits(s[rr].y) | nonfinite_bits(s[rr].z) |
-                                 nonfinite_bits(s[rr].w);
+                if (status && (nonfinite_bits(s[rr].x) | nonfinite_bits(s[rr].y) | nonfinite_bits(s[rr].z) |
+                               nonfinite_bits(s[rr].w)))
+                    atomicOr(status, 1);
             }
         }
         float ps = 0.f;
@@ -199,7 +199,7 @@ recurrent_kernel(const RecParams p) {
             const size_t oi = row * HvD + h * kD + j0 + tid;
             st_out(static_cast<Tout*>(p.out) + oi, y);
             if (p.prenorm) p.prenorm[oi] = ov;
-            if (p.flags & kFlagCheckFinite) bad_out |= nonfinite_bits(y);
+            if (status && nonfinite_bits(y)) atomicOr(status, 2);
         }
         // ---- conv state after token t: window (w1, w2, x_t); raw values, bit-exact
         Tact* cout = static_cast<Tact*>(p.conv_out) + static_cast<size_t>(b) * p.conv_out_b +
@@ -216,10 +216,6 @@ recurrent_kernel(const RecParams p) {
             wq[0] = wq[1]; wq[1] = wq[2]; wq[2] = xq;
             wk[0] = wk[1]; wk[1] = wk[2]; wk[2] = xk;
         }
-    }
-    if (p.dev_status && (p.flags & kFlagCheckFinite)) {
-        const int st = (__any_sync(0xffffffffu, bad_state) ? 1 : 0) | (__any_sync(0xffffffffu, bad_out) ? 2 : 0);
-        if (lane == 0 && st) atomicOr(p.dev_status + b * p.Hv + h, st);
     }
     // no CTA leaves while another may still read its rms_part
     cluster_sync_all();

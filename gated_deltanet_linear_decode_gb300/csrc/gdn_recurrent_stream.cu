@@ -1,0 +1,275 @@
+// gdn_recurrent_stream.cu -- persistent, TMA-streamed form of the recurrent
+// gated DeltaNet step (decode step and speculative-verify walk) for large
+// batches, where the fp32 state (64 KiB per (sequence, v-head)) is the whole
+// cost and the kernel must keep HBM busy.
+//
+// Method: xwen CLAUDE.md page, "Architecture cheat sheet (Qwen 3.6, ggml-org
+// GGUF)", "Gated DeltaNet layer" (recurrent step), and its "Drafting" section
+// (per-position state planes for verify rollback).
+//
+// One CTA per SM loops over work items (sequence b, q/k head kh, v-head m of
+// the group): items of one (b, kh) group are consecutive, and a group never
+// leaves its CTA, so the in-place conv-state update has a single writer.  For
+// every item a bulk asynchronous copy (cp.async.bulk, completion counted on an
+// mbarrier) lands the head's 128 x 128 state tile and its inputs -- the raw
+// rows of its q/k/v channels, z, conv taps -- in one of two shared-memory
+// stages, two items ahead of the compute.  On arrival the state goes to
+// registers (warp w owns rows 16w..16w+15, lane = 4 consecutive columns) and
+// the small inputs to a private area, so the stage is refilled at once.
+//
+// S.k and S.q of a warp's 16 rows (32 partial sums per lane) are reduced with
+// one transposed butterfly (31 shuffles).  Decode and verify share this code,
+// so verify checkpoints equal decode replays bit for bit.
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kSThreads = 256;     // 8 warps x 16 rows
+constexpr int kStages = 2;
+
+__device__ __forceinline__ float conv4(float4 w, float x0, float x1, float x2, float cur) {
+    return fmaf(w.w, cur, fmaf(w.z, x2, fmaf(w.y, x1, w.x * x0)));
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(tc::smem_u32(mbar))
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(mbar)), "r"(bytes)
+                 : "memory");
+}
+
+// Byte layout of one stage (es = activation element size).
+struct StageLayout {
+    uint32_t cw, xr, zr, bytes;   // conv taps (q|k|v), raw rows [K+3][q|k|v], z rows [K]
+    __host__ __device__ StageLayout(int K, int es) {
+        cw = 65536;
+        xr = cw + 384 * 16;
+        zr = xr + (K + 3) * 384 * es;
+        bytes = zr + K * 128 * es;
+    }
+};
+
+template <typename Tact, typename Tout>
+__global__ void __launch_bounds__(kSThreads, 1)
+recurrent_stream_kernel(const RecParams p) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    constexpr int es = sizeof(Tact);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = p.K, C = p.C, HvD = p.Hv * kD;
+    const int r = p.Hv / p.Hk;
+    const int n_groups = p.B * p.Hk;
+    const StageLayout L(K, es);
+    // private copy of the current item's small inputs, after the stages
+    uint8_t* cur = sm + kStages * L.bytes;
+    const uint32_t cur_bytes = L.bytes - 65536;
+    float* qk_s = reinterpret_cast<float*>(cur + ((cur_bytes + 15) & ~15u));   // [K][256] q_hat | k_hat
+    float* v_s = qk_s + K * 256;                                                  // [K][128]
+    float* o_s = v_s + K * 128;                                                   // [128]
+    float* red = o_s + 128;                                                       // [2][8]
+    float* part = red + 16;                                                       // [8]
+    float* gates = part + 8;                                                      // [K][2]
+    float* nw_s = gates + 2 * kMaxK;                                              // [128]
+    uint64_t* full = reinterpret_cast<uint64_t*>(nw_s + 128);                     // [kStages]
+
+    if (tid == 0)
+        for (int st = 0; st < kStages; ++st) tc::mbar_init(&full[st], 1);
+    if (tid < kD) nw_s[tid] = p.norm_w[tid];
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();
+
+    // item i of this CTA -> (group, m)
+    const int G = gridDim.x;
+    const int my_groups = blockIdx.x < n_groups ? (n_groups - 1 - blockIdx.x) / G + 1 : 0;
+    const int n_items = my_groups * r;
+    auto item_group = [&](int i) { return blockIdx.x + (i / r) * G; };
+
+    auto issue = [&](int i) {      // one thread: load item i into stage i % kStages
+        const int g = item_group(i), m = i % r;
+        const int b = g / p.Hk, kh = g % p.Hk, h = kh + m * p.Hk;
+        uint64_t* mb = &full[i % kStages];
+        const uint32_t base = tc::smem_u32(sm + (i % kStages) * L.bytes);
+        const uint32_t seg = 128 * es;   // one head's channels of one row
+        mbar_expect_tx(mb, L.bytes);
+        const float* Sh = p.S_in + (static_cast<size_t>(b) * p.Hv + h) * kD * kD;
+        for (int q = 0; q < 4; ++q) bulk_g2s(base + q * 16384, Sh + q * 4096, 16384, mb);
+        bulk_g2s(base + L.cw, p.conv_w + 4 * (kh * kD), 128 * 16, mb);
+        bulk_g2s(base + L.cw + 128 * 16, p.conv_w + 4 * (p.Hk * kD + kh * kD), 128 * 16, mb);
+        bulk_g2s(base + L.cw + 256 * 16, p.conv_w + 4 * (2 * p.Hk * kD + h * kD), 128 * 16, mb);
+        const Tact* cin = static_cast<const Tact*>(p.conv_in) + static_cast<size_t>(b) * 3 * C;
+        const Tact* xin = static_cast<const Tact*>(p.x) + static_cast<size_t>(b) * K * C;
+        for (int rr = 0; rr < K + 3; ++rr) {
+            const Tact* src = rr < 3 ? cin + rr * C : xin + static_cast<size_t>(rr - 3) * C;
+            const uint32_t d = base + L.xr + rr * 3 * seg;
+            bulk_g2s(d, src + kh * kD, seg, mb);
+            bulk_g2s(d + seg, src + p.Hk * kD + kh * kD, seg, mb);
+            bulk_g2s(d + 2 * seg, src + 2 * p.Hk * kD + h * kD, seg, mb);
+        }
+        const Tact* zin = static_cast<const Tact*>(p.z) + static_cast<size_t>(b) * K * HvD + h * kD;
+        for (int t = 0; t < K; ++t) bulk_g2s(base + L.zr + t * seg, zin + static_cast<size_t>(t) * HvD, seg, mb);
+    };
+
+    if (tid == 0)
+        for (int i = 0; i < kStages && i < n_items; ++i) issue(i);
+
+    float4 sreg[16];
+    for (int i = 0; i < n_items; ++i) {
+        const int g = item_group(i), m = i % r;
+        const int b = g / p.Hk, kh = g % p.Hk, h = kh + m * p.Hk;
+        const uint8_t* stg = sm + (i % kStages) * L.bytes;
+        // gates for the item's tokens: plain loads, issued before the wait
+        float a_raw = 0.f, b_raw = 0.f;
+        if (tid < K) {
+            const size_t gi = (static_cast<size_t>(b) * K + tid) * p.Hv + h;
+            a_raw = ld_act(static_cast<const Tact*>(p.a_raw) + gi);
+            b_raw = ld_act(static_cast<const Tact*>(p.b_raw) + gi);
+        }
+        const float a_dt = p.dt_bias[h], a_ssm = p.ssm_a[h];
+        if (!tc::mbar_wait(&full[i % kStages], (i / kStages) & 1, 1 << 22)) {
+            if (tid == 0 && p.dev_status) atomicOr(p.dev_status + b * p.Hv + h, 16);
+        }
+        // state rows -> registers; small inputs -> private area
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr)
+            sreg[rr] = *reinterpret_cast<const float4*>(stg + (warp * 16 + rr) * 512 + 16 * lane);
+        for (uint32_t e = tid * 16; e < cur_bytes; e += kSThreads * 16)
+            *reinterpret_cast<uint4*>(cur + e) = *reinterpret_cast<const uint4*>(stg + 65536 + e);
+        if (tid < K) {
+            gates[2 * tid] = sigmoidf_(b_raw);
+            gates[2 * tid + 1] = a_ssm * softplusf_(a_raw + a_dt);
+        }
+        __syncthreads();
+        if (tid == 0 && i + kStages < n_items) issue(i + kStages);
+
+        const float4* cw = reinterpret_cast<const float4*>(cur);                      // [384] taps
+        const Tact* xr = reinterpret_cast<const Tact*>(cur + (L.xr - 65536));          // [K+3][384]
+        const Tact* zr = reinterpret_cast<const Tact*>(cur + (L.zr - 65536));          // [K][128]
+        // ---- steps 1-4 for every token of the item: thread c < 256 owns q/k channel c, c < 128 v channel c
+        {
+            const float4 w = cw[tid];
+            const float4 wv = tid < kD ? cw[256 + tid] : make_float4(0, 0, 0, 0);
+            for (int t = 0; t < K; ++t) {
+                const float val = siluf_(conv4(w, to_f(xr[t * 384 + tid]), to_f(xr[(t + 1) * 384 + tid]),
+                                               to_f(xr[(t + 2) * 384 + tid]), to_f(xr[(t + 3) * 384 + tid])));
+                const float ss = warp_sum(val * val);
+                if (lane == 0) red[(warp >> 2) * 8 + (warp & 3)] = ss;
+                if (tid < kD)
+                    v_s[t * kD + tid] =
+                        siluf_(conv4(wv, to_f(xr[t * 384 + 256 + tid]), to_f(xr[(t + 1) * 384 + 256 + tid]),
+                                     to_f(xr[(t + 2) * 384 + 256 + tid]), to_f(xr[(t + 3) * 384 + 256 + tid])));
+                __syncthreads();
+                const float* rd = red + (warp >> 2) * 8;
+                const float nrm = sqrtf((rd[0] + rd[1]) + (rd[2] + rd[3]));
+                qk_s[t * 256 + tid] = val / fmaxf(nrm, p.eps);
+                __syncthreads();
+            }
+        }
+
+        int* const status = (p.dev_status && (p.flags & kFlagCheckFinite)) ? p.dev_status + b * p.Hv + h : nullptr;
+        for (int t = 0; t < K; ++t) {
+            // ---- step 7 on my 16 rows
+            const float4 qq = *reinterpret_cast<const float4*>(&qk_s[t * 256 + 4 * lane]);
+            const float4 kk = *reinterpret_cast<const float4*>(&qk_s[t * 256 + 128 + 4 * lane]);
+            const float kq = warp_sum(fmaf(kk.w, qq.w, fmaf(kk.z, qq.z, fmaf(kk.y, qq.y, kk.x * qq.x))));
+            const float beta = gates[2 * t];
+            const float eg = expf(gates[2 * t + 1]);
+            float* Sout = p.S_out + static_cast<size_t>(b) * p.S_out_b + static_cast<size_t>(t) * p.S_out_p +
+                          (static_cast<size_t>(h) * kD + warp * 16) * kD;
+            // partial S.k and S.q of my 16 rows: slot 2rr = row rr . k, slot 2rr+1 = row rr . q
+            float pv[32];
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const float4 sv = sreg[rr];
+                pv[2 * rr] = fmaf(sv.w, kk.w, fmaf(sv.z, kk.z, fmaf(sv.y, kk.y, sv.x * kk.x)));
+                pv[2 * rr + 1] = fmaf(sv.w, qq.w, fmaf(sv.z, qq.z, fmaf(sv.y, qq.y, sv.x * qq.x)));
+            }
+            const float full_sum = reduce32_transposed(pv);   // lane 2rr: (S k)_rr, lane 2rr+1: (S q)_rr
+            const int my_row = lane >> 1;
+            // d = (v - e^g S.k) beta in the even lane; the odd lane forms o from it
+            const float d_even = (v_s[t * kD + warp * 16 + my_row] - eg * full_sum) * beta;
+            const float d_pair = __shfl_xor_sync(0xffffffffu, d_even, 1);
+            const float o = fmaf(d_pair, kq, eg * full_sum) * kInvSqrtD;   // meaningful in odd lanes
+            const float o_mine = (lane & 1) ? o : 0.f;
+            const float ps = warp_sum(o_mine * o_mine);
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const float d = __shfl_sync(0xffffffffu, d_even, 2 * rr);
+                const float4 sv = sreg[rr];
+                float4 nv;
+                nv.x = fmaf(d, kk.x, eg * sv.x);
+                nv.y = fmaf(d, kk.y, eg * sv.y);
+                nv.z = fmaf(d, kk.z, eg * sv.z);
+                nv.w = fmaf(d, kk.w, eg * sv.w);
+                sreg[rr] = nv;
+                st_f4(Sout + rr * kD + 4 * lane, nv);
+                if (status && (nonfinite_bits(nv.x) | nonfinite_bits(nv.y) | nonfinite_bits(nv.z) | nonfinite_bits(nv.w)))
+                    atomicOr(status, 1);
+            }
+            if (lane & 1) o_s[warp * 16 + my_row] = o;
+            if (lane == 0) part[warp] = ps;
+            __syncthreads();
+            // ---- step 8: gated RMSNorm, thread c < 128 -> output j = c
+            const size_t row = static_cast<size_t>(b) * K + t;
+            if (tid < kD) {
+                float tot = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) tot += part[w];
+                const float rs = 1.0f / sqrtf(tot * (1.0f / kD) + p.eps);
+                const float ov = o_s[tid];
+                const float y = ov * rs * nw_s[tid] * siluf_(to_f(zr[t * kD + tid]));
+                const size_t oi = row * HvD + h * kD + tid;
+                st_out(static_cast<Tout*>(p.out) + oi, y);
+                if (p.prenorm) p.prenorm[oi] = ov;
+                if (status && nonfinite_bits(y)) atomicOr(status, 2);
+            }
+            // ---- conv state after token t: rows t+1, t+2, t+3 of the raw window (bit-exact).
+            // q/k channels are written by the group's last head only (every head of the
+            // group has its inputs staged before that head runs).
+            Tact* cout = static_cast<Tact*>(p.conv_out) + static_cast<size_t>(b) * p.conv_out_b +
+                         static_cast<size_t>(t) * p.conv_out_p;
+            if (tid < kD) {
+                const int cv = 2 * p.Hk * kD + h * kD + tid;
+#pragma unroll
+                for (int q = 0; q < 3; ++q) cout[q * C + cv] = xr[(t + 1 + q) * 384 + 256 + tid];
+            }
+            if (m == r - 1) {
+                const int ch = tid < kD ? kh * kD + tid : p.Hk * kD + kh * kD + (tid - kD);
+#pragma unroll
+                for (int q = 0; q < 3; ++q) cout[q * C + ch] = xr[(t + 1 + q) * 384 + tid];
+            }
+            __syncthreads();
+        }
+    }
+}
+
+}  // namespace
+
+size_t recurrent_stream_smem(int K, int act_dtype) {
+    const int es = act_dtype == 1 ? 2 : 4;
+    const StageLayout L(K, es);
+    const size_t cur = ((L.bytes - 65536 + 15) & ~static_cast<size_t>(15));
+    const size_t misc = (static_cast<size_t>(K) * 384 + 128 + 16 + 8 + 2 * kMaxK + 128) * 4 + kStages * 8;
+    return kStages * static_cast<size_t>(L.bytes) + cur + misc;
+}
+
+cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_dtype, int grid, cudaStream_t stream) {
+    const size_t smem = recurrent_stream_smem(p.K, act_dtype);
+    auto go = [&](auto kernel) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        kernel<<<grid, kSThreads, smem, stream>>>(p);
+        return cudaGetLastError();
+    };
+    if (act_dtype == 1)
+        return out_dtype == 1 ? go(recurrent_stream_kernel<__nv_bfloat16, __nv_bfloat16>)
+                              : go(recurrent_stream_kernel<__nv_bfloat16, float>);
+    return out_dtype == 1 ? go(recurrent_stream_kernel<float, __nv_bfloat16>) : go(recurrent_stream_kernel<float, float>);
+}
+
+}  // namespace gdn

@@ -152,6 +152,42 @@ def test_verify_checkpoints_bitexact_vs_decode_steps(K):
     assert G.conv_bits_equal(ck_conv, c_ck_ref, c.act_dtype)
 
 
+@pytest.mark.parametrize("K,act", [(2, torch.bfloat16), (1, torch.float32), (5, torch.bfloat16)])
+def test_large_batch_verify_bitexact_vs_decode(K, act):
+    """At B*H_k of several items per SM the library takes its streaming
+    (persistent) kernel for both calls; checkpoints still equal decode
+    replays bit for bit and match the oracle."""
+    B = 64
+    c = gdn_inputs.make_case("lv", Hk=16, Hv=32, B=B, K=K, act_dtype=act, seed=40 + K)
+    d, w = G.dims(c), G.weights(c)
+    conv0, S0 = G.dev(c.conv0), G.dev(c.S0)
+    ck_conv = torch.empty(B, K, 3, c.C, device="cuda", dtype=act)
+    ck_S = torch.empty(B, K, c.Hv, 128, 128, device="cuda")
+    out = torch.empty(B * K, c.Hv * 128, device="cuda")
+    gdn.gdn_verify_k(d, w, K, G.dev(c.x), G.dev(c.z), G.dev(c.a_raw), G.dev(c.b_raw), conv0, S0, ck_conv, ck_S, out)
+    conv, S = conv0.clone(), S0.clone()
+    xs = c.x.view(B, K, -1); zs = c.z.view(B, K, -1); as_ = c.a_raw.view(B, K, -1); bs = c.b_raw.view(B, K, -1)
+    for p in range(K):
+        o = torch.empty(B, c.Hv * 128, device="cuda")
+        gdn.gdn_decode_step(d, w, G.dev(xs[:, p]), G.dev(zs[:, p]), G.dev(as_[:, p]), G.dev(bs[:, p]), conv, S, o)
+        torch.cuda.synchronize()
+        assert torch.equal(ck_S[:, p], S) and torch.equal(ck_conv[:, p], conv)
+        assert torch.equal(out.view(B, K, -1)[:, p], o)
+    o_ref, _, S_ck_ref, c_ck_ref = oracle.verify_checkpoints(c.Hk, c.Hv, c.x, c.z, c.a_raw, c.b_raw, c.conv_w,
+                                                             c.dt_bias, c.ssm_a, c.norm_w, c.conv0, c.S0, K)
+    G.assert_out_close(out, o_ref, act)
+    G.assert_state_close(ck_S, S_ck_ref, act)
+    assert G.conv_bits_equal(ck_conv, c_ck_ref, act)
+
+
+def test_large_batch_nonfinite_reported():
+    c = gdn_inputs.make_case("lnan", Hk=16, Hv=32, B=64, K=1, seed=13)
+    c.x[7, 2 * 16 * 128 + 3 * 128 + 9] = float("nan")     # sequence 7, v-head 3, row 9
+    _, _, _, _, st = _decode(c, check_finite=True)
+    st = st.cpu().view(64, 32)
+    assert st[7, 3] == 3 and int((st != 0).sum()) == 1
+
+
 def test_verify_b64_k3_commit():
     """The verify workload (B=64, K=3, 16/32, bf16): outputs and checkpoints vs
     the oracle; commit(accept_len) makes the live state bit-identical to
