@@ -60,9 +60,10 @@ constexpr uint32_t kXf = kR3 + 33280;   // fp32 [3][16][16]
 constexpr uint32_t kWh = kR3;           // W^T hi (128 i x 64 t)
 constexpr uint32_t kA1 = kR3;           // D^T hi +0, lo +16384            (128 j x 64 t)
 constexpr uint32_t kA2 = kR3 + 32768;   // D^T diag(e^{Gam_n-Gam}) hi, lo
+constexpr uint32_t kDm = kR3 + 36864;   // fp32 [64][65] decay matrix e^{Gam_t-Gam_r} (r <= t)
 constexpr uint32_t kXs = kR3;           // staged raw rows: [67][q 256 B | k 256 B | v 256 B]
 constexpr uint32_t kXrow = 768;
-constexpr uint32_t kZs = kR3;           // staged z rows: [64][256 B]
+constexpr uint32_t kZs = kR1 + 36864;   // staged z rows: [64][256 B], after O^T
 
 // tensor-memory columns
 constexpr uint32_t kColS = 0, kColQK = 128, kColDU = 192, kColW = 256, kColO1 = 320, kColO2 = 384;
@@ -73,9 +74,18 @@ __device__ __forceinline__ float conv4(float4 w, float x0, float x1, float x2, f
     return fmaf(w.w, cur, fmaf(w.z, x2, fmaf(w.y, x1, w.x * x0)));
 }
 
-// SiLU with the fast exponential and a correctly rounded reciprocal (relative
-// error ~1e-6, far inside the output tolerance).
-__device__ __forceinline__ float silu_fast(float x) { return x * __frcp_rn(1.0f + __expf(-x)); }
+// SiLU with the fast exponential and fast division (relative error of a few
+// ulp, far inside the output tolerance; 0 for large negative x).
+__device__ __forceinline__ float silu_fast(float x) { return x * __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ void st_out4(float* p, const float (&y)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(y[0], y[1], y[2], y[3]);
+}
+__device__ __forceinline__ void st_out4(__nv_bfloat16* p, const float (&y)[4]) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(y[0], y[1]), b = __floats2bfloat162_rn(y[2], y[3]);
+    *reinterpret_cast<uint2*>(p) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
 
 __device__ __forceinline__ void bf16x8_to_f32(uint4 u, float* f) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -91,20 +101,21 @@ __device__ __forceinline__ void bf16x4_to_f32(uint2 u, float* f) {
 }
 
 // (I + A)^{-1} for a strictly lower 64 x 64 A (fp32, row stride 65): the four
-// 16 x 16 diagonal blocks by forward substitution, then the off-diagonal
-// blocks level by level, T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
+// 16 x 16 diagonal blocks by forward substitution (column c of block b per
+// thread, each solved value folded into the rows below it at once), then the
+// off-diagonal blocks level by level, T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj,
+// four adjacent columns of one row per thread.
 __device__ void unit_lower_inverse(const float* Af, float* Tf, float* Xf) {
     const int tid = threadIdx.x;
     if (tid < 64) {
         const int b = tid >> 4, c = tid & 15, o = 16 * b;
         float x[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            float acc = 0.f;
+        for (int t = 0; t < 16; ++t) x[t] = t == c ? 1.f : 0.f;
 #pragma unroll
-            for (int r = 0; r < t; ++r) acc = fmaf(Af[(o + t) * 65 + o + r], x[r], acc);
-            x[t] = t < c ? 0.f : (t == c ? 1.f : -acc);
-        }
+        for (int r = 0; r < 15; ++r)
+#pragma unroll
+            for (int t = r + 1; t < 16; ++t) x[t] = fmaf(-Af[(o + t) * 65 + o + r], x[r], x[t]);
 #pragma unroll
         for (int t = 0; t < 16; ++t) Tf[(o + t) * 65 + o + c] = x[t];
     }
@@ -115,23 +126,33 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* Xf) {
     __syncthreads();
     for (int d = 1; d < 4; ++d) {
         const int nb = 4 - d;
-        for (int e = tid; e < nb * 256; e += kTcThreads) {
-            const int bi = d + (e >> 8), bj = bi - d, rr = (e >> 4) & 15, cc = e & 15;
-            float acc = 0.f;
+        if (tid < nb * 64) {
+            const int bi = d + (tid >> 6), bj = bi - d, rr = (tid >> 2) & 15, cc = (tid & 3) * 4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
             for (int k = bj; k < bi; ++k)
 #pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    acc = fmaf(Af[(16 * bi + rr) * 65 + 16 * k + m], Tf[(16 * k + m) * 65 + 16 * bj + cc], acc);
-            Xf[(e >> 8) * 256 + rr * 16 + cc] = acc;
+                for (int m = 0; m < 16; ++m) {
+                    const float a = Af[(16 * bi + rr) * 65 + 16 * k + m];
+                    const float* tr = Tf + (16 * k + m) * 65 + 16 * bj + cc;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[q] = fmaf(a, tr[q], acc[q]);
+                }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) Xf[(tid >> 6) * 256 + rr * 16 + cc + q] = acc[q];
         }
         __syncthreads();
-        for (int e = tid; e < nb * 256; e += kTcThreads) {
-            const int bi = d + (e >> 8), bj = bi - d, rr = (e >> 4) & 15, cc = e & 15;
-            float acc = 0.f;
+        if (tid < nb * 64) {
+            const int bi = d + (tid >> 6), bj = bi - d, rr = (tid >> 2) & 15, cc = (tid & 3) * 4;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-                acc = fmaf(Tf[(16 * bi + rr) * 65 + 16 * bi + m], Xf[(e >> 8) * 256 + m * 16 + cc], acc);
-            Tf[(16 * bi + rr) * 65 + 16 * bj + cc] = -acc;
+            for (int m = 0; m < 16; ++m) {
+                const float a = Tf[(16 * bi + rr) * 65 + 16 * bi + m];
+                const float* xr = Xf + (tid >> 6) * 256 + m * 16 + cc;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[q] = fmaf(a, xr[q], acc[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) Tf[(16 * bi + rr) * 65 + 16 * bj + cc + q] = -acc[q];
         }
         __syncthreads();
     }
@@ -154,6 +175,7 @@ prefill_tc_kernel(const PrefillParams p) {
     float* ghi_s = reinterpret_cast<float*>(sm + kMisc + 512);
     float* glo_s = reinterpret_cast<float*>(sm + kMisc + 768);
     float* egam_s = reinterpret_cast<float*>(sm + kMisc + 1024);
+    float* elast_s = reinterpret_cast<float*>(sm + kMisc + 1536);   // e^{Gam_last - Gam_t}
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sm + kMisc + 1280);
     uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + kMisc + 1288);
     int* err_s = reinterpret_cast<int*>(sm + kMisc + 1296);
@@ -215,39 +237,49 @@ prefill_tc_kernel(const PrefillParams p) {
     const float a_dt = p.dt_bias[h], a_ssm = p.ssm_a[h];
     bool bad = false;
 
+    // Raw rows of positions cb-3 .. cb+n-1 (q/k channels of kh, v channels of h)
+    // into shared memory with asynchronous copies; completed by the next drain.
+    auto stage_rows = [&](int cb) {
+        const int nrow = min(kChunk, L - cb) + 3;
+        for (int e = tid; e < nrow * 48; e += kTcThreads) {
+            const int rr = e / 48, piece = e % 48, sec = piece >> 4, off = (piece & 15) * 8;
+            const int pos = cb - 3 + rr;
+            const int ch = (sec == 0 ? kh * kD : sec == 1 ? p.Hk * kD + kh * kD : 2 * p.Hk * kD + h * kD) + off;
+            uint8_t* dst = sm + kXs + rr * kXrow + sec * 256 + off * 2;
+            if (pos >= 0)
+                tc::cp_async16(dst, x + static_cast<size_t>(t0 + pos) * C + ch);
+            else if (!p.zero_init)
+                tc::cp_async16(dst, cst + (3 + pos) * C + ch);
+            else
+                *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
+    };
+    // Raw gate inputs of token cb + tid (threads 0..63), 0 past the sequence.
+    float nx_a = 0.f, nx_b = 0.f;
+    auto load_gates = [&](int cb) {
+        nx_a = 0.f;
+        nx_b = 0.f;
+        if (tid < min(kChunk, L - cb)) {
+            const size_t gi = static_cast<size_t>(t0 + cb + tid) * p.Hv + h;
+            nx_b = ld_act(static_cast<const __nv_bfloat16*>(p.b_raw) + gi);
+            nx_a = ld_act(static_cast<const __nv_bfloat16*>(p.a_raw) + gi);
+        }
+    };
+    if (L > 0) {
+        stage_rows(0);
+        load_gates(0);
+    }
+
     for (int c0 = 0; c0 < L && !abort; c0 += kChunk) {
         const int n = min(kChunk, L - c0);
-        __syncthreads();
-        // ===== phase a: stage the chunk's raw rows (positions c0-3 .. c0+n-1; q/k
-        // channels of kh and v channels of h) with one round of async copies,
-        // load the gates in parallel, then conv, SiLU, clamp L2 from shared memory.
-        {
-            const int nrow = n + 3;
-            for (int e = tid; e < nrow * 48; e += kTcThreads) {
-                const int rr = e / 48, piece = e % 48, sec = piece >> 4, off = (piece & 15) * 8;
-                const int pos = c0 - 3 + rr;
-                const int ch = (sec == 0 ? kh * kD : sec == 1 ? p.Hk * kD + kh * kD : 2 * p.Hk * kD + h * kD) + off;
-                uint8_t* dst = sm + kXs + rr * kXrow + sec * 256 + off * 2;
-                if (pos >= 0)
-                    tc::cp_async16(dst, x + static_cast<size_t>(t0 + pos) * C + ch);
-                else if (!p.zero_init)
-                    tc::cp_async16(dst, cst + (3 + pos) * C + ch);
-                else
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-            }
-            if (tid < kChunk) {
-                float bt = 0.f, gt = 0.f;
-                if (tid < n) {
-                    const size_t gi = static_cast<size_t>(t0 + c0 + tid) * p.Hv + h;
-                    bt = sigmoidf_(ld_act(static_cast<const __nv_bfloat16*>(p.b_raw) + gi));
-                    gt = a_ssm * softplusf_(ld_act(static_cast<const __nv_bfloat16*>(p.a_raw) + gi) + a_dt);
-                }
-                beta_s[tid] = bt;
-                g_s[tid] = gt;
-            }
-            tc::cp_async_drain();
-            __syncthreads();
+        // ===== phase a: gates of the chunk; its raw rows were staged during the
+        // previous chunk's output phase (or before the loop) and land here.
+        if (tid < kChunk) {
+            beta_s[tid] = tid < n ? sigmoidf_(nx_b) : 0.f;
+            g_s[tid] = tid < n ? a_ssm * softplusf_(nx_a + a_dt) : 0.f;
         }
+        tc::cp_async_drain();
+        __syncthreads();
         if (warp == 0) {
             // inclusive scan of g in fp64: lane l owns tokens 2l, 2l+1
             const double g0 = static_cast<double>(g_s[2 * lane]), g1 = static_cast<double>(g_s[2 * lane + 1]);
@@ -267,6 +299,7 @@ prefill_tc_kernel(const PrefillParams p) {
             egam_s[2 * lane] = __expf(h0);
             egam_s[2 * lane + 1] = __expf(h1);
         }
+#pragma unroll 2
         for (int t = warp; t < kChunk; t += 8) {
             const uint32_t qrow = is_q ? t : 64 + t;
             if (t < n) {
@@ -285,7 +318,7 @@ prefill_tc_kernel(const PrefillParams p) {
                 }
 #pragma unroll
                 for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);   // within 16-lane halves
-                const float inv = 1.0f / fmaxf(sqrtf(ss), p.eps);
+                const float inv = rsqrtf(fmaxf(ss, p.eps * p.eps));   // 1 / max(||x||, eps)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) val[i] *= inv;
                 uint4 hi, lo;
@@ -327,6 +360,19 @@ prefill_tc_kernel(const PrefillParams p) {
             }
             tc::mma_commit(mbar);
         }
+        // while the MMAs run: decay matrix e^{Gam_t - Gam_r} (r <= t, else 0) and
+        // e^{Gam_last - Gam_t}; the staged raw rows under kDm are consumed
+        {
+            float* Dm = reinterpret_cast<float*>(sm + kDm);
+            const int tt = tid >> 2, r0 = (tid & 3) * 16;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int r = r0 + i;
+                Dm[tt * 65 + r] = r <= tt ? __expf(dgam(tt, r)) : 0.f;
+            }
+            if (tid < kChunk) elast_s[tid] = __expf(dgam(nl, tid));
+        }
+        __syncthreads();
         wait_mma();
 
         // ===== phase c: P and A from the stacked product; T = (I + A)^{-1}
@@ -334,6 +380,7 @@ prefill_tc_kernel(const PrefillParams p) {
             float* Af = reinterpret_cast<float*>(sm + kAf);
             float* Tf = reinterpret_cast<float*>(sm + kTf);
             float* Xf = reinterpret_cast<float*>(sm + kXf);
+            const float* Dm = reinterpret_cast<const float*>(sm + kDm);
             float v[32];
             const int t = row & 63;
             tc::tmem_ld32(tl + kColQK + 32 * chalf, v);
@@ -344,7 +391,7 @@ prefill_tc_kernel(const PrefillParams p) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int r = 32 * chalf + 8 * g8 + i;
-                        pv[i] = r <= t ? __expf(dgam(t, r)) * v[8 * g8 + i] : 0.f;
+                        pv[i] = Dm[t * 65 + r] * v[8 * g8 + i];
                     }
                     uint4 hi, lo;
                     tc::split8(pv, hi, lo);
@@ -356,7 +403,7 @@ prefill_tc_kernel(const PrefillParams p) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int r = 32 * chalf + i;
-                    Af[t * 65 + r] = r < t ? beta_s[t] * __expf(dgam(t, r)) * v[i] : 0.f;
+                    Af[t * 65 + r] = r < t ? beta_s[t] * Dm[t * 65 + r] * v[i] : 0.f;
                 }
             }
             tc::fence_before_sync();
@@ -456,8 +503,14 @@ prefill_tc_kernel(const PrefillParams p) {
         }
         wait_mma();
 
-        // ===== phase g: D^T -> fp16 operands (plain and scaled by e^{Gam_n - Gam_t})
+        // ===== phase g: D^T -> fp16 operands (plain and scaled by e^{Gam_n - Gam_t});
+        // the chunk's z rows start loading behind the free S operand
         {
+            for (int e = tid; e < n * 16; e += kTcThreads) {   // 16 x 16 B per row
+                const int t = e >> 4, off = (e & 15) * 8;
+                tc::cp_async16(sm + kZs + t * 256 + off * 2, static_cast<const __nv_bfloat16*>(p.z) +
+                                                                  static_cast<size_t>(t0 + c0 + t) * HvD + h * kD + off);
+            }
             float v[32];
             tc::tmem_ld32(tl + kColDU + 32 * chalf, v);
 #pragma unroll
@@ -466,7 +519,7 @@ prefill_tc_kernel(const PrefillParams p) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int t = 32 * chalf + 8 * g8 + i;
-                    sc[i] = v[8 * g8 + i] * __expf(dgam(nl, t));
+                    sc[i] = v[8 * g8 + i] * elast_s[t];
                 }
                 uint4 hi, lo;
                 const uint32_t o = tc::cl_off(row, 32 * chalf + 8 * g8, 128);
@@ -504,11 +557,6 @@ prefill_tc_kernel(const PrefillParams p) {
         // ===== phase i: o = (e^Gam O1 + O2)/sqrt(128) -> transpose -> gated RMSNorm -> out
         {
             float* OT = reinterpret_cast<float*>(sm + kOT);
-            for (int e = tid; e < n * 16; e += kTcThreads) {   // z rows of the chunk, 16 x 16 B each
-                const int t = e >> 4, off = (e & 15) * 8;
-                tc::cp_async16(sm + kZs + t * 256 + off * 2, static_cast<const __nv_bfloat16*>(p.z) +
-                                                                  static_cast<size_t>(t0 + c0 + t) * HvD + h * kD + off);
-            }
             float v1[32], v2[32];
             tc::tmem_ld32(tl + kColO1 + 32 * chalf, v1);
             tc::tmem_ld32(tl + kColO2 + 32 * chalf, v2);
@@ -521,29 +569,31 @@ prefill_tc_kernel(const PrefillParams p) {
             tc::fence_before_sync();
             __syncthreads();
             if (*err_s) abort = true;
+            if (!abort && c0 + kChunk < L) {   // next chunk's inputs load behind the output
+                stage_rows(c0 + kChunk);
+                load_gates(c0 + kChunk);
+            }
             for (int t = warp; t < n; t += 8) {
                 const float4 o4 = *reinterpret_cast<const float4*>(OT + t * kLdO + 4 * lane);
                 float ss = o4.x * o4.x + o4.y * o4.y + o4.z * o4.z + o4.w * o4.w;
                 ss = warp_sum(ss);
-                const float rs = 1.0f / sqrtf(ss * (1.0f / kD) + p.eps);
+                const float rs = rsqrtf(ss * (1.0f / kD) + p.eps);
                 const size_t oi = static_cast<size_t>(t0 + c0 + t) * HvD + h * kD + 4 * lane;
                 float zf[4];
                 bf16x4_to_f32(*reinterpret_cast<const uint2*>(sm + kZs + t * 256 + 8 * lane), zf);
                 const float4 w4 = *reinterpret_cast<const float4*>(p.norm_w + 4 * lane);
                 const float y[4] = {o4.x * rs * w4.x * silu_fast(zf[0]), o4.y * rs * w4.y * silu_fast(zf[1]),
                                     o4.z * rs * w4.z * silu_fast(zf[2]), o4.w * rs * w4.w * silu_fast(zf[3])};
-                Tout* out = static_cast<Tout*>(p.out) + oi;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    st_out(out + i, y[i]);
-                    if (p.flags & kFlagCheckFinite) bad |= nonfinite_bits(y[i]);
-                }
+                st_out4(static_cast<Tout*>(p.out) + oi, y);
+                if (p.flags & kFlagCheckFinite)
+                    bad |= nonfinite_bits(y[0]) | nonfinite_bits(y[1]) | nonfinite_bits(y[2]) | nonfinite_bits(y[3]);
                 if (p.prenorm) *reinterpret_cast<float4*>(p.prenorm + oi) = o4;
             }
         }
     }
 
     // ---- final state out (lane j = row j)
+    tc::cp_async_drain();
     __syncthreads();
     bool bad_s = false;
     {

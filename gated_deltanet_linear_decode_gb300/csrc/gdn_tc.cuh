@@ -138,26 +138,28 @@ __device__ __forceinline__ void split_f16(float x, __half& hi, __half& lo) {
     lo = __float2half_rn(x - __half2float(hi));
 }
 
-__device__ __forceinline__ uint32_t pack_h2(__half a, __half b) {
-    return static_cast<uint32_t>(__half_as_ushort(a)) | (static_cast<uint32_t>(__half_as_ushort(b)) << 16);
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// Two floats -> packed (hi, lo) fp16 pairs, using the paired conversions.
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 back = __half22float2(h);
+    hi = h2_bits(h);
+    lo = h2_bits(__floats2half2_rn(a - back.x, b - back.y));
 }
 
 // Split 8 floats into 8 fp16 his and 8 fp16 los (16 bytes each).
 __device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
-    __half h[8], l[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) split_f16(x[i], h[i], l[i]);
-    hi = make_uint4(pack_h2(h[0], h[1]), pack_h2(h[2], h[3]), pack_h2(h[4], h[5]), pack_h2(h[6], h[7]));
-    lo = make_uint4(pack_h2(l[0], l[1]), pack_h2(l[2], l[3]), pack_h2(l[4], l[5]), pack_h2(l[6], l[7]));
+    split2(x[0], x[1], hi.x, lo.x);
+    split2(x[2], x[3], hi.y, lo.y);
+    split2(x[4], x[5], hi.z, lo.z);
+    split2(x[6], x[7], hi.w, lo.w);
 }
 
 // Split 4 floats into 4 fp16 his and 4 los (8 bytes each).
 __device__ __forceinline__ void split4(const float* x, uint2& hi, uint2& lo) {
-    __half h[4], l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) split_f16(x[i], h[i], l[i]);
-    hi = make_uint2(pack_h2(h[0], h[1]), pack_h2(h[2], h[3]));
-    lo = make_uint2(pack_h2(l[0], l[1]), pack_h2(l[2], l[3]));
+    split2(x[0], x[1], hi.x, lo.x);
+    split2(x[2], x[3], hi.y, lo.y);
 }
 
 }  // namespace tc
