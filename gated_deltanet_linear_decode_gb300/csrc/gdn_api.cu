@@ -222,7 +222,7 @@ gdn_status gdn_commit(const gdn_dims* dims, int32_t B, int32_t K, const int32_t*
 
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t n_seq, int64_t T_total) {
     if (check_dims(dims) != GDN_OK || n_seq < 0 || T_total < 0) return 0;
-    return gdn::prefill_workspace_bytes(dims->H_k, dims->H_v, n_seq, T_total);
+    return gdn::prefill_workspace_bytes(dims->H_k, dims->H_v, n_seq, T_total, dims->act_dtype, dims->flags);
 }
 
 gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, int32_t n_seq,
@@ -236,16 +236,18 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, int32
     if (n_seq == 0) return GDN_OK;
     if (!cu_seqlens_host || cu_seqlens_host[0] != 0) return GDN_E_INVALID_ARG;
     int max_len = 0;
+    long long n_chunks = 0;
     for (int i = 0; i < n_seq; ++i) {
         const int32_t L = cu_seqlens_host[i + 1] - cu_seqlens_host[i];
         if (cu_seqlens_host[i + 1] < cu_seqlens_host[i]) return GDN_E_INVALID_ARG;
         if (L > max_len) max_len = L;
+        n_chunks += (L + 63) / 64;   // chunks of 64 tokens
     }
     const int64_t T = cu_seqlens_host[n_seq];
     if ((s = check_weights(w)) != GDN_OK) return s;
     if ((s = check_ptrs({cu_seqlens_dev, conv_state, S}, {prenorm_out, dev_status, workspace})) != GDN_OK) return s;
     if (T > 0 && (s = check_ptrs({x, z, a_raw, b_raw, out}, {})) != GDN_OK) return s;
-    const size_t need = gdn::prefill_workspace_bytes(dims->H_k, dims->H_v, n_seq, T);
+    const size_t need = gdn::prefill_workspace_bytes(dims->H_k, dims->H_v, n_seq, T, dims->act_dtype, dims->flags);
     if (need > 0 && (!workspace || workspace_bytes < need)) return GDN_E_WORKSPACE;
     const int Hk = dims->H_k, Hv = dims->H_v;
     const size_t C = static_cast<size_t>(kD) * (2 * Hk + Hv);
@@ -268,6 +270,8 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, int32
     p.conv_w = w->conv_w; p.dt_bias = w->dt_bias; p.ssm_a = w->ssm_a; p.norm_w = w->norm_w;
     p.conv_state = conv_state; p.S = S; p.out = out; p.prenorm = prenorm_out; p.dev_status = dev_status;
     p.workspace = workspace;
+    p.n_chunks = static_cast<int>(n_chunks);
+    gdn::prefill_bind_workspace(p, dims->act_dtype);
     return cuda_status(gdn::launch_prefill(p, dims->act_dtype, dims->out_dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 

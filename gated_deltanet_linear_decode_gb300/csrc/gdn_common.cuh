@@ -64,6 +64,23 @@ __device__ __forceinline__ float reduce32_transposed(float (&v)[32]) {
     return v[0];
 }
 
+// The same for 16 partial sums per lane: afterwards every lane l holds the
+// sum over all 32 lanes of partial l % 16 (16 shuffles).
+__device__ __forceinline__ float reduce16_transposed(float (&v)[16]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float send = up ? v[i] : v[i + o];
+            const float keep = up ? v[i + o] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
 // ---------------------------------------------------------------- clusters (PTX ISA: barrier.cluster, mapa, ld.shared::cluster)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

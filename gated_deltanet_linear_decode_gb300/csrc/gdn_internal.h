@@ -73,9 +73,17 @@ struct PrefillParams {
     float* prenorm;
     int* dev_status;
     void* workspace;
+    // tensor-core prefill: chunk table and records inside the workspace
+    int n_chunks;            // total chunks over all sequences
+    int* chunk_base;         // device [n_seq+1]
+    uint8_t* ws_qk;          // q/k records, [n_chunks][Hk]
+    uint8_t* ws_v;           // v-head records, [n_chunks][Hv]
 };
 
-size_t prefill_workspace_bytes(int Hk, int Hv, int n_seq, long long T);
+// Workspace bytes of gdn_prefill_chunked for the path that act_dtype / flags select.
+size_t prefill_workspace_bytes(int Hk, int Hv, int n_seq, long long T, int act_dtype, uint32_t flags);
+// Point the chunk table and record arrays of p into p.workspace.
+void prefill_bind_workspace(PrefillParams& p, int act_dtype);
 cudaError_t launch_prefill(const PrefillParams& p, int act_dtype, int out_dtype, cudaStream_t stream);
 
 cudaError_t launch_recurrent(const RecParams& p, int act_dtype, int out_dtype, int rows_per_cta,

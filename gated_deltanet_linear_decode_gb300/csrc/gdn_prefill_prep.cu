@@ -1,0 +1,412 @@
+// gdn_prefill_prep.cu -- first kernel of the tensor-core prefill: the work of
+// a chunk that does not depend on the state, for every chunk of every
+// sequence at once (xwen CLAUDE.md page, "Ground truth": chunk = 64 form;
+// "Architecture cheat sheet", "Gated DeltaNet layer": conv1d k=4 without bias,
+// SiLU, clamp L2 norm, tiled heads, beta = sigmoid(b), g = ssm_a softplus(a + dt_bias)).
+//
+// One CTA of 8 warps per (chunk, q/k head kh).  It computes q_hat and k_hat of
+// the chunk once and the raw products [Q; K] K^T once on the tensor cores,
+// then for each v-head h with h mod H_k = kh (tiled heads):
+//   gates, Gam (fp64 scan), e^Gam, decay matrix e^{Gam_t-Gam_r};
+//   P = decay (.) Q K^T (r <= t) -> record, A = beta decay (.) K K^T (r < t);
+//   T = (I + A)^{-1} on the CUDA cores (fp32);
+//   U^T = V^T (T diag beta)^T, W^T = K^T (T diag(beta e^Gam))^T on the tensor
+//   cores (fp16 hi/lo split, three MMAs per product) -> record.
+// The records (layouts in gdn_prefill_tc.cuh) feed the state pass.
+#include "gdn_internal.h"
+#include "gdn_prefill_tc.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kPrepThreads = 256;
+
+// shared memory map (bytes)
+constexpr uint32_t kQKs = 0;           // [Q;K] hi +0, lo +32768   (128 rows x 128, canonical)
+constexpr uint32_t kVs = 65536;        // V hi +0, lo +16384       (64 r x 128 j, canonical 64 rows)
+constexpr uint32_t kTb = 98304;        // T diag(beta) hi +0, lo +8192
+constexpr uint32_t kTbe = 114688;      // T diag(beta e^Gam) hi +0, lo +8192
+constexpr uint32_t kAf = 131072;       // fp32 [64][65] A
+constexpr uint32_t kTf = 147712;       // fp32 [64][65] T
+constexpr uint32_t kXf = 164352;       // fp32 [3][16][16]
+constexpr uint32_t kDm = 167424;       // fp32 [64][65] decay matrix
+constexpr uint32_t kXqk = 131072;      // staged raw q|k rows [67][512 B] (consumed before kAf.. are used)
+constexpr uint32_t kXv = 184064;       // staged raw v rows [67][256 B]
+constexpr uint32_t kMisc = 201216;
+constexpr uint32_t kPrepSmem = kMisc + 1600;
+static_assert(kXqk + 67 * 512 <= kDm, "q/k staging overlaps the decay matrix");
+static_assert(kDm + 64 * 65 * 4 <= kXv, "decay matrix overlaps the v staging");
+
+constexpr uint32_t kColQK = 0, kColU = 64, kColW = 128, kPrepTmemCols = 256;
+constexpr int kWaitLimit = 1 << 22;
+
+__global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const PrefillParams p) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gc = blockIdx.x, kh = blockIdx.y;
+    const int Hk = p.Hk, Hv = p.Hv, C = p.C;
+
+    // sequence of this chunk: the last s with chunk_base[s] <= gc (a non-empty one)
+    const int* tab = p.chunk_base;
+    int lo = 0, hi = p.n_seq;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tab[mid] <= gc) lo = mid; else hi = mid;
+    }
+    const int s = lo;
+    const int c0 = (gc - tab[s]) * kChunk;
+    const int t0 = p.cu_seqlens[s];
+    const int n = min(kChunk, p.cu_seqlens[s + 1] - t0 - c0);
+    const int nl = n - 1;
+
+    float* beta_s = reinterpret_cast<float*>(sm + kMisc);
+    float* g_s = beta_s + 64;
+    // Gam_t as an unevaluated sum ghi + glo of two floats (formed from an fp64
+    // scan), so Gam_t - Gam_r keeps fp32 relative accuracy with fp32 arithmetic.
+    float* ghi_s = beta_s + 128;
+    float* glo_s = beta_s + 192;
+    float* egam_s = beta_s + 256;
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sm + kMisc + 1536);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + kMisc + 1544);
+    int* err_s = reinterpret_cast<int*>(sm + kMisc + 1552);
+    const uint32_t sb = tc::smem_u32(sm);
+
+    if (warp == 0) tc::tmem_alloc(tmem_base_s, kPrepTmemCols);
+    if (tid == 0) {
+        tc::mbar_init(mbar, 1);
+        *err_s = 0;
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_base_s;
+    const int quarter = warp & 3, chalf = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    auto dgam = [&](int t, int r) { return (ghi_s[t] - ghi_s[r]) + (glo_s[t] - glo_s[r]); };
+    uint32_t phase = 0;
+    auto wait_mma = [&]() {
+        const bool ok = tc::mbar_wait(mbar, phase, kWaitLimit);
+        phase ^= 1u;
+        if (!ok) atomicExch(err_s, 1);
+        tc::fence_after_sync();
+    };
+
+    // ---- stage the raw rows of positions c0-3 .. c0+n-1 (left context from the
+    // carried conv state in the first chunk of a sequence)
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x);
+    const __nv_bfloat16* cst = static_cast<const __nv_bfloat16*>(p.conv_state) + static_cast<size_t>(s) * 3 * C;
+    const int nrow = n + 3;
+    auto stage16 = [&](uint8_t* dst, int pos, int ch) {
+        if (pos >= 0)
+            tc::cp_async16(dst, x + static_cast<size_t>(t0 + pos) * C + ch);
+        else if (!p.zero_init)
+            tc::cp_async16(dst, cst + (3 + pos) * C + ch);
+        else
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    };
+    for (int e = tid; e < nrow * 32; e += kPrepThreads) {
+        const int rr = e >> 5, piece = e & 31, sec = piece >> 4, off = (piece & 15) * 8;
+        stage16(sm + kXqk + rr * 512 + sec * 256 + off * 2, c0 - 3 + rr, sec * Hk * kD + kh * kD + off);
+    }
+    auto stage_v = [&](int h) {
+        for (int e = tid; e < nrow * 16; e += kPrepThreads) {
+            const int rr = e >> 4, off = (e & 15) * 8;
+            stage16(sm + kXv + rr * 256 + off * 2, c0 - 3 + rr, 2 * Hk * kD + h * kD + off);
+        }
+    };
+    stage_v(kh);
+    float nx_a = 0.f, nx_b = 0.f;   // raw gate inputs of token c0 + tid
+    auto load_gates = [&](int h) {
+        if (tid < n) {
+            const size_t gi = static_cast<size_t>(t0 + c0 + tid) * Hv + h;
+            nx_b = ld_act(static_cast<const __nv_bfloat16*>(p.b_raw) + gi);
+            nx_a = ld_act(static_cast<const __nv_bfloat16*>(p.a_raw) + gi);
+        }
+    };
+    load_gates(kh);
+    tc::cp_async_drain();
+    __syncthreads();
+
+    // ---- q_hat, k_hat: conv, SiLU, clamp L2 -> [Q;K] hi/lo in shared memory and the q/k record
+    {
+        const bool is_q = lane < 16;
+        const int l16 = lane & 15;
+        const int ch0 = (is_q ? 0 : Hk * kD) + kh * kD + 8 * l16;
+        float4 w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const float4*>(p.conv_w + 4 * (ch0 + i));
+        uint8_t* rec = p.ws_qk + (static_cast<size_t>(gc) * Hk + kh) * pf::kQKRec + (is_q ? pf::kRecQhi : pf::kRecKhi);
+#pragma unroll 2
+        for (int t = warp; t < kChunk; t += 8) {
+            uint4 vh = make_uint4(0, 0, 0, 0), vl = make_uint4(0, 0, 0, 0);
+            if (t < n) {
+                float win[4][8];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    pf::bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + kXqk + (t + r) * 512 + (is_q ? 0 : 256) + 16 * l16),
+                                      win[r]);
+                float val[8], ss = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    val[i] = pf::silu_fast(pf::conv4(w[i], win[0][i], win[1][i], win[2][i], win[3][i]));
+                    ss = fmaf(val[i], val[i], ss);
+                }
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);   // within 16-lane halves
+                const float inv = rsqrtf(fmaxf(ss, p.eps * p.eps));   // 1 / max(||x||, eps)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) val[i] *= inv;
+                tc::split8(val, vh, vl);
+            }
+            const uint32_t so = tc::cl_off(is_q ? t : 64 + t, 8 * l16, 128);
+            *reinterpret_cast<uint4*>(sm + kQKs + so) = vh;
+            *reinterpret_cast<uint4*>(sm + kQKs + 32768 + so) = vl;
+            const uint32_t go = tc::cl_off(t, 8 * l16, 64);
+            *reinterpret_cast<uint4*>(rec + go) = vh;
+            *reinterpret_cast<uint4*>(rec + 16384 + go) = vl;
+        }
+    }
+    tc::fence_proxy_async();
+    __syncthreads();
+    // [Q;K] K^T (3 passes, K = 128): rows t < 64 give Q K^T, rows 64 + t give K K^T
+    if (tid == 0) {
+        tc::fence_after_sync();
+        constexpr uint32_t id = tc::idesc_f16(128, 64, 0, 0, 0);
+        for (int ps = 0; ps < 3; ++ps) {
+            const uint32_t a = sb + kQKs + (ps == 2 ? 32768u : 0u);
+            const uint32_t b = sb + kQKs + (ps == 1 ? 32768u : 0u) + 1024u;
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_f16(tmem + kColQK, tc::sdesc(a + ks * 4096, 2048, 128), tc::sdesc(b + ks * 4096, 2048, 128), id,
+                            (ps | ks) ? 1u : 0u);
+        }
+        tc::mma_commit(mbar);
+    }
+
+    const int G = Hv / Hk;
+    const float* Af = reinterpret_cast<const float*>(sm + kAf);
+    for (int g = 0; g < G; ++g) {
+        const int h = kh + g * Hk;
+        uint8_t* vrec = p.ws_v + (static_cast<size_t>(gc) * Hv + h) * pf::kVRec;
+        if (tid < kChunk) {
+            beta_s[tid] = tid < n ? sigmoidf_(nx_b) : 0.f;
+            g_s[tid] = tid < n ? p.ssm_a[h] * softplusf_(nx_a + p.dt_bias[h]) : 0.f;
+        }
+        __syncthreads();
+        if (g + 1 < G) load_gates(h + Hk);
+        if (warp == 0) {
+            // inclusive scan of g in fp64: lane l owns tokens 2l, 2l+1
+            const double g0 = static_cast<double>(g_s[2 * lane]), g1 = static_cast<double>(g_s[2 * lane + 1]);
+            double run = g0 + g1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double up = __shfl_up_sync(0xffffffffu, run, o);
+                if (lane >= o) run += up;
+            }
+            const double G0 = run - g1, G1 = run;
+            const float h0 = static_cast<float>(G0), h1 = static_cast<float>(G1);
+            ghi_s[2 * lane] = h0;
+            glo_s[2 * lane] = static_cast<float>(G0 - static_cast<double>(h0));
+            ghi_s[2 * lane + 1] = h1;
+            glo_s[2 * lane + 1] = static_cast<float>(G1 - static_cast<double>(h1));
+            egam_s[2 * lane] = __expf(h0);
+            egam_s[2 * lane + 1] = __expf(h1);
+        }
+        // v: conv, SiLU -> V hi/lo (64 r x 128 j)
+        {
+            float4 wv[4];
+            const int v_ch = 2 * Hk * kD + h * kD + 4 * lane;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) wv[i] = *reinterpret_cast<const float4*>(p.conv_w + 4 * (v_ch + i));
+#pragma unroll 2
+            for (int t = warp; t < kChunk; t += 8) {
+                uint2 vh = make_uint2(0, 0), vl = make_uint2(0, 0);
+                if (t < n) {
+                    float winv[4][4], vv[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        pf::bf16x4_to_f32(*reinterpret_cast<const uint2*>(sm + kXv + (t + r) * 256 + 8 * lane), winv[r]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) vv[i] = pf::silu_fast(pf::conv4(wv[i], winv[0][i], winv[1][i], winv[2][i], winv[3][i]));
+                    tc::split4(vv, vh, vl);
+                }
+                const uint32_t ov = tc::cl_off(t, 4 * lane, 64);
+                *reinterpret_cast<uint2*>(sm + kVs + ov) = vh;
+                *reinterpret_cast<uint2*>(sm + kVs + 16384 + ov) = vl;
+            }
+        }
+        __syncthreads();
+        if (g + 1 < G) stage_v(h + Hk);   // next v-head's raw rows load behind this head's work
+        // decay matrix e^{Gam_t - Gam_r} (r <= t, else 0); e^Gam and e^{Gam_last - Gam_t} -> record
+        {
+            float* Dm = reinterpret_cast<float*>(sm + kDm);
+            const int tt = tid >> 2, r0 = (tid & 3) * 16;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int r = r0 + i;
+                Dm[tt * 65 + r] = r <= tt ? __expf(dgam(tt, r)) : 0.f;
+            }
+            if (tid < kChunk) {
+                reinterpret_cast<float*>(vrec + pf::kRecEgam)[tid] = egam_s[tid];
+                reinterpret_cast<float*>(vrec + pf::kRecElast)[tid] = __expf(dgam(nl, tid));
+            }
+        }
+        __syncthreads();
+        if (g == 0) wait_mma();   // the [Q;K] K^T products
+        else tc::fence_after_sync();
+        // P (rows t < 64 of the product) -> record; A (rows 64 + t) -> shared fp32
+        {
+            const float* Dm = reinterpret_cast<const float*>(sm + kDm);
+            float* Afw = reinterpret_cast<float*>(sm + kAf);
+            float v[32];
+            const int t = row & 63;
+            tc::tmem_ld32(tl + kColQK + 32 * chalf, v);
+            if (row < 64) {
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    float pv[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) pv[i] = Dm[t * 65 + 32 * chalf + 8 * g8 + i] * v[8 * g8 + i];
+                    uint4 ph, pl;
+                    tc::split8(pv, ph, pl);
+                    const uint32_t o = tc::cl_off(t, 32 * chalf + 8 * g8, 64);
+                    *reinterpret_cast<uint4*>(vrec + pf::kRecPhi + o) = ph;
+                    *reinterpret_cast<uint4*>(vrec + pf::kRecPlo + o) = pl;
+                }
+            } else {
+                const float bt = beta_s[t];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int r = 32 * chalf + i;
+                    Afw[t * 65 + r] = r < t ? bt * Dm[t * 65 + r] * v[i] : 0.f;
+                }
+            }
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        pf::unit_lower_inverse<kPrepThreads>(Af, reinterpret_cast<float*>(sm + kTf), reinterpret_cast<float*>(sm + kXf));
+        // T diag(beta) and T diag(beta e^Gam): thread -> row tid/4, 16 columns
+        {
+            const float* Tf = reinterpret_cast<const float*>(sm + kTf);
+            const int tr = tid >> 2, r0 = (tid & 3) * 16;
+#pragma unroll
+            for (int g8 = 0; g8 < 2; ++g8) {
+                float a8[8], b8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = r0 + 8 * g8 + i;
+                    const float tb = Tf[tr * 65 + r] * beta_s[r];
+                    a8[i] = tb;
+                    b8[i] = tb * egam_s[r];
+                }
+                uint4 hi8, lo8;
+                const uint32_t o = tc::cl_off(tr, r0 + 8 * g8, 64);
+                tc::split8(a8, hi8, lo8);
+                *reinterpret_cast<uint4*>(sm + kTb + o) = hi8;
+                *reinterpret_cast<uint4*>(sm + kTb + 8192 + o) = lo8;
+                tc::split8(b8, hi8, lo8);
+                *reinterpret_cast<uint4*>(sm + kTbe + o) = hi8;
+                *reinterpret_cast<uint4*>(sm + kTbe + 8192 + o) = lo8;
+            }
+        }
+        tc::fence_proxy_async();
+        __syncthreads();
+        // U^T = V^T (T diag beta)^T ;  W^T = K^T (T diag(beta e^Gam))^T   (3 passes each, K = 64)
+        if (tid == 0) {
+            tc::fence_after_sync();
+            constexpr uint32_t id = tc::idesc_f16(128, 64, 1, 0, 0);
+            for (int ps = 0; ps < 3; ++ps) {
+                const uint32_t ah = ps == 2 ? 1u : 0u, bh = ps == 1 ? 1u : 0u;
+                for (int ks = 0; ks < 4; ++ks) {
+                    tc::mma_f16(tmem + kColU, tc::sdesc(sb + kVs + ah * 16384 + ks * 256, 128, 1024),
+                                tc::sdesc(sb + kTb + bh * 8192 + ks * 2048, 1024, 128), id, (ps | ks) ? 1u : 0u);
+                    tc::mma_f16(tmem + kColW, tc::sdesc(sb + kQKs + ah * 32768 + 1024 + ks * 256, 128, 2048),
+                                tc::sdesc(sb + kTbe + bh * 8192 + ks * 2048, 1024, 128), id, (ps | ks) ? 1u : 0u);
+                }
+            }
+            tc::mma_commit(mbar);
+        }
+        wait_mma();
+        // W^T -> fp16 hi (rows i) and U^T -> fp32 (rows j) into the record
+        {
+            float v[32];
+            tc::tmem_ld32(tl + kColW + 32 * chalf, v);
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+                uint4 wh, wl;
+                tc::split8(v + 8 * g8, wh, wl);
+                *reinterpret_cast<uint4*>(vrec + pf::kRecW + tc::cl_off(row, 32 * chalf + 8 * g8, 128)) = wh;
+            }
+            tc::tmem_ld32(tl + kColU + 32 * chalf, v);
+            float4* U4 = reinterpret_cast<float4*>(vrec + pf::kRecU);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                U4[(8 * chalf + q) * kD + row] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+        tc::cp_async_drain();
+        tc::fence_before_sync();
+    }
+    __syncthreads();
+    if (p.dev_status && tid == 0 && *err_s) atomicOr(p.dev_status + s * Hv + kh, 16);
+    if (warp == 0) tc::tmem_dealloc(tmem, kPrepTmemCols);
+}
+
+// Exclusive prefix of the per-sequence chunk counts: chunk_base[s] is the
+// global index of sequence s's first chunk, chunk_base[n_seq] the total.
+__global__ void chunk_table_kernel(const int* cu_seqlens, int n_seq, int* chunk_base) {
+    __shared__ int carry_s;
+    __shared__ int warp_s[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    if (tid == 0) carry_s = 0;
+    __syncthreads();
+    for (int base = 0; base < n_seq; base += blockDim.x) {
+        const int i = base + tid;
+        const int cnt = i < n_seq ? (cu_seqlens[i + 1] - cu_seqlens[i] + kChunk - 1) / kChunk : 0;
+        int v = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int up = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += up;
+        }
+        if (lane == 31) warp_s[warp] = v;
+        __syncthreads();
+        if (warp == 0) {
+            int w = lane < nw ? warp_s[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int up = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += up;
+            }
+            if (lane < nw) warp_s[lane] = w;   // inclusive over warps
+        }
+        __syncthreads();
+        const int carry = carry_s;
+        const int incl = v + (warp > 0 ? warp_s[warp - 1] : 0) + carry;
+        if (i < n_seq) chunk_base[i] = incl - cnt;
+        __syncthreads();
+        if (tid == blockDim.x - 1) carry_s = incl;
+        __syncthreads();
+    }
+    if (tid == 0) chunk_base[n_seq] = carry_s;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t stream) {
+    chunk_table_kernel<<<1, 256, 0, stream>>>(p.cu_seqlens, p.n_seq, p.chunk_base);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_prep(const PrefillParams& p, cudaStream_t stream) {
+    if (p.n_chunks == 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kPrepSmem));
+    if (e != cudaSuccess) return e;
+    chunk_prep_kernel<<<dim3(static_cast<unsigned>(p.n_chunks), static_cast<unsigned>(p.Hk)), kPrepThreads, kPrepSmem,
+                        stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -19,6 +19,7 @@
 // column walks free of bank conflicts).
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_prefill_tc.cuh"
 
 namespace gdn {
 
@@ -290,17 +291,45 @@ cudaError_t launch_prefill_simt(const PrefillParams& p, int act_dtype, int out_d
                           : launch_prefill_simt_t<float, float>(p, stream);
 }
 
-cudaError_t launch_prefill_tc(const PrefillParams& p, int out_dtype, cudaStream_t stream);
+cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t stream);
+cudaError_t launch_chunk_prep(const PrefillParams& p, cudaStream_t stream);
+cudaError_t launch_state_pass(const PrefillParams& p, int out_dtype, cudaStream_t stream);
 
-size_t prefill_workspace_bytes(int, int, int, long long) { return 0; }
+namespace {
+bool use_tensor_cores(int act_dtype, uint32_t flags) { return act_dtype == 1 && !(flags & kFlagForceSimt); }
+}  // namespace
 
-// bf16 activations take the tensor-core kernel; fp32 activations (whose 1e-5
-// tolerance needs fp32 products) take the CUDA-core kernel.  Either is
+// The tensor-core path keeps, per chunk, the q/k record of every q/k head and
+// the v record of every v-head; a sequence of L tokens has ceil(L/64) <= L/64 + 1
+// chunks, so T/64 + n_seq chunks bound every packing of T tokens.
+size_t prefill_workspace_bytes(int Hk, int Hv, int n_seq, long long T, int act_dtype, uint32_t flags) {
+    if (!use_tensor_cores(act_dtype, flags)) return 0;
+    const size_t nc = static_cast<size_t>((T + kChunk - 1) / kChunk) + static_cast<size_t>(n_seq);
+    return pf::table_bytes(n_seq) + nc * (static_cast<size_t>(Hk) * pf::kQKRec + static_cast<size_t>(Hv) * pf::kVRec);
+}
+
+void prefill_bind_workspace(PrefillParams& p, int act_dtype) {
+    if (!use_tensor_cores(act_dtype, p.flags)) return;
+    uint8_t* base = static_cast<uint8_t*>(p.workspace);
+    p.chunk_base = reinterpret_cast<int*>(base);
+    p.ws_qk = base + pf::table_bytes(p.n_seq);
+    p.ws_v = p.ws_qk + static_cast<size_t>(p.n_chunks) * p.Hk * pf::kQKRec;
+}
+
+// bf16 activations take the tensor-core path (chunk table, chunk preparation
+// over all chunks, state pass per (sequence, v-head)); fp32 activations (whose
+// 1e-5 tolerance needs fp32 products) take the CUDA-core kernel.  Either is
 // followed by the conv-state update, which must run after every CTA has read
 // the old rows.
 cudaError_t launch_prefill(const PrefillParams& p, int act_dtype, int out_dtype, cudaStream_t stream) {
-    cudaError_t e = act_dtype == 1 && !(p.flags & kFlagForceSimt) ? launch_prefill_tc(p, out_dtype, stream)
-                                                                   : launch_prefill_simt(p, act_dtype, out_dtype, stream);
+    cudaError_t e;
+    if (use_tensor_cores(act_dtype, p.flags)) {
+        if ((e = launch_chunk_table(p, stream)) != cudaSuccess) return e;
+        if ((e = launch_chunk_prep(p, stream)) != cudaSuccess) return e;
+        e = launch_state_pass(p, out_dtype, stream);
+    } else {
+        e = launch_prefill_simt(p, act_dtype, out_dtype, stream);
+    }
     if (e != cudaSuccess) return e;
     if (act_dtype == 1)
         conv_state_finalize_kernel<__nv_bfloat16><<<dim3((p.C + 255) / 256, p.n_seq), 256, 0, stream>>>(p);
