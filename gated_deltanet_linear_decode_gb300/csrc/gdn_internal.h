@@ -76,7 +76,6 @@ struct PrefillParams {
     // tensor-core prefill: chunk table and records inside the workspace
     int n_chunks;            // total chunks over all sequences
     int* chunk_base;         // device [n_seq+1]
-    uint8_t* ws_qk;          // q/k records, [n_chunks][Hk]
     uint8_t* ws_v;           // v-head records, [n_chunks][Hv]
 };
 

@@ -10,6 +10,7 @@
 //   gates, Gam (fp64 scan), e^Gam, decay matrix e^{Gam_t-Gam_r};
 //   P = decay (.) Q K^T (r <= t) -> record, A = beta decay (.) K K^T (r < t);
 //   T = (I + A)^{-1} on the CUDA cores (fp32);
+//   Q' = diag(e^Gam) Q and K' = diag(e^{Gam_last-Gam}) K -> record;
 //   U^T = V^T (T diag beta)^T, W^T = K^T (T diag(beta e^Gam))^T on the tensor
 //   cores (fp16 hi/lo split, three MMAs per product) -> record.
 // The records (layouts in gdn_prefill_tc.cuh) feed the state pass.
@@ -67,6 +68,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
     float* ghi_s = beta_s + 128;
     float* glo_s = beta_s + 192;
     float* egam_s = beta_s + 256;
+    float* elast_s = beta_s + 320;   // e^{Gam_last - Gam_t}
+    static_assert(384 * 4 <= 1536, "misc area");
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sm + kMisc + 1536);
     uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + kMisc + 1544);
     int* err_s = reinterpret_cast<int*>(sm + kMisc + 1552);
@@ -130,7 +133,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
     tc::cp_async_drain();
     __syncthreads();
 
-    // ---- q_hat, k_hat: conv, SiLU, clamp L2 -> [Q;K] hi/lo in shared memory and the q/k record
+    // ---- q_hat, k_hat: conv, SiLU, clamp L2 -> [Q;K] hi/lo in shared memory
     {
         const bool is_q = lane < 16;
         const int l16 = lane & 15;
@@ -138,7 +141,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         float4 w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const float4*>(p.conv_w + 4 * (ch0 + i));
-        uint8_t* rec = p.ws_qk + (static_cast<size_t>(gc) * Hk + kh) * pf::kQKRec + (is_q ? pf::kRecQhi : pf::kRecKhi);
 #pragma unroll 2
         for (int t = warp; t < kChunk; t += 8) {
             uint4 vh = make_uint4(0, 0, 0, 0), vl = make_uint4(0, 0, 0, 0);
@@ -164,9 +166,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
             const uint32_t so = tc::cl_off(is_q ? t : 64 + t, 8 * l16, 128);
             *reinterpret_cast<uint4*>(sm + kQKs + so) = vh;
             *reinterpret_cast<uint4*>(sm + kQKs + 32768 + so) = vl;
-            const uint32_t go = tc::cl_off(t, 8 * l16, 64);
-            *reinterpret_cast<uint4*>(rec + go) = vh;
-            *reinterpret_cast<uint4*>(rec + 16384 + go) = vl;
         }
     }
     tc::fence_proxy_async();
@@ -249,8 +248,40 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
                 Dm[tt * 65 + r] = r <= tt ? __expf(dgam(tt, r)) : 0.f;
             }
             if (tid < kChunk) {
+                const float el = __expf(dgam(nl, tid));
+                elast_s[tid] = el;
                 reinterpret_cast<float*>(vrec + pf::kRecEgam)[tid] = egam_s[tid];
-                reinterpret_cast<float*>(vrec + pf::kRecElast)[tid] = __expf(dgam(nl, tid));
+                reinterpret_cast<float*>(vrec + pf::kRecElast)[tid] = el;
+            }
+        }
+        __syncthreads();
+        // Q' = diag(e^Gam) Q and K' = diag(e^{Gam_last - Gam}) K from the hi/lo operands -> fp16
+        // hi/lo records (thread: token tid/4, 32 indices, of Q then of K)
+#pragma unroll 1
+        for (int qk = 0; qk < 2; ++qk) {
+            const int tt = tid >> 2;
+            const float e = qk == 0 ? egam_s[tt] : elast_s[tt];
+            uint8_t* dst = vrec + (qk == 0 ? pf::kRecQhi : pf::kRecKhi);
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+                const int i0 = 32 * (tid & 3) + 8 * g8;
+                const uint32_t so = tc::cl_off(64 * qk + tt, i0, 128);
+                const uint4 qh = *reinterpret_cast<const uint4*>(sm + kQKs + so);
+                const uint4 ql = *reinterpret_cast<const uint4*>(sm + kQKs + 32768 + so);
+                const uint32_t hw[4] = {qh.x, qh.y, qh.z, qh.w}, lw[4] = {ql.x, ql.y, ql.z, ql.w};
+                float qv[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 h2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[k]));
+                    const float2 l2 = __half22float2(*reinterpret_cast<const __half2*>(&lw[k]));
+                    qv[2 * k] = fmaf(e, h2.x, e * l2.x);
+                    qv[2 * k + 1] = fmaf(e, h2.y, e * l2.y);
+                }
+                uint4 oh, ol;
+                tc::split8(qv, oh, ol);
+                const uint32_t go = tc::cl_off(tt, i0, 64);
+                *reinterpret_cast<uint4*>(dst + go) = oh;
+                *reinterpret_cast<uint4*>(dst + 16384 + go) = ol;
             }
         }
         __syncthreads();

@@ -299,21 +299,20 @@ namespace {
 bool use_tensor_cores(int act_dtype, uint32_t flags) { return act_dtype == 1 && !(flags & kFlagForceSimt); }
 }  // namespace
 
-// The tensor-core path keeps, per chunk, the q/k record of every q/k head and
-// the v record of every v-head; a sequence of L tokens has ceil(L/64) <= L/64 + 1
-// chunks, so T/64 + n_seq chunks bound every packing of T tokens.
-size_t prefill_workspace_bytes(int Hk, int Hv, int n_seq, long long T, int act_dtype, uint32_t flags) {
+// The tensor-core path keeps, per chunk, the record of every v-head; a sequence
+// of L tokens has ceil(L/64) <= L/64 + 1 chunks, so T/64 + n_seq chunks bound
+// every packing of T tokens.
+size_t prefill_workspace_bytes(int, int Hv, int n_seq, long long T, int act_dtype, uint32_t flags) {
     if (!use_tensor_cores(act_dtype, flags)) return 0;
     const size_t nc = static_cast<size_t>((T + kChunk - 1) / kChunk) + static_cast<size_t>(n_seq);
-    return pf::table_bytes(n_seq) + nc * (static_cast<size_t>(Hk) * pf::kQKRec + static_cast<size_t>(Hv) * pf::kVRec);
+    return pf::table_bytes(n_seq) + nc * static_cast<size_t>(Hv) * pf::kVRec;
 }
 
 void prefill_bind_workspace(PrefillParams& p, int act_dtype) {
     if (!use_tensor_cores(act_dtype, p.flags)) return;
     uint8_t* base = static_cast<uint8_t*>(p.workspace);
     p.chunk_base = reinterpret_cast<int*>(base);
-    p.ws_qk = base + pf::table_bytes(p.n_seq);
-    p.ws_v = p.ws_qk + static_cast<size_t>(p.n_chunks) * p.Hk * pf::kQKRec;
+    p.ws_v = base + pf::table_bytes(p.n_seq);
 }
 
 // bf16 activations take the tensor-core path (chunk table, chunk preparation

@@ -9,17 +9,18 @@
 // (lane j = v-row j).  Per chunk, with every product transposed so the MMA
 // runs at M = 128:
 //   Dacc = S W^T        (fp16 hi/lo of S x W^T hi, one MMA pass)
-//   O1   = S Q^T        (three passes: hi.hi + hi.lo + lo.hi)
-//   D^T  = U^T - Dacc,  D'^T = D^T diag(e^{Gam_last - Gam})
-//   S    = e^{Gam_last} S + D'^T K   (three passes)
-//   O2   = D^T P^T      (three passes)
-//   o_t  = (e^{Gam_t} O1 + O2)[:, t] / sqrt(128)  -> gated RMSNorm -> out
-// Warp roles:
-//   warps 0-7   convert: S -> fp16 operand (and the decay of S), Dacc -> D, D'
-//   warps 8-11  epilogue: O1, O2 -> o -> gated RMSNorm -> out (one chunk behind)
-//   warp 12     control: one lane issues the bulk copies of the records and the MMAs
-// and they meet only at mbarriers, so the epilogue of a chunk and the bulk
-// copies of the next overlap the conversions and MMAs of the current one.
+//   O    = S Q'^T       (Q' = diag(e^Gam) Q; three passes: hi.hi + hi.lo + lo.hi)
+//   D^T  = U^T - Dacc
+//   S    = e^{Gam_last} S + D^T K'   (K' = diag(e^{Gam_last - Gam}) K; three passes)
+//   O   += D^T P^T      (three passes)
+//   o_t  = O[:, t] / sqrt(128)  -> gated RMSNorm -> out
+// Warp roles, meeting only at mbarriers:
+//   warps 0-7   convert: S -> fp16 operand (and the decay of S), Dacc -> D
+//   warps 8-11  epilogue: O -> o -> gated RMSNorm -> out, up to three chunks behind
+//               (O is triple-buffered in tensor memory; z is staged by cp.async)
+//   warp 12     control: one lane issues the MMAs
+//   warp 13     copies: one lane issues the bulk copies of the records, each as
+//               soon as the MMAs that read its buffer have retired
 // Every wait has an iteration limit; a timeout sets dev_status bit 4.
 #include "gdn_internal.h"
 #include "gdn_prefill_tc.cuh"
@@ -29,52 +30,53 @@ namespace gdn {
 namespace {
 
 constexpr int kConvWarps = 8, kEpiWarps = 4;
-constexpr int kCtrlWarp = kConvWarps + kEpiWarps;
-constexpr int kStateThreads = (kConvWarps + kEpiWarps + 1) * 32;
+constexpr int kCtrlWarp = kConvWarps + kEpiWarps;   // MMA issue
+constexpr int kCopyWarp = kCtrlWarp + 1;            // bulk copies of the records
+constexpr int kStateThreads = (kConvWarps + kEpiWarps + 2) * 32;
 constexpr int kConvThreads = kConvWarps * 32, kEpiThreads = kEpiWarps * 32;
 
 // shared memory map (bytes)
 constexpr uint32_t kSs = 0;           // S hi +0, lo +32768        (128 j x 128 i, canonical 128 rows)
-constexpr uint32_t kDs = 65536;       // D hi +0, lo +16384; D' hi +32768, lo +49152  (128 j x 64 t)
-constexpr uint32_t kQs = 131072;      // Q hi +0, lo +16384        (64 t x 128 i, canonical 64 rows)
-constexpr uint32_t kKs = 163840;      // K hi +0, lo +16384
-constexpr uint32_t kWs = 196608;      // W^T hi                   (128 i x 64 t, canonical 128 rows)
-constexpr uint32_t kPs = 212992;      // P hi +0, lo +8192         (64 t x 64 r, canonical 64 rows)
-constexpr uint32_t kRs = 229376;      // RMS partial sums [2][4][64] fp32
-constexpr uint32_t kEs = 231424;      // e^Gam of even / odd chunks [2][64] fp32
-constexpr uint32_t kBar = 231936;     // mbarriers, then the TMEM base and the error flag
-constexpr uint32_t kStateSmem = kBar + 160;
+constexpr uint32_t kDs = 65536;       // D hi +0, lo +16384        (128 j x 64 t, canonical 128 rows)
+constexpr uint32_t kQs = 98304;       // Q' hi +0, lo +16384       (64 t x 128 i, canonical 64 rows)
+constexpr uint32_t kKs = 131072;      // K' hi +0, lo +16384       (64 t x 128 i, canonical 64 rows)
+constexpr uint32_t kWs = 163840;      // W^T hi                   (128 i x 64 t, canonical 128 rows)
+constexpr uint32_t kPs = 180224;      // P hi +0, lo +8192         (64 t x 64 r, canonical 64 rows)
+constexpr uint32_t kZs = 196608;      // z of a chunk, bf16 [64 t][128 j]
+constexpr uint32_t kRs = 212992;      // RMS partial sums [2][4][64] fp32
+constexpr uint32_t kBar = 215040;     // mbarriers, then the TMEM base and the error flag
+constexpr uint32_t kStateSmem = kBar + 176;
 static_assert(kStateSmem <= 232448, "shared memory of the state pass exceeds 227 KB");
 
 // mbarrier slots
 enum : int {
-    kLdQ = 0, kLdK, kLdW, kLdP,        // record copies landed (transaction count)
-    kMmaD, kMmaO1, kMmaS,              // MMA groups retired (tcgen05.commit)
-    kMmaO2a, kMmaO2b,                  // O2 of even / odd chunks retired
-    kSReady, kDReady,                  // converters wrote S / D operands (256 arrivals)
-    kEpiA, kEpiB,                      // epilogue done with O buffers of even / odd chunks (128 arrivals)
+    kLdW = 0, kLdQ, kLdK, kLdP,        // record copies landed (transaction count)
+    kMmaD, kMmaO1, kMmaS,              // Dacc / first O group / state update retired (tcgen05.commit)
+    kODone0, kODone1, kODone2,         // O of chunks c with c % 3 = 0, 1, 2 complete
+    kSReady, kDReady,                  // converters wrote the S / D operands (256 arrivals)
+    kEpi0, kEpi1, kEpi2,               // epilogue done with the O buffer of chunk c % 3 = 0, 1, 2 (128 arrivals)
     kRsReady,                          // epilogue wrote its per-token partial sums (128 arrivals)
-    kLdEa, kLdEb,                      // e^Gam of an even / odd chunk landed
+    kZReady,                           // the epilogue's copies of a chunk's z landed (128 arrivals)
     kDrain,                            // error path: every MMA issued so far retired
     kNumBars
 };
 
 // tensor-memory columns
-constexpr uint32_t kColS = 0, kColD = 128, kColO1 = 192, kColO2 = 320;   // O1 / O2: two buffers of 64
+constexpr uint32_t kColS = 0, kColD = 128, kColO = 192, kColG = 384;   // O: three buffers of 64; G: norm_w silu(z)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kWaitLimit = 1 << 24;
 
 template <typename Tout>
 __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    const int s = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv, kh = h % p.Hk;
+    const int s = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = p.cu_seqlens[s], L = p.cu_seqlens[s + 1] - t0;
     const int cbase = p.chunk_base[s], nch = p.chunk_base[s + 1] - cbase;
-    const int Hv = p.Hv, Hk = p.Hk, HvD = Hv * kD;
+    const int Hv = p.Hv, HvD = Hv * kD;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBar);
-    static_assert(8 * kNumBars + 8 <= 160, "mbarrier area");
+    static_assert(8 * kNumBars + 8 <= 176, "mbarrier area");
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sm + kBar + 8 * kNumBars);
     volatile int* err_s = reinterpret_cast<volatile int*>(sm + kBar + 8 * kNumBars + 4);
     const uint32_t sb = tc::smem_u32(sm);
@@ -82,9 +84,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
     if (warp == 0) tc::tmem_alloc(tmem_base_s, kTmemCols);
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
-            const uint32_t cnt = (i == kSReady || i == kDReady)                 ? kConvThreads
-                                 : (i == kEpiA || i == kEpiB || i == kRsReady) ? kEpiThreads
-                                                                               : 1;
+            uint32_t cnt = 1;
+            if (i == kSReady || i == kDReady) cnt = kConvThreads;
+            if (i == kEpi0 || i == kEpi1 || i == kEpi2 || i == kRsReady || i == kZReady) cnt = kEpiThreads;
             tc::mbar_init(bars + i, cnt);
         }
         *err_s = 0;
@@ -97,8 +99,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
 
     // Bounded wait that also gives up as soon as another role has timed out.
     // Converter and epilogue warps back off with short sleeps so that waiting
-    // warps leave the issue slots to the working ones; the control lane polls.
-    const bool sleepy = warp != kConvWarps + kEpiWarps;
+    // warps leave the issue slots to the working ones (the converters, on the
+    // state chain, sleep at most 64 ns); the control and copy lanes poll.
+    const bool sleepy = warp != kCtrlWarp && warp != kCopyWarp;
+    const uint32_t sleep_cap = warp < kConvWarps ? 64u : 256u;
     auto wait = [&](int bar, uint32_t parity) -> bool {
         uint32_t ns = 32;
         for (int it = 0; it < kWaitLimit; it += 8) {
@@ -106,7 +110,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
             if (*err_s) return false;
             if (sleepy) {
                 __nanosleep(ns);
-                ns = min(ns * 2, 256u);
+                ns = min(ns * 2, sleep_cap);
             }
         }
         *err_s = 1;
@@ -115,9 +119,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
 
     float* Sg = p.S + (static_cast<size_t>(s) * Hv + h) * kD * kD;
     const uint8_t* vrec0 = p.ws_v + (static_cast<size_t>(cbase) * Hv + h) * pf::kVRec;
-    const uint8_t* qkrec0 = p.ws_qk + (static_cast<size_t>(cbase) * Hk + kh) * pf::kQKRec;
     auto vrec = [&](int c) { return vrec0 + static_cast<size_t>(c) * Hv * pf::kVRec; };
-    auto qkrec = [&](int c) { return qkrec0 + static_cast<size_t>(c) * Hk * pf::kQKRec; };
 
     // ---- initial state into tensor memory (converter warps; lane j = row j)
     const int quarter = warp & 3;
@@ -145,39 +147,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
 
     bool bad = false;
     if (warp == kCtrlWarp) {
-        // ================= control: bulk copies of the records and the MMAs
+        // ================= control: the MMAs
         if (lane == 0 && nch > 0) {
-            // chunks whose records were requested / seen landed, for the (Q, W) and
-            // (K, P) barrier pairs (an error path drains the difference)
-            int req_qw = 0, got_qw = 0, req_k = 0, req_p = 0, got_kp = 0;
-            auto load = [&](int bar, void* dst, const uint8_t* src, uint32_t bytes) {
-                tc::mbar_expect_tx(bars + bar, bytes);
-                tc::bulk_g2s(dst, src, bytes, bars + bar);
-            };
-            auto load_q = [&](int c) { load(kLdQ, sm + kQs, qkrec(c) + pf::kRecQhi, 32768); };
-            auto load_k = [&](int c) { load(kLdK, sm + kKs, qkrec(c) + pf::kRecKhi, 32768); req_k = c + 1; };
-            auto load_w = [&](int c) { load(kLdW, sm + kWs, vrec(c) + pf::kRecW, 16384); req_qw = c + 1; };
-            auto load_p = [&](int c) { load(kLdP, sm + kPs, vrec(c) + pf::kRecPhi, 16384); req_p = c + 1; };
-            int req_e[2] = {0, 0}, got_e = 0;   // E copies are waited for by the epilogue
-            auto load_e = [&](int c) {
-                load(c & 1 ? kLdEb : kLdEa, sm + kEs + 256 * (c & 1), vrec(c) + pf::kRecEgam, 256);
-                req_e[c & 1] = c + 1;
-            };
-            auto prefetch = [&](int c) {   // chunk c's records toward L2
-                tc::bulk_prefetch_l2(qkrec(c), pf::kQKRec);
-                tc::bulk_prefetch_l2(vrec(c), pf::kRecU);
-            };
-            load_q(0); load_w(0); load_k(0); load_p(0); load_e(0);
-            if (nch > 1) { load_e(1); prefetch(1); }
-            if (nch > 2) prefetch(2);
-            (void)got_e;
             bool ok = true;
-            int c = 0;
-            for (; c < nch && ok; ++c) {
-                const uint32_t pc = c & 1, b = c & 1, pb = (c >> 1) & 1;
-                ok = wait(kSReady, pc) && wait(kLdW, pc) && wait(kLdQ, pc);
-                if (!ok) break;
-                got_qw = c + 1;
+            for (int c = 0; c < nch && ok; ++c) {
+                const uint32_t pc = c & 1, b = c % 3;
+                if (!(ok = wait(kSReady, pc) && wait(kLdW, pc))) break;
                 tc::fence_after_sync();
                 {   // Dacc = S W^T (1 pass, K = 128)
                     constexpr uint32_t id = tc::idesc_f16(128, 64, 0, 1, 0);
@@ -186,36 +161,26 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
                                     tc::sdesc(sb + kWs + ks * 256, 128, 2048), id, ks ? 1u : 0u);
                     tc::mma_commit(bars + kMmaD);
                 }
-                if (c >= 2) {
-                    if (!(ok = wait(b ? kEpiB : kEpiA, ((c - 2) >> 1) & 1))) break;
-                    load_e(c);
-                }
-                if (c + 3 < nch) prefetch(c + 3);
+                if (!(ok = (c < 3 || wait(kEpi0 + b, ((c - 3) / 3) & 1)) && wait(kLdQ, pc))) break;
                 tc::fence_after_sync();
-                {   // O1[b] = S Q^T (3 passes, K = 128)
+                {   // O[b] = S Q'^T (3 passes, K = 128)
                     constexpr uint32_t id = tc::idesc_f16(128, 64, 0, 0, 0);
                     for (int ps = 0; ps < 3; ++ps) {
                         const uint32_t ah = ps == 2 ? 32768u : 0u, bh = ps == 1 ? 16384u : 0u;
                         for (int ks = 0; ks < 8; ++ks)
-                            tc::mma_f16(tmem + kColO1 + 64 * b, tc::sdesc(sb + kSs + ah + ks * 4096, 2048, 128),
+                            tc::mma_f16(tmem + kColO + 64 * b, tc::sdesc(sb + kSs + ah + ks * 4096, 2048, 128),
                                         tc::sdesc(sb + kQs + bh + ks * 2048, 1024, 128), id, (ps | ks) ? 1u : 0u);
                     }
                     tc::mma_commit(bars + kMmaO1);
                 }
-                if (c + 1 < nch) {   // Q and W of the next chunk as soon as O1 (the last reader) retires
-                    if (!(ok = wait(kMmaO1, pc))) break;
-                    load_q(c + 1); load_w(c + 1);
-                }
-                ok = wait(kDReady, pc) && wait(kLdK, pc) && wait(kLdP, pc);
-                if (!ok) break;
-                got_kp = c + 1;
+                if (!(ok = wait(kDReady, pc) && wait(kLdK, pc) && wait(kLdP, pc))) break;
                 tc::fence_after_sync();
-                {   // S += D'^T K (3 passes, K = 64);  O2[b] = D^T P^T (3 passes, K = 64)
+                {   // S += D^T K' (3 passes, K = 64);  O[b] += D^T P^T (3 passes, K = 64)
                     constexpr uint32_t idk = tc::idesc_f16(128, 128, 0, 1, 0);
                     for (int ps = 0; ps < 3; ++ps) {
                         const uint32_t ah = ps == 2 ? 16384u : 0u, bh = ps == 1 ? 16384u : 0u;
                         for (int ks = 0; ks < 4; ++ks)
-                            tc::mma_f16(tmem + kColS, tc::sdesc(sb + kDs + 32768 + ah + ks * 4096, 2048, 128),
+                            tc::mma_f16(tmem + kColS, tc::sdesc(sb + kDs + ah + ks * 4096, 2048, 128),
                                         tc::sdesc(sb + kKs + bh + ks * 256, 128, 1024), idk, 1u);
                     }
                     tc::mma_commit(bars + kMmaS);
@@ -223,32 +188,49 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
                     for (int ps = 0; ps < 3; ++ps) {
                         const uint32_t ah = ps == 2 ? 16384u : 0u, bh = ps == 1 ? 8192u : 0u;
                         for (int ks = 0; ks < 4; ++ks)
-                            tc::mma_f16(tmem + kColO2 + 64 * b, tc::sdesc(sb + kDs + ah + ks * 4096, 2048, 128),
-                                        tc::sdesc(sb + kPs + bh + ks * 2048, 1024, 128), idp, (ps | ks) ? 1u : 0u);
+                            tc::mma_f16(tmem + kColO + 64 * b, tc::sdesc(sb + kDs + ah + ks * 4096, 2048, 128),
+                                        tc::sdesc(sb + kPs + bh + ks * 2048, 1024, 128), idp, 1u);
                     }
-                    tc::mma_commit(bars + (b ? kMmaO2b : kMmaO2a));
-                }
-                if (c + 1 < nch) {   // K and P of the next chunk, each as soon as its buffer is free
-                    if (!(ok = wait(kMmaS, pc))) break;
-                    load_k(c + 1);
-                    if (!(ok = wait(b ? kMmaO2b : kMmaO2a, pb))) break;
-                    load_p(c + 1);
+                    tc::mma_commit(bars + kODone0 + b);
                 }
             }
-            if (!ok) {
-                // error path: let every issued MMA retire and every issued copy land
-                // before the CTA releases its tensor and shared memory
+            if (!ok) {   // error path: let every issued MMA retire before the CTA releases its memory
                 tc::mma_commit(bars + kDrain);
                 tc::mbar_wait(bars + kDrain, 0, kWaitLimit);
-                if (req_qw > got_qw) {
-                    tc::mbar_wait(bars + kLdQ, (req_qw - 1) & 1, kWaitLimit);
-                    tc::mbar_wait(bars + kLdW, (req_qw - 1) & 1, kWaitLimit);
-                }
-                if (req_k > got_kp) tc::mbar_wait(bars + kLdK, (req_k - 1) & 1, kWaitLimit);
-                // E copies: wait for the last one issued into each buffer (its parity)
-                if (req_e[0]) tc::mbar_wait(bars + kLdEa, ((req_e[0] - 1) >> 1) & 1, kWaitLimit);
-                if (req_e[1]) tc::mbar_wait(bars + kLdEb, ((req_e[1] - 1) >> 1) & 1, kWaitLimit);
-                if (req_p > got_kp) tc::mbar_wait(bars + kLdP, (req_p - 1) & 1, kWaitLimit);
+            }
+        }
+    } else if (warp == kCopyWarp) {
+        // ================= copies: the records of chunk c + 1 as soon as chunk c's MMAs free the buffers
+        if (lane == 0 && nch > 0) {
+            int req_w = 0, req_q = 0, req_k = 0, req_p = 0;   // chunks requested per barrier (an error path drains them)
+            auto load = [&](int bar, uint32_t dst, int c, uint32_t off, uint32_t bytes, int& req) {
+                tc::mbar_expect_tx(bars + bar, bytes);
+                tc::bulk_g2s(sm + dst, vrec(c) + off, bytes, bars + bar);
+                req = c + 1;
+            };
+            load(kLdW, kWs, 0, pf::kRecW, 16384, req_w);
+            load(kLdQ, kQs, 0, pf::kRecQhi, 32768, req_q);
+            load(kLdK, kKs, 0, pf::kRecKhi, 32768, req_k);
+            load(kLdP, kPs, 0, pf::kRecPhi, 16384, req_p);
+            for (int c = 1; c < 3 && c < nch; ++c) tc::bulk_prefetch_l2(vrec(c), pf::kRecU);   // toward L2
+            bool ok = true;
+            for (int c = 0; c + 1 < nch && ok; ++c) {
+                const uint32_t pc = c & 1, b = c % 3, pb = (c / 3) & 1;
+                if (c + 3 < nch) tc::bulk_prefetch_l2(vrec(c + 3), pf::kRecU);
+                if (!(ok = wait(kMmaD, pc))) break;         // W^T read by Dacc
+                load(kLdW, kWs, c + 1, pf::kRecW, 16384, req_w);
+                if (!(ok = wait(kMmaO1, pc))) break;        // Q' read by the first O group
+                load(kLdQ, kQs, c + 1, pf::kRecQhi, 32768, req_q);
+                if (!(ok = wait(kMmaS, pc))) break;         // K' read by the state update
+                load(kLdK, kKs, c + 1, pf::kRecKhi, 32768, req_k);
+                if (!(ok = wait(kODone0 + b, pb))) break;   // P read by the O update
+                load(kLdP, kPs, c + 1, pf::kRecPhi, 16384, req_p);
+            }
+            if (!ok) {   // error path: let every issued copy land before the CTA releases its memory
+                if (req_w) tc::mbar_wait(bars + kLdW, (req_w - 1) & 1, kWaitLimit);
+                if (req_q) tc::mbar_wait(bars + kLdQ, (req_q - 1) & 1, kWaitLimit);
+                if (req_k) tc::mbar_wait(bars + kLdK, (req_k - 1) & 1, kWaitLimit);
+                if (req_p) tc::mbar_wait(bars + kLdP, (req_p - 1) & 1, kWaitLimit);
             }
         }
     } else if (warp < kConvWarps) {
@@ -263,14 +245,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
 #pragma unroll
             for (int q = 0; q < 8; ++q)
                 u4[q] = __ldg(reinterpret_cast<const float4*>(vr + pf::kRecU) + (8 * chalf + q) * kD + row);
-            const float4* el4 = reinterpret_cast<const float4*>(vr + pf::kRecElast) + 8 * chalf;
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(el4));   // its 32 decay factors: one 128-byte line
             const float eg_last = __ldg(reinterpret_cast<const float*>(vr + pf::kRecEgam) + 63);
-            if (c + 1 < nch) {   // the next chunk's U and decay vectors toward L2
-                const uint8_t* vn = vrec(c + 1);
-                tc::bulk_prefetch_l2(vn + pf::kRecU + tid * 128, 128);
-                if (tid < 4) tc::bulk_prefetch_l2(vn + pf::kRecEgam + tid * 128, 128);
-            }
+            if (c + 1 < nch && tid == 0)   // the next chunk's U and decay vectors toward L2 (one bulk request)
+                tc::bulk_prefetch_l2(vrec(c + 1) + pf::kRecU, pf::kVRec - pf::kRecU);
             if (c > 0 && !(ok = wait(kMmaS, (c - 1) & 1))) break;
             tc::fence_after_sync();
             // S -> fp16 hi/lo operand; S <- e^{Gam_last} S   (this thread: row j, 64 columns)
@@ -298,9 +275,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
             tc::fence_before_sync();
             tc::mbar_arrive(bars + kSReady);
             if (!(ok = wait(kMmaD, pc))) break;
-            if (c > 0 && !(ok = wait((c - 1) & 1 ? kMmaO2b : kMmaO2a, ((c - 1) >> 1) & 1))) break;
+            if (c > 0 && !(ok = wait(kODone0 + (c - 1) % 3, ((c - 1) / 3) & 1))) break;   // D read by O(c-1)
             tc::fence_after_sync();
-            // D^T = U^T - Dacc ; D'^T = D^T diag(e^{Gam_last - Gam_t}) -> fp16 hi/lo operands
+            // D^T = U^T - Dacc -> fp16 hi/lo operand
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 float v[16];
@@ -308,23 +285,15 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
 #pragma unroll
                 for (int g8l = 0; g8l < 2; ++g8l) {
                     const int g8 = 2 * hh + g8l;
-                    float d[8], dp[8];
-                    const float4 ua = u4[2 * g8], ub = u4[2 * g8 + 1], ea = __ldg(el4 + 2 * g8), eb = __ldg(el4 + 2 * g8 + 1);
-                    const float uu[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
-                    const float ee[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        d[i] = uu[i] - v[8 * g8l + i];
-                        dp[i] = d[i] * ee[i];
-                    }
+                    const float4 ua = u4[2 * g8], ub = u4[2 * g8 + 1];
+                    const float d[8] = {ua.x - v[8 * g8l], ua.y - v[8 * g8l + 1], ua.z - v[8 * g8l + 2],
+                                        ua.w - v[8 * g8l + 3], ub.x - v[8 * g8l + 4], ub.y - v[8 * g8l + 5],
+                                        ub.z - v[8 * g8l + 6], ub.w - v[8 * g8l + 7]};
                     uint4 hi, lo;
                     const uint32_t o = tc::cl_off(row, 32 * chalf + 8 * g8, 128);
                     tc::split8(d, hi, lo);
                     *reinterpret_cast<uint4*>(sm + kDs + o) = hi;
                     *reinterpret_cast<uint4*>(sm + kDs + 16384 + o) = lo;
-                    tc::split8(dp, hi, lo);
-                    *reinterpret_cast<uint4*>(sm + kDs + 32768 + o) = hi;
-                    *reinterpret_cast<uint4*>(sm + kDs + 49152 + o) = lo;
                 }
             }
             tc::fence_proxy_async();
@@ -350,96 +319,100 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
                 }
             }
         }
-    } else {
+    } else {   // warps kConvWarps .. kConvWarps + kEpiWarps - 1
         // ================= epilogue: thread = v-row j, the 64 tokens of a chunk in blocks of 16
         const int eq = warp - kConvWarps;   // lane quarter
-        const int j = eq * 32 + lane;
+        const int j = eq * 32 + lane, e = tid - kConvThreads;
         const uint32_t te = tmem + (static_cast<uint32_t>(eq * 32) << 16);
         float* Rs = reinterpret_cast<float*>(sm + kRs);
+        const unsigned short* zs = reinterpret_cast<const unsigned short*>(sm + kZs) + j;
         const float wj = p.norm_w[j];
-        const unsigned short* __restrict__ zj = static_cast<const unsigned short*>(p.z) + h * kD + j;
+        const __nv_bfloat16* zh = static_cast<const __nv_bfloat16*>(p.z) + h * kD;
         Tout* __restrict__ outj = static_cast<Tout*>(p.out) + h * kD + j;
         float* __restrict__ prej = p.prenorm ? p.prenorm + h * kD + j : nullptr;
         const bool check = (p.flags & kFlagCheckFinite) != 0;
-        // z of tokens [t, t + 16) of column j as raw bf16 bits (0 past the chunk)
-        auto load_z = [&](uint32_t (&zr)[16], size_t row0, int nrem) {
+        // chunk c's z rows (256 bytes of head h each) into shared memory by 16-byte
+        // asynchronous copies, zero past the sequence; they arrive on kZReady
+        auto stage_z = [&](int c) {
+            const int n = min(kChunk, L - c * kChunk);
+            const __nv_bfloat16* src = zh + static_cast<size_t>(t0 + c * kChunk) * HvD;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) zr[i] = i < nrem ? __ldg(zj + (row0 + i) * HvD) : 0u;
+            for (int k = 0; k < 8; ++k) {
+                const int piece = e + kEpiThreads * k, rr = piece >> 4, c16 = piece & 15;
+                const bool valid = rr < n;
+                tc::cp_async16_zfill(sm + kZs + rr * 256 + c16 * 16, src + static_cast<size_t>(valid ? rr : 0) * HvD + c16 * 8,
+                                     valid ? 16u : 0u);
+            }
+            tc::cp_async_mbar_arrive(bars + kZReady);
         };
+        if (nch > 0) stage_z(0);
         bool ok = true;
         for (int c = 0; c < nch && ok; ++c) {
-            const uint32_t b = c & 1;
+            const uint32_t b = c % 3, r = c & 1;   // O buffer, partial-sum buffer
             const int c0 = c * kChunk, n = min(kChunk, L - c0);
             const size_t row0 = static_cast<size_t>(t0 + c0);
-            if (c + 1 < nch) {   // next chunk's z rows toward L2: one 128-byte half row per thread
-                const int t = tid - kConvThreads;   // 0..127
-                if (t < 2 * min(kChunk, L - c0 - kChunk))
-                    tc::bulk_prefetch_l2(static_cast<const __nv_bfloat16*>(p.z) + (row0 + kChunk + (t >> 1)) * HvD + h * kD +
-                                             64 * (t & 1), 128);
-            }
-            uint32_t zc[16];
-            load_z(zc, row0, n);
-            if (!(ok = wait(b ? kMmaO2b : kMmaO2a, (c >> 1) & 1) && wait(b ? kLdEb : kLdEa, (c >> 1) & 1))) break;
+            if (c + 1 < nch && e < 2 * min(kChunk, L - c0 - kChunk))   // next chunk's z toward L2: a half row per thread
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(zh + (row0 + kChunk + (e >> 1)) * HvD + 64 * (e & 1)));
+            if (!(ok = wait(kODone0 + b, (c / 3) & 1) && wait(kZReady, c & 1))) break;
             tc::fence_after_sync();
-            const float* eg = reinterpret_cast<const float*>(sm + kEs + 256 * b);
-            // pass 1: o = (e^Gam O1 + O2)/sqrt(128) back into the O1 buffer, norm_w silu(z) into
-            // the O2 buffer, per-token partial sums of o^2 over this warp's 32 rows
+            // pass 1: per-token partial sums of o^2 over this warp's 32 rows (o = O / sqrt(128)),
+            // norm_w silu(z) into the G columns
 #pragma unroll 1
             for (int q = 0; q < 4; ++q) {
-                uint32_t zn[16];
-                if (q < 3) load_z(zn, row0 + 16 * (q + 1), n - 16 * (q + 1));
                 float v1[16], v2[16];
-                const uint32_t c1 = kColO1 + 64 * b + 16 * q, c2 = kColO2 + 64 * b + 16 * q;
-                tc::tmem_ld16(te + c1, v1);
-                tc::tmem_ld16(te + c2, v2);
+                tc::tmem_ld16(te + kColO + 64 * b + 16 * q, v1);
 #pragma unroll
-                for (int i = 0; i < 16; i += 4) {
-                    const float4 e = *reinterpret_cast<const float4*>(eg + 16 * q + i);
-                    const float ee[4] = {e.x, e.y, e.z, e.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        v1[i + k] = fmaf(ee[k], v1[i + k], v2[i + k]) * kInvSqrtD;
-                        v2[i + k] = wj * pf::silu_fast(__uint_as_float(zc[i + k] << 16));
-                    }
+                for (int i = 0; i < 16; ++i) {
+                    v2[i] = wj * pf::silu_fast(__uint_as_float(static_cast<uint32_t>(zs[(16 * q + i) * kD]) << 16));
+                    v1[i] *= v1[i] * (kInvSqrtD * kInvSqrtD);
                 }
-                tc::tmem_st16(te + c1, v1);
-                tc::tmem_st16(te + c2, v2);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v1[i] *= v1[i];
+                tc::tmem_st16(te + kColG + 16 * q, v2);
                 const float ssum = reduce16_transposed(v1);
-                if (lane < 16) Rs[(b * 4 + eq) * 64 + 16 * q + lane] = ssum;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) zc[i] = zn[i];
+                if (lane < 16) Rs[(r * 4 + eq) * 64 + 16 * q + lane] = ssum;
             }
             tc::tmem_wait_st();
             tc::mbar_arrive(bars + kRsReady);
             if (!(ok = wait(kRsReady, c & 1))) break;
+            if (c + 1 < nch) stage_z(c + 1);   // every epilogue thread is past its reads of this chunk's z
             // 1/sqrt(mean o^2 + eps) of tokens lane and 32 + lane
-            const float* rb = Rs + b * 256;
+            const float* rb = Rs + r * 256;
             const float rs_a = rsqrtf(((rb[lane] + rb[64 + lane]) + (rb[128 + lane] + rb[192 + lane])) * (1.0f / kD) + p.eps);
             const float rs_b = rsqrtf(((rb[32 + lane] + rb[96 + lane]) + (rb[160 + lane] + rb[224 + lane])) * (1.0f / kD) + p.eps);
-            // pass 2: y = o * rs * norm_w silu(z)
+            // pass 2: y = o * rs * norm_w silu(z); all 16 values first, then the stores
 #pragma unroll 1
             for (int q = 0; q < 4; ++q) {
                 float v1[16], v2[16];
-                tc::tmem_ld16(te + kColO1 + 64 * b + 16 * q, v1);
-                tc::tmem_ld16(te + kColO2 + 64 * b + 16 * q, v2);
+                tc::tmem_ld16(te + kColO + 64 * b + 16 * q, v1);
+                tc::tmem_ld16(te + kColG + 16 * q, v2);
                 const float rsq = q < 2 ? rs_a : rs_b;
-                Tout* oq = outj + (row0 + 16 * q) * HvD;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float rs = __shfl_sync(0xffffffffu, rsq, (16 * q + i) & 31);
-                    const float y = v1[i] * rs * v2[i];
-                    if (16 * q + i < n) {
-                        st_out(oq + static_cast<size_t>(i) * HvD, y);
-                        if (check) bad |= nonfinite_bits(y);
-                        if (prej) prej[(row0 + 16 * q + i) * HvD] = v1[i];
-                    }
+                    v1[i] *= kInvSqrtD;
+                    v2[i] *= v1[i] * __shfl_sync(0xffffffffu, rsq, (16 * q + i) & 31);
                 }
+                Tout* oq = outj + (row0 + 16 * q) * HvD;
+                float* pq = prej ? prej + (row0 + 16 * q) * HvD : nullptr;
+                const int nq = n - 16 * q;
+                if (nq >= 16) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) st_out(oq + static_cast<size_t>(i) * HvD, v2[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (i < nq) st_out(oq + static_cast<size_t>(i) * HvD, v2[i]);
+                }
+                if (check)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) bad |= i < nq && nonfinite_bits(v2[i]);
+                if (pq)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (i < nq) pq[static_cast<size_t>(i) * HvD] = v1[i];
             }
             tc::fence_before_sync();
-            tc::mbar_arrive(bars + (b ? kEpiB : kEpiA));
+            tc::mbar_arrive(bars + kEpi0 + b);
         }
+        tc::cp_async_drain();   // no copy of this thread may land after the CTA exits (error path)
     }
 
     tc::fence_before_sync();

@@ -10,8 +10,10 @@
 //   U = T diag(beta) V,   W = T diag(beta e^Gam) K,   D = U - W S^T
 //   O = diag(e^Gam) Q S^T + P D,   P[t][r] = e^{Gam_t-Gam_r} (q_t . k_r), r <= t
 //   S' = e^{Gam_n} S + D^T diag(e^{Gam_n-Gam}) K
-// Only D, O and S' involve the state; A, T, U, W, P and the decay vectors are
-// computed for all chunks at once by the preparation kernel.
+// Only D, O and S' involve the state; A, T, U, W, P, the decay-scaled
+// Q' = diag(e^Gam) Q and K' = diag(e^{Gam_n-Gam}) K and the decay vectors are
+// computed for all chunks at once by the preparation kernel, so that
+//   O = Q' S^T + P D,   S' = e^{Gam_n} S + D^T K'.
 #pragma once
 
 #include "gdn_common.cuh"
@@ -21,22 +23,20 @@ namespace gdn {
 namespace pf {
 
 // ---------------------------------------------------------------- workspace records
-// Per (chunk, q/k head): q_hat and k_hat as fp16 hi and lo parts, each a
-// 64 (token t) x 128 (index i) tile in the canonical no-swizzle layout with
-// 64 rows (element (t, i) at cl_off(t, i, 64)).
-constexpr uint32_t kQKRec = 65536;
-constexpr uint32_t kRecQhi = 0, kRecQlo = 16384, kRecKhi = 32768, kRecKlo = 49152;
-// Per (chunk, v-head):
-//   W^T hi      128 (i) x 64 (t) fp16, canonical with 128 rows      16384 B
-//   P hi, lo    64 (t) x 64 (r) fp16, canonical with 64 rows      2 x 8192 B
-//   U           fp32, float4 groups [t/4][j][t%4] (j = v-row)       32768 B
-//   e^Gam_t [64] fp32, then e^{Gam_last - Gam_t} [64] fp32             512 B
-constexpr uint32_t kVRec = 66048;
-constexpr uint32_t kRecW = 0, kRecPhi = 16384, kRecPlo = 24576, kRecU = 32768, kRecEgam = 65536,
-                   kRecElast = 65792;
+// Per (chunk, v-head), fp16 tiles in the canonical no-swizzle layout (element
+// (a, b) of a tile with A rows at cl_off(a, b, A)):
+//   Q' = diag(e^Gam) Q hi, lo              64 (t) x 128 (i), 64 rows       2 x 16384 B
+//   K' = diag(e^{Gam_last - Gam}) K hi, lo  64 (t) x 128 (i), 64 rows       2 x 16384 B
+//   W^T hi                                  128 (i) x 64 (t), 128 rows         16384 B
+//   P hi, lo                                64 (t) x 64 (r), 64 rows        2 x 8192 B
+//   U                 fp32, float4 groups [t/4][j][t%4] (j = v-row)            32768 B
+//   e^Gam_t [64] fp32, then e^{Gam_last - Gam_t} [64] fp32                       512 B
+constexpr uint32_t kVRec = 131584;
+constexpr uint32_t kRecQhi = 0, kRecQlo = 16384, kRecKhi = 32768, kRecKlo = 49152, kRecW = 65536, kRecPhi = 81920,
+                   kRecPlo = 90112, kRecU = 98304, kRecEgam = 131072, kRecElast = 131328;
 
-// Workspace = chunk table (int32 [n_seq+1], padded to 256 B), then the q/k
-// records of every (chunk, q/k head), then the v records of every (chunk, v-head).
+// Workspace = chunk table (int32 [n_seq+1], padded to 256 B), then the records
+// of every (chunk, v-head).
 __host__ __device__ inline size_t table_bytes(int n_seq) {
     return (static_cast<size_t>(n_seq + 1) * 4 + 255) / 256 * 256;
 }

@@ -182,6 +182,17 @@ __device__ __forceinline__ void cp_async_drain() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
+// 16-byte asynchronous copy that reads `src_bytes` (16 or 0) and zero-fills the rest.
+__device__ __forceinline__ void cp_async16_zfill(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(src_bytes)
+                 : "memory");
+}
+// Arrive on `mbar` once every cp.async this thread issued so far has landed
+// (the arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* mbar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(mbar)) : "memory");
+}
+
 // fp32 -> (hi, lo) fp16 pair with hi + lo = x to ~2^-22 relative.
 __device__ __forceinline__ void split_f16(float x, __half& hi, __half& lo) {
     hi = __float2half_rn(x);
