@@ -24,17 +24,19 @@ __all__ = [
     "GdnError", "GdnDims", "GdnWeights", "make_dims", "make_weights", "library",
     "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step",
     "gdn_verify_k", "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked",
-    "EXPORTED_SYMBOLS", "HEAD_DIM",
+    "gdn_prefill_chunked_static", "PREFILL_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "HEAD_DIM",
 ]
 
 HEAD_DIM = 128
 GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_CHECK_FINITE = 1
 GDN_FLAG_PREFILL_FP32 = 2
+PREFILL_STATIC_SCRATCH_BYTES = 128 * 1024 * 1024   # GDN_PREFILL_STATIC_SCRATCH_BYTES
 
 EXPORTED_SYMBOLS = (
     "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step",
     "gdn_verify_k", "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked",
+    "gdn_prefill_chunked_static",
 )
 
 
@@ -79,6 +81,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         "gdn_commit": (ctypes.c_int, [D, I32, I32, P, P, P, P, P, P]),
         "gdn_prefill_workspace_bytes": (SZ, [D, I32, ctypes.c_int64]),
         "gdn_prefill_chunked": (ctypes.c_int, [D, W, I32, P, P, P, P, P, P, P, P, I32, P, P, P, SZ, P, P]),
+        "gdn_prefill_chunked_static": (ctypes.c_int, [D, W, I32, P, P, P, P, P, P, P, P, I32, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -257,3 +260,30 @@ def gdn_prefill_chunked(dims: GdnDims, w: Weights, cu_seqlens_host, cu_seqlens_d
         ctypes.byref(dims), ctypes.byref(w.struct()), N, cu.data_ptr(), _ptr(cu_seqlens_dev), _ptr(x), _ptr(z),
         _ptr(a_raw), _ptr(b_raw), _ptr(conv_state), _ptr(S), int(bool(zero_init)), _ptr(out),
         _ptr(prenorm_out), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)))
+
+
+def gdn_prefill_chunked_static(dims: GdnDims, w: Weights, cu_seqlens_host, cu_seqlens_dev, x, z, a_raw, b_raw,
+                               conv_state, S, out, zero_init: bool = False, prenorm_out=None, dev_status=None,
+                               stream=None) -> None:
+    """gdn_prefill_chunked without a workspace: the library's fixed device
+    scratch area (PREFILL_STATIC_SCRATCH_BYTES, shared by every call) serves
+    instead, for callers that cannot allocate device memory.  Problems that
+    need more scratch than the area holds raise GdnError (GDN_E_WORKSPACE)."""
+    cu = cu_seqlens_host
+    if not isinstance(cu, torch.Tensor):
+        cu = torch.tensor(list(cu), dtype=torch.int32)
+    if cu.is_cuda or cu.dtype != torch.int32 or not cu.is_contiguous():
+        raise ValueError("cu_seqlens_host must be a contiguous int32 CPU tensor")
+    N = cu.numel() - 1
+    T = int(cu[-1])
+    C, HvD = HEAD_DIM * (2 * dims.H_k + dims.H_v), dims.H_v * HEAD_DIM
+    a = _act(dims)
+    _need(cu_seqlens_dev, torch.int32, (N + 1,))
+    _need(x, a, (T, C)); _need(z, a, (T, HvD)); _need(a_raw, a, (T, dims.H_v)); _need(b_raw, a, (T, dims.H_v))
+    _need(conv_state, a, (N, 3, C)); _need(S, torch.float32, (N, dims.H_v, HEAD_DIM, HEAD_DIM))
+    _need(out, _out(dims), (T, HvD)); _need(prenorm_out, torch.float32, (T, HvD), optional=True)
+    _need(dev_status, torch.int32, (N * dims.H_v,), optional=True)
+    _check("gdn_prefill_chunked_static", library().gdn_prefill_chunked_static(
+        ctypes.byref(dims), ctypes.byref(w.struct()), N, cu.data_ptr(), _ptr(cu_seqlens_dev), _ptr(x), _ptr(z),
+        _ptr(a_raw), _ptr(b_raw), _ptr(conv_state), _ptr(S), int(bool(zero_init)), _ptr(out),
+        _ptr(prenorm_out), _ptr(dev_status), _stream(stream)))

@@ -188,6 +188,48 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, int32
                                float* prenorm_out, void* workspace, size_t workspace_bytes,
                                int32_t* dev_status, gdn_stream_t stream);
 
+/*
+ * Size in bytes of the fixed device scratch area behind
+ * gdn_prefill_chunked_static (128 MiB).
+ */
+#define GDN_PREFILL_STATIC_SCRATCH_BYTES (128u * 1024u * 1024u)
+
+/*
+ * gdn_prefill_chunked_static -- gdn_prefill_chunked for callers that cannot
+ * allocate device memory when they call it: a runtime whose allocator owns the
+ * whole device pool, a plugin that is handed only its input and output
+ * buffers, or code in a region where allocating is not allowed.  The pages
+ * describe no such entry point; it is a convenience of this library.
+ *
+ * Arguments, layouts and results are those of gdn_prefill_chunked, without
+ * the workspace.  The scratch comes instead from one area of
+ * GDN_PREFILL_STATIC_SCRATCH_BYTES that the library declares statically in
+ * device memory, so every GPU on which the library is used holds that area
+ * until the process exits.  The call allocates and frees nothing.
+ *
+ * Limit: a problem whose gdn_prefill_workspace_bytes() exceeds
+ * GDN_PREFILL_STATIC_SCRATCH_BYTES is rejected with GDN_E_WORKSPACE before
+ * anything is enqueued (with bf16 activations and 48 v-heads, one sequence of
+ * up to 1,280 tokens fits).  Calls that need no workspace (fp32 activations,
+ * or GDN_FLAG_PREFILL_FP32) do not touch the area.
+ *
+ * Set-up: the first call on a device that needs the area looks up its device
+ * address (cudaGetSymbolAddress with that device current), which can
+ * initialise the CUDA context; make that first call before any stream
+ * capture.  A failed look-up returns GDN_E_CUDA.
+ *
+ * Sharing: every call uses the same area, which keeps the previous call's
+ * contents; nothing in it has to start at zero, because each call writes
+ * every byte it reads before reading it.  Calls whose work overlaps on the
+ * GPU (two streams, or two host threads without ordering between their
+ * streams) race on the area and corrupt each other's results: order them.
+ */
+gdn_status gdn_prefill_chunked_static(const gdn_dims* dims, const gdn_weights* w, int32_t n_seq,
+                                      const int32_t* cu_seqlens_host, const int32_t* cu_seqlens_dev,
+                                      const void* x, const void* z, const void* a_raw, const void* b_raw,
+                                      void* conv_state, float* S, int32_t zero_init, void* out,
+                                      float* prenorm_out, int32_t* dev_status, gdn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
