@@ -32,11 +32,15 @@ constexpr uint32_t kAf = 131072;       // fp32 [64][65] A
 constexpr uint32_t kTf = 147712;       // fp32 [64][65] T
 constexpr uint32_t kXf = 164352;       // fp32 [3][16][16]
 constexpr uint32_t kDm = 167424;       // fp32 [64][65] decay matrix
-constexpr uint32_t kXqk = 131072;      // staged raw q|k rows [67][512 B] (consumed before kAf.. are used)
-constexpr uint32_t kXv = 184064;       // staged raw v rows [67][256 B]
+// Raw rows are staged channel-group major: 16 bytes (8 channels) of row rr for
+// channel group cg at ((cg) * kXrows + rr) * 16, so that a warp reading one
+// channel group of 32 consecutive rows touches 512 consecutive bytes.
+constexpr int kXrows = 67;             // positions c0-3 .. c0+63
+constexpr uint32_t kXqk = 131072;      // raw q|k rows: groups 0-15 q, 16-31 k (consumed before kAf.. are used)
+constexpr uint32_t kXv = 184064;       // raw v rows: groups 0-15
 constexpr uint32_t kMisc = 201216;
 constexpr uint32_t kPrepSmem = kMisc + 1600;
-static_assert(kXqk + 67 * 512 <= kDm, "q/k staging overlaps the decay matrix");
+static_assert(kXqk + 32 * kXrows * 16 <= kDm, "q/k staging overlaps the decay matrix");
 static_assert(kDm + 64 * 65 * 4 <= kXv, "decay matrix overlaps the v staging");
 
 constexpr uint32_t kColQK = 0, kColU = 64, kColW = 128, kPrepTmemCols = 256;
@@ -111,13 +115,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
             *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     };
     for (int e = tid; e < nrow * 32; e += kPrepThreads) {
-        const int rr = e >> 5, piece = e & 31, sec = piece >> 4, off = (piece & 15) * 8;
-        stage16(sm + kXqk + rr * 512 + sec * 256 + off * 2, c0 - 3 + rr, sec * Hk * kD + kh * kD + off);
+        const int rr = e >> 5, cg = e & 31, sec = cg >> 4;
+        stage16(sm + kXqk + (cg * kXrows + rr) * 16, c0 - 3 + rr, sec * Hk * kD + kh * kD + 8 * (cg & 15));
     }
     auto stage_v = [&](int h) {
         for (int e = tid; e < nrow * 16; e += kPrepThreads) {
-            const int rr = e >> 4, off = (e & 15) * 8;
-            stage16(sm + kXv + rr * 256 + off * 2, c0 - 3 + rr, 2 * Hk * kD + h * kD + off);
+            const int rr = e >> 4, cg = e & 15;
+            stage16(sm + kXv + (cg * kXrows + rr) * 16, c0 - 3 + rr, 2 * Hk * kD + h * kD + 8 * cg);
         }
     };
     stage_v(kh);
@@ -133,37 +137,41 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
     tc::cp_async_drain();
     __syncthreads();
 
-    // ---- q_hat, k_hat: conv, SiLU, clamp L2 -> [Q;K] hi/lo in shared memory
+    // ---- q_hat, k_hat: conv, SiLU, clamp L2 -> [Q;K] hi/lo in shared memory.
+    // Thread = token t (lanes = consecutive tokens) x 64 channels: group 0/1 the
+    // low/high half of q, 2/3 the same of k; the halves' sums of squares meet in
+    // shared memory (the decay-matrix area, unused until later).
     {
-        const bool is_q = lane < 16;
-        const int l16 = lane & 15;
-        const int ch0 = (is_q ? 0 : Hk * kD) + kh * kD + 8 * l16;
-        float4 w[8];
+        const int grp = tid >> 6, t = tid & 63, sec = grp >> 1, cg0 = 16 * sec + 8 * (grp & 1);
+        const float4* wq = reinterpret_cast<const float4*>(p.conv_w) + (sec * Hk * kD + kh * kD + 64 * (grp & 1));
+        float* ssq = reinterpret_cast<float*>(sm + kDm);
+        float val[64];
+        float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const float4*>(p.conv_w + 4 * (ch0 + i));
-#pragma unroll 2
-        for (int t = warp; t < kChunk; t += 8) {
-            uint4 vh = make_uint4(0, 0, 0, 0), vl = make_uint4(0, 0, 0, 0);
-            if (t < n) {
-                float win[4][8];
+        for (int g = 0; g < 8; ++g) {
+            float win[4][8];
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    pf::bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + kXqk + (t + r) * 512 + (is_q ? 0 : 256) + 16 * l16),
-                                      win[r]);
-                float val[8], ss = 0.f;
+            for (int r = 0; r < 4; ++r)
+                pf::bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + kXqk + ((cg0 + g) * kXrows + t + r) * 16), win[r]);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    val[i] = pf::silu_fast(pf::conv4(w[i], win[0][i], win[1][i], win[2][i], win[3][i]));
-                    ss = fmaf(val[i], val[i], ss);
-                }
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);   // within 16-lane halves
-                const float inv = rsqrtf(fmaxf(ss, p.eps * p.eps));   // 1 / max(||x||, eps)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) val[i] *= inv;
-                tc::split8(val, vh, vl);
+            for (int i = 0; i < 8; ++i) {
+                const float v = t < n ? pf::silu_fast(pf::conv4(__ldg(wq + 8 * g + i), win[0][i], win[1][i], win[2][i],
+                                                                win[3][i]))
+                                      : 0.f;
+                val[8 * g + i] = v;
+                ss = fmaf(v, v, ss);
             }
-            const uint32_t so = tc::cl_off(is_q ? t : 64 + t, 8 * l16, 128);
+        }
+        ssq[grp * 64 + t] = ss;
+        __syncthreads();
+        const float inv = rsqrtf(fmaxf(ss + ssq[(grp ^ 1) * 64 + t], p.eps * p.eps));   // 1 / max(||x||, eps)
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) val[8 * g + i] *= inv;
+            uint4 vh, vl;
+            tc::split8(val + 8 * g, vh, vl);
+            const uint32_t so = tc::cl_off(64 * sec + t, 8 * (cg0 - 16 * sec + g), 128);
             *reinterpret_cast<uint4*>(sm + kQKs + so) = vh;
             *reinterpret_cast<uint4*>(sm + kQKs + 32768 + so) = vl;
         }
@@ -213,27 +221,27 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
             egam_s[2 * lane] = __expf(h0);
             egam_s[2 * lane + 1] = __expf(h1);
         }
-        // v: conv, SiLU -> V hi/lo (64 r x 128 j)
+        // v: conv, SiLU -> V hi/lo (64 r x 128 j); thread = token t x 32 channels
         {
-            float4 wv[4];
-            const int v_ch = 2 * Hk * kD + h * kD + 4 * lane;
+            const int t = tid & 63, cgb = 4 * (tid >> 6);
+            const float4* wv = reinterpret_cast<const float4*>(p.conv_w) + (2 * Hk * kD + h * kD + 8 * cgb);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) wv[i] = *reinterpret_cast<const float4*>(p.conv_w + 4 * (v_ch + i));
-#pragma unroll 2
-            for (int t = warp; t < kChunk; t += 8) {
-                uint2 vh = make_uint2(0, 0), vl = make_uint2(0, 0);
+            for (int g4 = 0; g4 < 4; ++g4) {
+                uint4 vh = make_uint4(0, 0, 0, 0), vl = make_uint4(0, 0, 0, 0);
                 if (t < n) {
-                    float winv[4][4], vv[4];
+                    float win[4][8], vv[8];
 #pragma unroll
                     for (int r = 0; r < 4; ++r)
-                        pf::bf16x4_to_f32(*reinterpret_cast<const uint2*>(sm + kXv + (t + r) * 256 + 8 * lane), winv[r]);
+                        pf::bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + kXv + ((cgb + g4) * kXrows + t + r) * 16),
+                                          win[r]);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) vv[i] = pf::silu_fast(pf::conv4(wv[i], winv[0][i], winv[1][i], winv[2][i], winv[3][i]));
-                    tc::split4(vv, vh, vl);
+                    for (int i = 0; i < 8; ++i)
+                        vv[i] = pf::silu_fast(pf::conv4(__ldg(wv + 8 * g4 + i), win[0][i], win[1][i], win[2][i], win[3][i]));
+                    tc::split8(vv, vh, vl);
                 }
-                const uint32_t ov = tc::cl_off(t, 4 * lane, 64);
-                *reinterpret_cast<uint2*>(sm + kVs + ov) = vh;
-                *reinterpret_cast<uint2*>(sm + kVs + 16384 + ov) = vl;
+                const uint32_t ov = tc::cl_off(t, 8 * (cgb + g4), 64);
+                *reinterpret_cast<uint4*>(sm + kVs + ov) = vh;
+                *reinterpret_cast<uint4*>(sm + kVs + 16384 + ov) = vl;
             }
         }
         __syncthreads();
@@ -241,7 +249,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         // decay matrix e^{Gam_t - Gam_r} (r <= t, else 0); e^Gam and e^{Gam_last - Gam_t} -> record
         {
             float* Dm = reinterpret_cast<float*>(sm + kDm);
-            const int tt = tid >> 2, r0 = (tid & 3) * 16;
+            const int tt = tid & 63, r0 = (tid >> 6) * 16;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int r = r0 + i;
@@ -256,15 +264,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         }
         __syncthreads();
         // Q' = diag(e^Gam) Q and K' = diag(e^{Gam_last - Gam}) K from the hi/lo operands -> fp16
-        // hi/lo records (thread: token tid/4, 32 indices, of Q then of K)
+        // hi/lo records (thread: token tid%64, 32 indices, of Q then of K)
 #pragma unroll 1
         for (int qk = 0; qk < 2; ++qk) {
-            const int tt = tid >> 2;
+            const int tt = tid & 63;
             const float e = qk == 0 ? egam_s[tt] : elast_s[tt];
             uint8_t* dst = vrec + (qk == 0 ? pf::kRecQhi : pf::kRecKhi);
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
-                const int i0 = 32 * (tid & 3) + 8 * g8;
+                const int i0 = 32 * (tid >> 6) + 8 * g8;
                 const uint32_t so = tc::cl_off(64 * qk + tt, i0, 128);
                 const uint4 qh = *reinterpret_cast<const uint4*>(sm + kQKs + so);
                 const uint4 ql = *reinterpret_cast<const uint4*>(sm + kQKs + 32768 + so);
@@ -318,10 +326,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         tc::fence_before_sync();
         __syncthreads();
         pf::unit_lower_inverse<kPrepThreads>(Af, reinterpret_cast<float*>(sm + kTf), reinterpret_cast<float*>(sm + kXf));
-        // T diag(beta) and T diag(beta e^Gam): thread -> row tid/4, 16 columns
+        // T diag(beta) and T diag(beta e^Gam): thread -> row tid%64, 16 columns
         {
             const float* Tf = reinterpret_cast<const float*>(sm + kTf);
-            const int tr = tid >> 2, r0 = (tid & 3) * 16;
+            const int tr = tid & 63, r0 = (tid >> 6) * 16;
 #pragma unroll
             for (int g8 = 0; g8 < 2; ++g8) {
                 float a8[8], b8[8];
