@@ -138,42 +138,55 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
     __syncthreads();
 
     // ---- q_hat, k_hat: conv, SiLU, clamp L2 -> [Q;K] hi/lo in shared memory.
-    // Thread = token t (lanes = consecutive tokens) x 64 channels: group 0/1 the
-    // low/high half of q, 2/3 the same of k; the halves' sums of squares meet in
-    // shared memory (the decay-matrix area, unused until later).
+    // Warp w owns staged channel groups 4w .. 4w+3 (q for w < 4, k for w >= 4;
+    // their conv taps held in registers), lanes = tokens lane and 32 + lane; the
+    // four warps of a section meet in shared memory (the decay-matrix area,
+    // unused until later) to form each token's norm.
     {
-        const int grp = tid >> 6, t = tid & 63, sec = grp >> 1, cg0 = 16 * sec + 8 * (grp & 1);
-        const float4* wq = reinterpret_cast<const float4*>(p.conv_w) + (sec * Hk * kD + kh * kD + 64 * (grp & 1));
-        float* ssq = reinterpret_cast<float*>(sm + kDm);
-        float val[64];
-        float ss = 0.f;
+        const int sec = warp >> 2;
+        float* ssq = reinterpret_cast<float*>(sm + kDm);   // [8 warps][64 tokens]
+        float val[2][4][8];
+        float ss[2] = {0.f, 0.f};
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-            float win[4][8];
+        for (int gq = 0; gq < 4; ++gq) {
+            const int cg = 4 * warp + gq;   // 0..31
+            const float4* wq = reinterpret_cast<const float4*>(p.conv_w) + (sec * Hk * kD + kh * kD + 8 * (cg & 15));
+            float4 w[8];
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-                pf::bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + kXqk + ((cg0 + g) * kXrows + t + r) * 16), win[r]);
+            for (int i = 0; i < 8; ++i) w[i] = __ldg(wq + i);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float v = t < n ? pf::silu_fast(pf::conv4(__ldg(wq + 8 * g + i), win[0][i], win[1][i], win[2][i],
-                                                                win[3][i]))
-                                      : 0.f;
-                val[8 * g + i] = v;
-                ss = fmaf(v, v, ss);
+            for (int hf = 0; hf < 2; ++hf) {
+                const int t = 32 * hf + lane;
+                float win[4][8];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    pf::bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + kXqk + (cg * kXrows + t + r) * 16), win[r]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float v = pf::silu_fast(pf::conv4(w[i], win[0][i], win[1][i], win[2][i], win[3][i]));
+                    val[hf][gq][i] = t < n ? v : 0.f;
+                    ss[hf] = fmaf(val[hf][gq][i], val[hf][gq][i], ss[hf]);
+                }
             }
         }
-        ssq[grp * 64 + t] = ss;
+        ssq[warp * 64 + lane] = ss[0];
+        ssq[warp * 64 + 32 + lane] = ss[1];
         __syncthreads();
-        const float inv = rsqrtf(fmaxf(ss + ssq[(grp ^ 1) * 64 + t], p.eps * p.eps));   // 1 / max(||x||, eps)
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
+        for (int hf = 0; hf < 2; ++hf) {
+            const int t = 32 * hf + lane;
+            const float* q4 = ssq + 4 * sec * 64 + t;
+            const float inv = rsqrtf(fmaxf((q4[0] + q4[64]) + (q4[128] + q4[192]), p.eps * p.eps));   // 1 / max(||x||, eps)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) val[8 * g + i] *= inv;
-            uint4 vh, vl;
-            tc::split8(val + 8 * g, vh, vl);
-            const uint32_t so = tc::cl_off(64 * sec + t, 8 * (cg0 - 16 * sec + g), 128);
-            *reinterpret_cast<uint4*>(sm + kQKs + so) = vh;
-            *reinterpret_cast<uint4*>(sm + kQKs + 32768 + so) = vl;
+            for (int gq = 0; gq < 4; ++gq) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) val[hf][gq][i] *= inv;
+                uint4 vh, vl;
+                tc::split8(val[hf][gq], vh, vl);
+                const uint32_t so = tc::cl_off(64 * sec + t, 8 * ((4 * warp + gq) & 15), 128);
+                *reinterpret_cast<uint4*>(sm + kQKs + so) = vh;
+                *reinterpret_cast<uint4*>(sm + kQKs + 32768 + so) = vl;
+            }
         }
     }
     tc::fence_proxy_async();
@@ -221,25 +234,29 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
             egam_s[2 * lane] = __expf(h0);
             egam_s[2 * lane + 1] = __expf(h1);
         }
-        // v: conv, SiLU -> V hi/lo (64 r x 128 j); thread = token t x 32 channels
-        {
-            const int t = tid & 63, cgb = 4 * (tid >> 6);
-            const float4* wv = reinterpret_cast<const float4*>(p.conv_w) + (2 * Hk * kD + h * kD + 8 * cgb);
+        // v: conv, SiLU -> V hi/lo (64 r x 128 j); warp w: channel groups 2w, 2w+1
+        // (taps in registers), lanes = tokens lane and 32 + lane
 #pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4) {
+        for (int gq = 0; gq < 2; ++gq) {
+            const int cg = 2 * warp + gq;
+            const float4* wv = reinterpret_cast<const float4*>(p.conv_w) + (2 * Hk * kD + h * kD + 8 * cg);
+            float4 w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = __ldg(wv + i);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int t = 32 * hf + lane;
                 uint4 vh = make_uint4(0, 0, 0, 0), vl = make_uint4(0, 0, 0, 0);
                 if (t < n) {
                     float win[4][8], vv[8];
 #pragma unroll
                     for (int r = 0; r < 4; ++r)
-                        pf::bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + kXv + ((cgb + g4) * kXrows + t + r) * 16),
-                                          win[r]);
+                        pf::bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + kXv + (cg * kXrows + t + r) * 16), win[r]);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        vv[i] = pf::silu_fast(pf::conv4(__ldg(wv + 8 * g4 + i), win[0][i], win[1][i], win[2][i], win[3][i]));
+                    for (int i = 0; i < 8; ++i) vv[i] = pf::silu_fast(pf::conv4(w[i], win[0][i], win[1][i], win[2][i], win[3][i]));
                     tc::split8(vv, vh, vl);
                 }
-                const uint32_t ov = tc::cl_off(t, 8 * (cgb + g4), 64);
+                const uint32_t ov = tc::cl_off(t, 8 * cg, 64);
                 *reinterpret_cast<uint4*>(sm + kVs + ov) = vh;
                 *reinterpret_cast<uint4*>(sm + kVs + 16384 + ov) = vl;
             }
