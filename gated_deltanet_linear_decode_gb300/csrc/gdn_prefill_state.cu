@@ -6,18 +6,20 @@
 // the records of the preparation kernel.
 //
 // One CTA per (sequence, v-head); the fp32 state lives in tensor memory
-// (lane j = v-row j).  Per chunk, with every product transposed so the MMA
-// runs at M = 128:
-//   Dacc = S W^T        (fp16 hi/lo of S x W^T hi, one MMA pass)
+// (lane j = v-row j), and so do its fp16 hi/lo parts and those of D, which the
+// MMAs read as their A operand straight from tensor memory (only W^T, Q', K'
+// and P come from shared memory, whose bandwidth bounds these MMAs).  Per chunk,
+// with every product transposed so the MMA runs at M = 128:
+//   Dacc = S W^T        (S hi x W^T hi, one MMA pass)
 //   O    = S Q'^T       (Q' = diag(e^Gam) Q; three passes: hi.hi + hi.lo + lo.hi)
 //   D^T  = U^T - Dacc
 //   S    = e^{Gam_last} S + D^T K'   (K' = diag(e^{Gam_last - Gam}) K; three passes)
 //   O   += D^T P^T      (three passes)
 //   o_t  = O[:, t] / sqrt(128)  -> gated RMSNorm -> out
 // Warp roles, meeting only at mbarriers:
-//   warps 0-7   convert: S -> fp16 operand (and the decay of S), Dacc -> D
-//   warps 8-11  epilogue: O -> o -> gated RMSNorm -> out, up to three chunks behind
-//               (O is triple-buffered in tensor memory; z is staged by cp.async)
+//   warps 0-7   convert: S -> fp16 hi/lo (and the decay of S), Dacc -> D hi/lo
+//   warps 8-11  epilogue: O -> o -> gated RMSNorm -> out, up to two chunks behind
+//               (O is double-buffered in tensor memory; z is staged by cp.async)
 //   warp 12     control: one lane issues the MMAs
 //   warp 13     copies: one lane issues the bulk copies of the records, each as
 //               soon as the MMAs that read its buffer have retired
@@ -36,15 +38,13 @@ constexpr int kStateThreads = (kConvWarps + kEpiWarps + 2) * 32;
 constexpr int kConvThreads = kConvWarps * 32, kEpiThreads = kEpiWarps * 32;
 
 // shared memory map (bytes)
-constexpr uint32_t kSs = 0;           // S hi +0, lo +32768        (128 j x 128 i, canonical 128 rows)
-constexpr uint32_t kDs = 65536;       // D hi +0, lo +16384        (128 j x 64 t, canonical 128 rows)
-constexpr uint32_t kQs = 98304;       // Q' hi +0, lo +16384       (64 t x 128 i, canonical 64 rows)
-constexpr uint32_t kKs = 131072;      // K' hi +0, lo +16384       (64 t x 128 i, canonical 64 rows)
-constexpr uint32_t kWs = 163840;      // W^T hi                   (128 i x 64 t, canonical 128 rows)
-constexpr uint32_t kPs = 180224;      // P hi +0, lo +8192         (64 t x 64 r, canonical 64 rows)
-constexpr uint32_t kZs = 196608;      // z of a chunk, bf16 [64 t][128 j]
-constexpr uint32_t kRs = 212992;      // RMS partial sums [2][4][64] fp32
-constexpr uint32_t kBar = 215040;     // mbarriers, then the TMEM base and the error flag
+constexpr uint32_t kQs = 0;           // Q' hi +0, lo +16384       (64 t x 128 i, canonical 64 rows)
+constexpr uint32_t kKs = 32768;       // K' hi +0, lo +16384       (64 t x 128 i, canonical 64 rows)
+constexpr uint32_t kWs = 65536;       // W^T hi                   (128 i x 64 t, canonical 128 rows)
+constexpr uint32_t kPs = 81920;       // P hi +0, lo +8192         (64 t x 64 r, canonical 64 rows)
+constexpr uint32_t kZs = 98304;       // z of even / odd chunks, bf16 [2][64 t][128 j]
+constexpr uint32_t kRs = 131072;      // RMS partial sums [2][4][64] fp32
+constexpr uint32_t kBar = 133120;     // mbarriers, then the TMEM base and the error flag
 constexpr uint32_t kStateSmem = kBar + 176;
 static_assert(kStateSmem <= 232448, "shared memory of the state pass exceeds 227 KB");
 
@@ -52,17 +52,18 @@ static_assert(kStateSmem <= 232448, "shared memory of the state pass exceeds 227
 enum : int {
     kLdW = 0, kLdQ, kLdK, kLdP,        // record copies landed (transaction count)
     kMmaD, kMmaO1, kMmaS,              // Dacc / first O group / state update retired (tcgen05.commit)
-    kODone0, kODone1, kODone2,         // O of chunks c with c % 3 = 0, 1, 2 complete
+    kODone0, kODone1,                  // O of even / odd chunks complete
     kSReady, kDReady,                  // converters wrote the S / D operands (256 arrivals)
-    kEpi0, kEpi1, kEpi2,               // epilogue done with the O buffer of chunk c % 3 = 0, 1, 2 (128 arrivals)
+    kEpi0, kEpi1,                      // epilogue done with the O buffer of even / odd chunks (128 arrivals)
     kRsReady,                          // epilogue wrote its per-token partial sums (128 arrivals)
     kZReady,                           // the epilogue's copies of a chunk's z landed (128 arrivals)
     kDrain,                            // error path: every MMA issued so far retired
     kNumBars
 };
 
-// tensor-memory columns
-constexpr uint32_t kColS = 0, kColD = 128, kColO = 192, kColG = 384;   // O: three buffers of 64; G: norm_w silu(z)
+// tensor-memory columns: S fp32, S hi / lo (fp16 pairs), Dacc fp32, D hi / lo
+// (fp16 pairs, K = 64 t), O (two buffers of 64)
+constexpr uint32_t kColS = 0, kColShi = 128, kColSlo = 192, kColD = 256, kColDhi = 320, kColDlo = 352, kColO = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kWaitLimit = 1 << 24;
 
@@ -86,7 +87,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t cnt = 1;
             if (i == kSReady || i == kDReady) cnt = kConvThreads;
-            if (i == kEpi0 || i == kEpi1 || i == kEpi2 || i == kRsReady || i == kZReady) cnt = kEpiThreads;
+            if (i == kEpi0 || i == kEpi1 || i == kRsReady || i == kZReady) cnt = kEpiThreads;
             tc::mbar_init(bars + i, cnt);
         }
         *err_s = 0;
@@ -151,45 +152,46 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
         if (lane == 0 && nch > 0) {
             bool ok = true;
             for (int c = 0; c < nch && ok; ++c) {
-                const uint32_t pc = c & 1, b = c % 3;
+                const uint32_t pc = c & 1, b = c & 1;
                 if (!(ok = wait(kSReady, pc) && wait(kLdW, pc))) break;
                 tc::fence_after_sync();
-                {   // Dacc = S W^T (1 pass, K = 128)
+                {   // Dacc = S W^T (1 pass, K = 128; A = S hi from tensor memory)
                     constexpr uint32_t id = tc::idesc_f16(128, 64, 0, 1, 0);
                     for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_f16(tmem + kColD, tc::sdesc(sb + kSs + ks * 4096, 2048, 128),
-                                    tc::sdesc(sb + kWs + ks * 256, 128, 2048), id, ks ? 1u : 0u);
+                        tc::mma_f16_ts(tmem + kColD, tmem + kColShi + 8 * ks, tc::sdesc(sb + kWs + ks * 256, 128, 2048), id,
+                                       ks ? 1u : 0u);
                     tc::mma_commit(bars + kMmaD);
                 }
-                if (!(ok = (c < 3 || wait(kEpi0 + b, ((c - 3) / 3) & 1)) && wait(kLdQ, pc))) break;
+                if (!(ok = (c < 2 || wait(kEpi0 + b, ((c - 2) >> 1) & 1)) && wait(kLdQ, pc))) break;
                 tc::fence_after_sync();
                 {   // O[b] = S Q'^T (3 passes, K = 128)
                     constexpr uint32_t id = tc::idesc_f16(128, 64, 0, 0, 0);
                     for (int ps = 0; ps < 3; ++ps) {
-                        const uint32_t ah = ps == 2 ? 32768u : 0u, bh = ps == 1 ? 16384u : 0u;
+                        const uint32_t ac = ps == 2 ? kColSlo : kColShi, bh = ps == 1 ? 16384u : 0u;
                         for (int ks = 0; ks < 8; ++ks)
-                            tc::mma_f16(tmem + kColO + 64 * b, tc::sdesc(sb + kSs + ah + ks * 4096, 2048, 128),
-                                        tc::sdesc(sb + kQs + bh + ks * 2048, 1024, 128), id, (ps | ks) ? 1u : 0u);
+                            tc::mma_f16_ts(tmem + kColO + 64 * b, tmem + ac + 8 * ks,
+                                           tc::sdesc(sb + kQs + bh + ks * 2048, 1024, 128), id, (ps | ks) ? 1u : 0u);
                     }
                     tc::mma_commit(bars + kMmaO1);
                 }
-                if (!(ok = wait(kDReady, pc) && wait(kLdK, pc) && wait(kLdP, pc))) break;
+                if (!(ok = wait(kDReady, pc) && wait(kLdK, pc))) break;
                 tc::fence_after_sync();
-                {   // S += D^T K' (3 passes, K = 64);  O[b] += D^T P^T (3 passes, K = 64)
+                {   // S += D^T K' (3 passes, K = 64);  O[b] += D^T P^T (3 passes, K = 64); A = D from tensor memory
                     constexpr uint32_t idk = tc::idesc_f16(128, 128, 0, 1, 0);
                     for (int ps = 0; ps < 3; ++ps) {
-                        const uint32_t ah = ps == 2 ? 16384u : 0u, bh = ps == 1 ? 16384u : 0u;
+                        const uint32_t ac = ps == 2 ? kColDlo : kColDhi, bh = ps == 1 ? 16384u : 0u;
                         for (int ks = 0; ks < 4; ++ks)
-                            tc::mma_f16(tmem + kColS, tc::sdesc(sb + kDs + ah + ks * 4096, 2048, 128),
-                                        tc::sdesc(sb + kKs + bh + ks * 256, 128, 1024), idk, 1u);
+                            tc::mma_f16_ts(tmem + kColS, tmem + ac + 8 * ks, tc::sdesc(sb + kKs + bh + ks * 256, 128, 1024),
+                                           idk, 1u);
                     }
                     tc::mma_commit(bars + kMmaS);
+                    if (!(ok = wait(kLdP, pc))) break;   // P is read only by the O update
                     constexpr uint32_t idp = tc::idesc_f16(128, 64, 0, 0, 0);
                     for (int ps = 0; ps < 3; ++ps) {
-                        const uint32_t ah = ps == 2 ? 16384u : 0u, bh = ps == 1 ? 8192u : 0u;
+                        const uint32_t ac = ps == 2 ? kColDlo : kColDhi, bh = ps == 1 ? 8192u : 0u;
                         for (int ks = 0; ks < 4; ++ks)
-                            tc::mma_f16(tmem + kColO + 64 * b, tc::sdesc(sb + kDs + ah + ks * 4096, 2048, 128),
-                                        tc::sdesc(sb + kPs + bh + ks * 2048, 1024, 128), idp, 1u);
+                            tc::mma_f16_ts(tmem + kColO + 64 * b, tmem + ac + 8 * ks,
+                                           tc::sdesc(sb + kPs + bh + ks * 2048, 1024, 128), idp, 1u);
                     }
                     tc::mma_commit(bars + kODone0 + b);
                 }
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
             for (int c = 1; c < 3 && c < nch; ++c) tc::bulk_prefetch_l2(vrec(c), pf::kRecU);   // toward L2
             bool ok = true;
             for (int c = 0; c + 1 < nch && ok; ++c) {
-                const uint32_t pc = c & 1, b = c % 3, pb = (c / 3) & 1;
+                const uint32_t pc = c & 1, b = c & 1, pb = (c >> 1) & 1;
                 if (c + 3 < nch) tc::bulk_prefetch_l2(vrec(c + 3), pf::kRecU);
                 if (!(ok = wait(kMmaD, pc))) break;         // W^T read by Dacc
                 load(kLdW, kWs, c + 1, pf::kRecW, 16384, req_w);
@@ -250,53 +252,45 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
                 tc::bulk_prefetch_l2(vrec(c + 1) + pf::kRecU, pf::kVRec - pf::kRecU);
             if (c > 0 && !(ok = wait(kMmaS, (c - 1) & 1))) break;
             tc::fence_after_sync();
-            // S -> fp16 hi/lo operand; S <- e^{Gam_last} S   (this thread: row j, 64 columns)
+            // S -> fp16 hi/lo pairs in tensor memory; S <- e^{Gam_last} S   (this thread: row j, 64 columns)
             {
                 float v[16];
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int col = 64 * chalf + 16 * cc;
                     tc::tmem_ld16(tl + kColS + col, v);
+                    uint32_t hi[8], lo[8];
 #pragma unroll
-                    for (int g8 = 0; g8 < 2; ++g8) {
-                        uint4 hi, lo;
-                        tc::split8(v + 8 * g8, hi, lo);
-                        const uint32_t o = tc::cl_off(row, col + 8 * g8, 128);
-                        *reinterpret_cast<uint4*>(sm + kSs + o) = hi;
-                        *reinterpret_cast<uint4*>(sm + kSs + 32768 + o) = lo;
-                    }
+                    for (int k = 0; k < 8; ++k) tc::split2(v[2 * k], v[2 * k + 1], hi[k], lo[k]);
+                    tc::tmem_st8(tl + kColShi + col / 2, hi);
+                    tc::tmem_st8(tl + kColSlo + col / 2, lo);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] *= eg_last;
                     tc::tmem_st16(tl + kColS + col, v);
                 }
                 tc::tmem_wait_st();
             }
-            tc::fence_proxy_async();
             tc::fence_before_sync();
             tc::mbar_arrive(bars + kSReady);
             if (!(ok = wait(kMmaD, pc))) break;
-            if (c > 0 && !(ok = wait(kODone0 + (c - 1) % 3, ((c - 1) / 3) & 1))) break;   // D read by O(c-1)
+            if (c > 0 && !(ok = wait(kODone0 + ((c - 1) & 1), ((c - 1) >> 1) & 1))) break;   // D read by O(c-1)
             tc::fence_after_sync();
-            // D^T = U^T - Dacc -> fp16 hi/lo operand
+            // D^T = U^T - Dacc -> fp16 hi/lo pairs in tensor memory (this thread: row j, tokens 32 chalf ..)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 float v[16];
                 tc::tmem_ld16(tl + kColD + 32 * chalf + 16 * hh, v);
+                uint32_t hi[8], lo[8];
 #pragma unroll
-                for (int g8l = 0; g8l < 2; ++g8l) {
-                    const int g8 = 2 * hh + g8l;
-                    const float4 ua = u4[2 * g8], ub = u4[2 * g8 + 1];
-                    const float d[8] = {ua.x - v[8 * g8l], ua.y - v[8 * g8l + 1], ua.z - v[8 * g8l + 2],
-                                        ua.w - v[8 * g8l + 3], ub.x - v[8 * g8l + 4], ub.y - v[8 * g8l + 5],
-                                        ub.z - v[8 * g8l + 6], ub.w - v[8 * g8l + 7]};
-                    uint4 hi, lo;
-                    const uint32_t o = tc::cl_off(row, 32 * chalf + 8 * g8, 128);
-                    tc::split8(d, hi, lo);
-                    *reinterpret_cast<uint4*>(sm + kDs + o) = hi;
-                    *reinterpret_cast<uint4*>(sm + kDs + 16384 + o) = lo;
+                for (int q = 0; q < 4; ++q) {
+                    const float4 u = u4[4 * hh + q];
+                    tc::split2(u.x - v[4 * q], u.y - v[4 * q + 1], hi[2 * q], lo[2 * q]);
+                    tc::split2(u.z - v[4 * q + 2], u.w - v[4 * q + 3], hi[2 * q + 1], lo[2 * q + 1]);
                 }
+                tc::tmem_st8(tl + kColDhi + 16 * chalf + 8 * hh, hi);
+                tc::tmem_st8(tl + kColDlo + 16 * chalf + 8 * hh, lo);
             }
-            tc::fence_proxy_async();
+            tc::tmem_wait_st();
             tc::fence_before_sync();
             tc::mbar_arrive(bars + kDReady);
         }
@@ -325,22 +319,23 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
         const int j = eq * 32 + lane, e = tid - kConvThreads;
         const uint32_t te = tmem + (static_cast<uint32_t>(eq * 32) << 16);
         float* Rs = reinterpret_cast<float*>(sm + kRs);
-        const unsigned short* zs = reinterpret_cast<const unsigned short*>(sm + kZs) + j;
+        const unsigned short* zs0 = reinterpret_cast<const unsigned short*>(sm + kZs) + j;
         const float wj = p.norm_w[j];
         const __nv_bfloat16* zh = static_cast<const __nv_bfloat16*>(p.z) + h * kD;
         Tout* __restrict__ outj = static_cast<Tout*>(p.out) + h * kD + j;
         float* __restrict__ prej = p.prenorm ? p.prenorm + h * kD + j : nullptr;
         const bool check = (p.flags & kFlagCheckFinite) != 0;
-        // chunk c's z rows (256 bytes of head h each) into shared memory by 16-byte
+        // chunk c's z rows (256 bytes of head h each) into z buffer c % 2 by 16-byte
         // asynchronous copies, zero past the sequence; they arrive on kZReady
         auto stage_z = [&](int c) {
             const int n = min(kChunk, L - c * kChunk);
             const __nv_bfloat16* src = zh + static_cast<size_t>(t0 + c * kChunk) * HvD;
+            uint8_t* dst = sm + kZs + 16384 * (c & 1);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int piece = e + kEpiThreads * k, rr = piece >> 4, c16 = piece & 15;
                 const bool valid = rr < n;
-                tc::cp_async16_zfill(sm + kZs + rr * 256 + c16 * 16, src + static_cast<size_t>(valid ? rr : 0) * HvD + c16 * 8,
+                tc::cp_async16_zfill(dst + rr * 256 + c16 * 16, src + static_cast<size_t>(valid ? rr : 0) * HvD + c16 * 8,
                                      valid ? 16u : 0u);
             }
             tc::cp_async_mbar_arrive(bars + kZReady);
@@ -348,34 +343,30 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
         if (nch > 0) stage_z(0);
         bool ok = true;
         for (int c = 0; c < nch && ok; ++c) {
-            const uint32_t b = c % 3, r = c & 1;   // O buffer, partial-sum buffer
+            const uint32_t b = c & 1;   // O, partial-sum and z buffer
+            const unsigned short* zs = zs0 + 8192 * b;
             const int c0 = c * kChunk, n = min(kChunk, L - c0);
             const size_t row0 = static_cast<size_t>(t0 + c0);
             if (c + 1 < nch && e < 2 * min(kChunk, L - c0 - kChunk))   // next chunk's z toward L2: a half row per thread
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(zh + (row0 + kChunk + (e >> 1)) * HvD + 64 * (e & 1)));
-            if (!(ok = wait(kODone0 + b, (c / 3) & 1) && wait(kZReady, c & 1))) break;
+            if (!(ok = wait(kODone0 + b, (c >> 1) & 1) && wait(kZReady, c & 1))) break;
             tc::fence_after_sync();
-            // pass 1: per-token partial sums of o^2 over this warp's 32 rows (o = O / sqrt(128)),
-            // norm_w silu(z) into the G columns
+            // pass 1: per-token partial sums of o^2 over this warp's 32 rows (o = O / sqrt(128))
 #pragma unroll 1
             for (int q = 0; q < 4; ++q) {
-                float v1[16], v2[16];
+                float v1[16];
                 tc::tmem_ld16(te + kColO + 64 * b + 16 * q, v1);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    v2[i] = wj * pf::silu_fast(__uint_as_float(static_cast<uint32_t>(zs[(16 * q + i) * kD]) << 16));
-                    v1[i] *= v1[i] * (kInvSqrtD * kInvSqrtD);
-                }
-                tc::tmem_st16(te + kColG + 16 * q, v2);
+                for (int i = 0; i < 16; ++i) v1[i] *= v1[i] * (kInvSqrtD * kInvSqrtD);
                 const float ssum = reduce16_transposed(v1);
-                if (lane < 16) Rs[(r * 4 + eq) * 64 + 16 * q + lane] = ssum;
+                if (lane < 16) Rs[(b * 4 + eq) * 64 + 16 * q + lane] = ssum;
             }
-            tc::tmem_wait_st();
             tc::mbar_arrive(bars + kRsReady);
             if (!(ok = wait(kRsReady, c & 1))) break;
-            if (c + 1 < nch) stage_z(c + 1);   // every epilogue thread is past its reads of this chunk's z
+            // every epilogue thread is past pass 2 of chunk c - 1, so z buffer (c + 1) % 2 is free
+            if (c + 1 < nch) stage_z(c + 1);
             // 1/sqrt(mean o^2 + eps) of tokens lane and 32 + lane
-            const float* rb = Rs + r * 256;
+            const float* rb = Rs + b * 256;
             const float rs_a = rsqrtf(((rb[lane] + rb[64 + lane]) + (rb[128 + lane] + rb[192 + lane])) * (1.0f / kD) + p.eps);
             const float rs_b = rsqrtf(((rb[32 + lane] + rb[96 + lane]) + (rb[160 + lane] + rb[224 + lane])) * (1.0f / kD) + p.eps);
             // pass 2: y = o * rs * norm_w silu(z); all 16 values first, then the stores
@@ -383,12 +374,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
             for (int q = 0; q < 4; ++q) {
                 float v1[16], v2[16];
                 tc::tmem_ld16(te + kColO + 64 * b + 16 * q, v1);
-                tc::tmem_ld16(te + kColG + 16 * q, v2);
                 const float rsq = q < 2 ? rs_a : rs_b;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     v1[i] *= kInvSqrtD;
-                    v2[i] *= v1[i] * __shfl_sync(0xffffffffu, rsq, (16 * q + i) & 31);
+                    const float g = wj * pf::silu_fast(__uint_as_float(static_cast<uint32_t>(zs[(16 * q + i) * kD]) << 16));
+                    v2[i] = v1[i] * __shfl_sync(0xffffffffu, rsq, (16 * q + i) & 31) * g;
                 }
                 Tout* oq = outj + (row0 + 16 * q) * HvD;
                 float* pq = prej ? prej + (row0 + 16 * q) * HvD : nullptr;
