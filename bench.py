@@ -77,6 +77,35 @@ def prefill_flops(T, Hv):
     return per * T * Hv
 
 
+def kernel_sources_hash() -> str:
+    """sha256 over the library's kernel sources and public header (sorted by name)."""
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    csrc = os.path.join(root, "gated_deltanet_linear_decode_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    files.append(os.path.join(root, "include", "gdn.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic() -> dict:
+    """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) recorded in
+    profiles/traffic.json, or {} when the kernel sources changed since they were taken."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return {}
+    if rec.get("kernel_sources_sha256") != kernel_sources_hash():
+        return {}
+    return {k: v["bytes"] for k, v in rec.get("parts", {}).items()}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -303,11 +332,13 @@ def run_gpu(args, rank, world):
     db = decode_bytes(dc.N, dc.Hk, dc.Hv)
     vb = decode_bytes(vc.N, vc.Hk, vc.Hv, K=vc.K, ckpt=True)
     pf = prefill_flops(pc.T, pc.Hv)
+    traffic = measured_traffic()
     p_roof = {"bound": "hbm", "achieved": pb / (pm / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
-              "frac": pb / (pm / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes": pb,
+              "frac": pb / (pm / 1e3) / 1e9 / hbm, "traffic": traffic.get("prefill"), "algorithmic_bytes": pb,
               "tensor_tflops_algorithmic": pf / (pm / 1e3) / 1e12, "peak_source": peak_src}
     d_roof = {"bound": "hbm", "achieved": db / (dm / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
-              "frac": db / (dm / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes": db, "peak_source": peak_src}
+              "frac": db / (dm / 1e3) / 1e9 / hbm, "traffic": traffic.get("decode"), "algorithmic_bytes": db,
+              "peak_source": peak_src}
     v_roof = {"bound": "hbm", "achieved": vb / (vm / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
               "frac": vb / (vm / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes_verify_only": vb,
               "note": "time includes the commit copy"}
