@@ -38,8 +38,10 @@ constexpr uint32_t kDm = 167424;       // fp32 [64][65] decay matrix
 constexpr int kXrows = 67;             // positions c0-3 .. c0+63
 constexpr uint32_t kXqk = 131072;      // raw q|k rows: groups 0-15 q, 16-31 k (consumed before kAf.. are used)
 constexpr uint32_t kXv = 184064;       // raw v rows: groups 0-15
-constexpr uint32_t kMisc = 201216;
-constexpr uint32_t kPrepSmem = kMisc + 1600;
+constexpr uint32_t kMisc = 201216;     // TMEM base, mbarrier, error flag
+constexpr uint32_t kGates = 201280;    // per v-head of the group: 7 x [64] fp32 (below)
+constexpr uint32_t kGateBytes = 7 * 256;
+inline uint32_t prep_smem(int G) { return kGates + static_cast<uint32_t>(G) * kGateBytes; }
 static_assert(kXqk + 32 * kXrows * 16 <= kDm, "q/k staging overlaps the decay matrix");
 static_assert(kDm + 64 * 65 * 4 <= kXv, "decay matrix overlaps the v staging");
 
@@ -65,18 +67,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
     const int n = min(kChunk, p.cu_seqlens[s + 1] - t0 - c0);
     const int nl = n - 1;
 
-    float* beta_s = reinterpret_cast<float*>(sm + kMisc);
-    float* g_s = beta_s + 64;
-    // Gam_t as an unevaluated sum ghi + glo of two floats (formed from an fp64
-    // scan), so Gam_t - Gam_r keeps fp32 relative accuracy with fp32 arithmetic.
-    float* ghi_s = beta_s + 128;
-    float* glo_s = beta_s + 192;
-    float* egam_s = beta_s + 256;
-    float* elast_s = beta_s + 320;   // e^{Gam_last - Gam_t}
-    static_assert(384 * 4 <= 1536, "misc area");
-    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sm + kMisc + 1536);
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + kMisc + 1544);
-    int* err_s = reinterpret_cast<int*>(sm + kMisc + 1552);
+    // Per v-head gate arrays (head g of the group at kGates + g * kGateBytes):
+    // beta, e^g, Gam_t as an unevaluated sum ghi + glo of two floats (formed from
+    // an fp64 scan, so Gam_t - Gam_r keeps fp32 relative accuracy), e^Gam_t and
+    // e^{Gam_last - Gam_t}.
+    auto gate = [&](int g, int k) { return reinterpret_cast<float*>(sm + kGates + g * kGateBytes) + 64 * k; };
+    enum { kBeta = 0, kEg, kGhi, kGlo, kEgam, kElast, kGraw };
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sm + kMisc);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + kMisc + 8);
+    int* err_s = reinterpret_cast<int*>(sm + kMisc + 16);
     const uint32_t sb = tc::smem_u32(sm);
 
     if (warp == 0) tc::tmem_alloc(tmem_base_s, kPrepTmemCols);
@@ -92,6 +91,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
     const int quarter = warp & 3, chalf = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float* ghi_s = nullptr;
+    const float* glo_s = nullptr;
     auto dgam = [&](int t, int r) { return (ghi_s[t] - ghi_s[r]) + (glo_s[t] - glo_s[r]); };
     uint32_t phase = 0;
     auto wait_mma = [&]() {
@@ -125,15 +126,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         }
     };
     stage_v(kh);
-    float nx_a = 0.f, nx_b = 0.f;   // raw gate inputs of token c0 + tid
-    auto load_gates = [&](int h) {
-        if (tid < n) {
-            const size_t gi = static_cast<size_t>(t0 + c0 + tid) * Hv + h;
-            nx_b = ld_act(static_cast<const __nv_bfloat16*>(p.b_raw) + gi);
-            nx_a = ld_act(static_cast<const __nv_bfloat16*>(p.a_raw) + gi);
-        }
-    };
-    load_gates(kh);
     tc::cp_async_drain();
     __syncthreads();
 
@@ -205,35 +197,55 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         tc::mma_commit(mbar);
     }
 
+    // ---- gates of every v-head of the group (while the products run): beta, g, e^g; then
+    // warp g scans head g's g in fp64 into Gam, e^Gam and e^{Gam_last - Gam}
     const int G = Hv / Hk;
+    for (int e = tid; e < kChunk * G; e += kPrepThreads) {
+        const int g = e >> 6, t = e & 63, h = kh + g * Hk;
+        float bt = 0.f, gt = 0.f;
+        if (t < n) {
+            const size_t gi = static_cast<size_t>(t0 + c0 + t) * Hv + h;
+            bt = sigmoidf_(ld_act(static_cast<const __nv_bfloat16*>(p.b_raw) + gi));
+            gt = p.ssm_a[h] * softplusf_(ld_act(static_cast<const __nv_bfloat16*>(p.a_raw) + gi) + p.dt_bias[h]);
+        }
+        gate(g, kBeta)[t] = bt;
+        gate(g, kGraw)[t] = gt;
+        gate(g, kEg)[t] = __expf(gt);
+    }
+    __syncthreads();
+    for (int g = warp; g < G; g += kPrepThreads / 32) {
+        // inclusive scan in fp64: lane l owns tokens 2l, 2l+1
+        const double g0 = static_cast<double>(gate(g, kGraw)[2 * lane]), g1 = static_cast<double>(gate(g, kGraw)[2 * lane + 1]);
+        double run = g0 + g1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double up = __shfl_up_sync(0xffffffffu, run, o);
+            if (lane >= o) run += up;
+        }
+        const double G0 = run - g1, G1 = run;
+        const double Gl = __shfl_sync(0xffffffffu, (nl & 1) ? G1 : G0, nl >> 1);   // Gam of the last token
+        const float h0 = static_cast<float>(G0), h1 = static_cast<float>(G1);
+        gate(g, kGhi)[2 * lane] = h0;
+        gate(g, kGlo)[2 * lane] = static_cast<float>(G0 - static_cast<double>(h0));
+        gate(g, kGhi)[2 * lane + 1] = h1;
+        gate(g, kGlo)[2 * lane + 1] = static_cast<float>(G1 - static_cast<double>(h1));
+        gate(g, kEgam)[2 * lane] = __expf(h0);
+        gate(g, kEgam)[2 * lane + 1] = __expf(h1);
+        gate(g, kElast)[2 * lane] = __expf(static_cast<float>(Gl - G0));
+        gate(g, kElast)[2 * lane + 1] = __expf(static_cast<float>(Gl - G1));
+    }
+    __syncthreads();
+
     const float* Af = reinterpret_cast<const float*>(sm + kAf);
     for (int g = 0; g < G; ++g) {
         const int h = kh + g * Hk;
         uint8_t* vrec = p.ws_v + (static_cast<size_t>(gc) * Hv + h) * pf::kVRec;
-        if (tid < kChunk) {
-            beta_s[tid] = tid < n ? sigmoidf_(nx_b) : 0.f;
-            g_s[tid] = tid < n ? p.ssm_a[h] * softplusf_(nx_a + p.dt_bias[h]) : 0.f;
-        }
-        __syncthreads();
-        if (g + 1 < G) load_gates(h + Hk);
-        if (warp == 0) {
-            // inclusive scan of g in fp64: lane l owns tokens 2l, 2l+1
-            const double g0 = static_cast<double>(g_s[2 * lane]), g1 = static_cast<double>(g_s[2 * lane + 1]);
-            double run = g0 + g1;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double up = __shfl_up_sync(0xffffffffu, run, o);
-                if (lane >= o) run += up;
-            }
-            const double G0 = run - g1, G1 = run;
-            const float h0 = static_cast<float>(G0), h1 = static_cast<float>(G1);
-            ghi_s[2 * lane] = h0;
-            glo_s[2 * lane] = static_cast<float>(G0 - static_cast<double>(h0));
-            ghi_s[2 * lane + 1] = h1;
-            glo_s[2 * lane + 1] = static_cast<float>(G1 - static_cast<double>(h1));
-            egam_s[2 * lane] = __expf(h0);
-            egam_s[2 * lane + 1] = __expf(h1);
-        }
+        const float* beta_s = gate(g, kBeta);
+        const float* eg_s = gate(g, kEg);
+        const float* egam_s = gate(g, kEgam);
+        const float* elast_s = gate(g, kElast);
+        ghi_s = gate(g, kGhi);
+        glo_s = gate(g, kGlo);
         // v: conv, SiLU -> V hi/lo (64 r x 128 j); warp w: channel groups 2w, 2w+1
         // (taps in registers), lanes = tokens lane and 32 + lane
 #pragma unroll
@@ -263,23 +275,24 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         }
         __syncthreads();
         if (g + 1 < G) stage_v(h + Hk);   // next v-head's raw rows load behind this head's work
-        // decay matrix e^{Gam_t - Gam_r} (r <= t, else 0); e^Gam and e^{Gam_last - Gam_t} -> record
+        // decay matrix e^{Gam_t - Gam_r} (r <= t, else 0): one exponential at the right end
+        // of the thread's 16 columns, then leftwards e^{Gam_t - Gam_{r-1}} = e^{Gam_t - Gam_r} e^{g_r};
+        // e^Gam and e^{Gam_last - Gam_t} -> record
         {
             float* Dm = reinterpret_cast<float*>(sm + kDm);
-            const int tt = tid & 63, r0 = (tid >> 6) * 16;
+            const int tt = tid & 63, r0 = (tid >> 6) * 16, rs = min(r0 + 15, tt);
+            float val = rs >= r0 ? __expf(dgam(tt, rs)) : 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 15; i >= 0; --i) {
                 const int r = r0 + i;
-                Dm[tt * 65 + r] = r <= tt ? __expf(dgam(tt, r)) : 0.f;
+                Dm[tt * 65 + r] = r <= rs ? val : 0.f;
+                if (r <= rs) val *= eg_s[r];
             }
             if (tid < kChunk) {
-                const float el = __expf(dgam(nl, tid));
-                elast_s[tid] = el;
                 reinterpret_cast<float*>(vrec + pf::kRecEgam)[tid] = egam_s[tid];
-                reinterpret_cast<float*>(vrec + pf::kRecElast)[tid] = el;
+                reinterpret_cast<float*>(vrec + pf::kRecElast)[tid] = elast_s[tid];
             }
         }
-        __syncthreads();
         // Q' = diag(e^Gam) Q and K' = diag(e^{Gam_last - Gam}) K from the hi/lo operands -> fp16
         // hi/lo records (thread: token tid%64, 32 indices, of Q then of K)
 #pragma unroll 1
@@ -457,10 +470,11 @@ cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t stream) {
 
 cudaError_t launch_chunk_prep(const PrefillParams& p, cudaStream_t stream) {
     if (p.n_chunks == 0) return cudaSuccess;
+    const uint32_t smem = prep_smem(p.Hv / p.Hk);
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kPrepSmem));
+                                         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    chunk_prep_kernel<<<dim3(static_cast<unsigned>(p.n_chunks), static_cast<unsigned>(p.Hk)), kPrepThreads, kPrepSmem,
+    chunk_prep_kernel<<<dim3(static_cast<unsigned>(p.n_chunks), static_cast<unsigned>(p.Hk)), kPrepThreads, smem,
                         stream>>>(p);
     return cudaGetLastError();
 }
