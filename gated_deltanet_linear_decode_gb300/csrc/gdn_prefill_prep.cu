@@ -4,10 +4,12 @@
 // "Architecture cheat sheet", "Gated DeltaNet layer": conv1d k=4 without bias,
 // SiLU, clamp L2 norm, tiled heads, beta = sigmoid(b), g = ssm_a softplus(a + dt_bias)).
 //
-// One CTA of 8 warps per (chunk, q/k head kh).  It computes q_hat and k_hat of
-// the chunk once and the raw products [Q; K] K^T once on the tensor cores,
-// then for each v-head h with h mod H_k = kh (tiled heads):
-//   gates, Gam (fp64 scan), e^Gam, decay matrix e^{Gam_t-Gam_r};
+// One CTA of 8 warps per (chunk, q/k head kh).  While the chunk's raw rows and
+// conv taps land it computes the gates of every v-head h with h mod H_k = kh
+// (tiled heads): beta, g, Gam (fp64 scan), e^Gam, e^{Gam_last-Gam}.  It computes
+// q_hat and k_hat of the chunk once and the raw products [Q; K] K^T once on the
+// tensor cores, then for each of those v-heads:
+//   decay matrix e^{Gam_t-Gam_r};
 //   P = decay (.) Q K^T (r <= t) -> record, A = beta decay (.) K K^T (r < t);
 //   T = (I + A)^{-1} on the CUDA cores (fp32);
 //   Q' = diag(e^Gam) Q and K' = diag(e^{Gam_last-Gam}) K -> record;
@@ -26,12 +28,11 @@ constexpr int kPrepThreads = 256;
 // shared memory map (bytes)
 constexpr uint32_t kQKs = 0;           // [Q;K] hi +0, lo +32768   (128 rows x 128, canonical)
 constexpr uint32_t kVs = 65536;        // V hi +0, lo +16384       (64 r x 128 j, canonical 64 rows)
-constexpr uint32_t kTb = 98304;        // T diag(beta) hi +0, lo +8192
-constexpr uint32_t kTbe = 114688;      // T diag(beta e^Gam) hi +0, lo +8192
-constexpr uint32_t kAf = 131072;       // fp32 [64][65] A
-constexpr uint32_t kTf = 147712;       // fp32 [64][65] T
-constexpr uint32_t kXf = 164352;       // fp32 [3][16][16]
-constexpr uint32_t kDm = 167424;       // fp32 [64][65] decay matrix
+constexpr uint32_t kTb = 98304;        // T diag(beta) hi +0, lo +8192 (first: q/k conv taps, float4 [256])
+constexpr uint32_t kTbe = 114688;      // T diag(beta e^Gam) hi +0, lo +8192 (first: raw gates g [G][64])
+constexpr uint32_t kAf = 131072;       // fp32 [64][pf::kTS] A
+constexpr uint32_t kTf = 148480;       // fp32 [64][pf::kTS] T
+constexpr uint32_t kDm = 167424;       // fp32 [64][65] decay matrix; then the solve's scratch (11520 bytes)
 // Raw rows are staged channel-group major: 16 bytes (8 channels) of row rr for
 // channel group cg at ((cg) * kXrows + rr) * 16, so that a warp reading one
 // channel group of 32 consecutive rows touches 512 consecutive bytes.
@@ -39,11 +40,15 @@ constexpr int kXrows = 67;             // positions c0-3 .. c0+63
 constexpr uint32_t kXqk = 131072;      // raw q|k rows: groups 0-15 q, 16-31 k (consumed before kAf.. are used)
 constexpr uint32_t kXv = 184064;       // raw v rows: groups 0-15
 constexpr uint32_t kMisc = 201216;     // TMEM base, mbarrier, error flag
-constexpr uint32_t kGates = 201280;    // per v-head of the group: 7 x [64] fp32 (below)
-constexpr uint32_t kGateBytes = 7 * 256;
-inline uint32_t prep_smem(int G) { return kGates + static_cast<uint32_t>(G) * kGateBytes; }
+constexpr uint32_t kGates = 201280;    // per v-head of the group: 6 x [64] fp32 (below)
+constexpr uint32_t kGateBytes = 6 * 256;
+// then the conv taps of the current v-head, float4 [128]
+__host__ __device__ inline uint32_t taps_v_off(int G) { return kGates + static_cast<uint32_t>(G) * kGateBytes; }
+inline uint32_t prep_smem(int G) { return taps_v_off(G) + 128 * 16; }
 static_assert(kXqk + 32 * kXrows * 16 <= kDm, "q/k staging overlaps the decay matrix");
 static_assert(kDm + 64 * 65 * 4 <= kXv, "decay matrix overlaps the v staging");
+static_assert(kXv + 16 * kXrows * 16 <= kMisc, "v staging overlaps the barriers");
+static_assert(kAf + 64 * pf::kTS * 4 <= kTf && kTf + 64 * pf::kTS * 4 <= kDm, "A / T tiles overlap");
 
 constexpr uint32_t kColQK = 0, kColU = 64, kColW = 128, kPrepTmemCols = 256;
 constexpr int kWaitLimit = 1 << 22;
@@ -72,7 +77,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
     // an fp64 scan, so Gam_t - Gam_r keeps fp32 relative accuracy), e^Gam_t and
     // e^{Gam_last - Gam_t}.
     auto gate = [&](int g, int k) { return reinterpret_cast<float*>(sm + kGates + g * kGateBytes) + 64 * k; };
-    enum { kBeta = 0, kEg, kGhi, kGlo, kEgam, kElast, kGraw };
+    enum { kBeta = 0, kEg, kGhi, kGlo, kEgam, kElast };
+    const int G = Hv / Hk;
+    const float4* taps_qk = reinterpret_cast<const float4*>(sm + kTb);
+    const float4* taps_v = reinterpret_cast<const float4*>(sm + taps_v_off(G));
     uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sm + kMisc);
     uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + kMisc + 8);
     int* err_s = reinterpret_cast<int*>(sm + kMisc + 16);
@@ -103,7 +111,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
     };
 
     // ---- stage the raw rows of positions c0-3 .. c0+n-1 (left context from the
-    // carried conv state in the first chunk of a sequence)
+    // carried conv state in the first chunk of a sequence) and the conv taps
     const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x);
     const __nv_bfloat16* cst = static_cast<const __nv_bfloat16*>(p.conv_state) + static_cast<size_t>(s) * 3 * C;
     const int nrow = n + 3;
@@ -119,13 +127,60 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         const int rr = e >> 5, cg = e & 31, sec = cg >> 4;
         stage16(sm + kXqk + (cg * kXrows + rr) * 16, c0 - 3 + rr, sec * Hk * kD + kh * kD + 8 * (cg & 15));
     }
+    static_assert(kPrepThreads == 256, "one q/k channel's taps per thread");
+    tc::cp_async16(sm + kTb + 16 * tid,
+                   reinterpret_cast<const float4*>(p.conv_w) + ((tid >> 7) * Hk * kD + kh * kD + (tid & 127)));
+    // v-head h's raw rows and conv taps
     auto stage_v = [&](int h) {
         for (int e = tid; e < nrow * 16; e += kPrepThreads) {
             const int rr = e >> 4, cg = e & 15;
             stage16(sm + kXv + (cg * kXrows + rr) * 16, c0 - 3 + rr, 2 * Hk * kD + h * kD + 8 * cg);
         }
+        if (tid < kD)
+            tc::cp_async16(sm + taps_v_off(G) + 16 * tid, reinterpret_cast<const float4*>(p.conv_w) + (2 * Hk * kD + h * kD + tid));
     };
     stage_v(kh);
+
+    // ---- gates of every v-head of the group while the rows land: beta, g, e^g; then
+    // warp g scans head g's g in fp64 into Gam, e^Gam and e^{Gam_last - Gam}
+    {
+        float* graw = reinterpret_cast<float*>(sm + kTbe);   // [G][64]
+        static_assert(16 * 64 * 4 <= 16384, "raw gates of up to 16 v-heads");
+        for (int e = tid; e < kChunk * G; e += kPrepThreads) {
+            const int g = e >> 6, t = e & 63, h = kh + g * Hk;
+            float bt = 0.f, gt = 0.f;
+            if (t < n) {
+                const size_t gi = static_cast<size_t>(t0 + c0 + t) * Hv + h;
+                bt = sigmoidf_(ld_act(static_cast<const __nv_bfloat16*>(p.b_raw) + gi));
+                gt = p.ssm_a[h] * softplusf_(ld_act(static_cast<const __nv_bfloat16*>(p.a_raw) + gi) + p.dt_bias[h]);
+            }
+            gate(g, kBeta)[t] = bt;
+            graw[e] = gt;
+            gate(g, kEg)[t] = __expf(gt);
+        }
+        __syncthreads();
+        for (int g = warp; g < G; g += kPrepThreads / 32) {
+            // inclusive scan in fp64: lane l owns tokens 2l, 2l+1
+            const double g0 = static_cast<double>(graw[64 * g + 2 * lane]), g1 = static_cast<double>(graw[64 * g + 2 * lane + 1]);
+            double run = g0 + g1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double up = __shfl_up_sync(0xffffffffu, run, o);
+                if (lane >= o) run += up;
+            }
+            const double G0 = run - g1, G1 = run;
+            const double Gl = __shfl_sync(0xffffffffu, (nl & 1) ? G1 : G0, nl >> 1);   // Gam of the last token
+            const float h0 = static_cast<float>(G0), h1 = static_cast<float>(G1);
+            gate(g, kGhi)[2 * lane] = h0;
+            gate(g, kGlo)[2 * lane] = static_cast<float>(G0 - static_cast<double>(h0));
+            gate(g, kGhi)[2 * lane + 1] = h1;
+            gate(g, kGlo)[2 * lane + 1] = static_cast<float>(G1 - static_cast<double>(h1));
+            gate(g, kEgam)[2 * lane] = __expf(h0);
+            gate(g, kEgam)[2 * lane + 1] = __expf(h1);
+            gate(g, kElast)[2 * lane] = __expf(static_cast<float>(Gl - G0));
+            gate(g, kElast)[2 * lane + 1] = __expf(static_cast<float>(Gl - G1));
+        }
+    }
     tc::cp_async_drain();
     __syncthreads();
 
@@ -142,10 +197,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
 #pragma unroll
         for (int gq = 0; gq < 4; ++gq) {
             const int cg = 4 * warp + gq;   // 0..31
-            const float4* wq = reinterpret_cast<const float4*>(p.conv_w) + (sec * Hk * kD + kh * kD + 8 * (cg & 15));
             float4 w[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) w[i] = __ldg(wq + i);
+            for (int i = 0; i < 8; ++i) w[i] = taps_qk[sec * kD + 8 * (cg & 15) + i];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int t = 32 * hf + lane;
@@ -197,45 +251,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         tc::mma_commit(mbar);
     }
 
-    // ---- gates of every v-head of the group (while the products run): beta, g, e^g; then
-    // warp g scans head g's g in fp64 into Gam, e^Gam and e^{Gam_last - Gam}
-    const int G = Hv / Hk;
-    for (int e = tid; e < kChunk * G; e += kPrepThreads) {
-        const int g = e >> 6, t = e & 63, h = kh + g * Hk;
-        float bt = 0.f, gt = 0.f;
-        if (t < n) {
-            const size_t gi = static_cast<size_t>(t0 + c0 + t) * Hv + h;
-            bt = sigmoidf_(ld_act(static_cast<const __nv_bfloat16*>(p.b_raw) + gi));
-            gt = p.ssm_a[h] * softplusf_(ld_act(static_cast<const __nv_bfloat16*>(p.a_raw) + gi) + p.dt_bias[h]);
-        }
-        gate(g, kBeta)[t] = bt;
-        gate(g, kGraw)[t] = gt;
-        gate(g, kEg)[t] = __expf(gt);
-    }
-    __syncthreads();
-    for (int g = warp; g < G; g += kPrepThreads / 32) {
-        // inclusive scan in fp64: lane l owns tokens 2l, 2l+1
-        const double g0 = static_cast<double>(gate(g, kGraw)[2 * lane]), g1 = static_cast<double>(gate(g, kGraw)[2 * lane + 1]);
-        double run = g0 + g1;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double up = __shfl_up_sync(0xffffffffu, run, o);
-            if (lane >= o) run += up;
-        }
-        const double G0 = run - g1, G1 = run;
-        const double Gl = __shfl_sync(0xffffffffu, (nl & 1) ? G1 : G0, nl >> 1);   // Gam of the last token
-        const float h0 = static_cast<float>(G0), h1 = static_cast<float>(G1);
-        gate(g, kGhi)[2 * lane] = h0;
-        gate(g, kGlo)[2 * lane] = static_cast<float>(G0 - static_cast<double>(h0));
-        gate(g, kGhi)[2 * lane + 1] = h1;
-        gate(g, kGlo)[2 * lane + 1] = static_cast<float>(G1 - static_cast<double>(h1));
-        gate(g, kEgam)[2 * lane] = __expf(h0);
-        gate(g, kEgam)[2 * lane + 1] = __expf(h1);
-        gate(g, kElast)[2 * lane] = __expf(static_cast<float>(Gl - G0));
-        gate(g, kElast)[2 * lane + 1] = __expf(static_cast<float>(Gl - G1));
-    }
-    __syncthreads();
-
     const float* Af = reinterpret_cast<const float*>(sm + kAf);
     for (int g = 0; g < G; ++g) {
         const int h = kh + g * Hk;
@@ -251,10 +266,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
 #pragma unroll
         for (int gq = 0; gq < 2; ++gq) {
             const int cg = 2 * warp + gq;
-            const float4* wv = reinterpret_cast<const float4*>(p.conv_w) + (2 * Hk * kD + h * kD + 8 * cg);
             float4 w[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) w[i] = __ldg(wv + i);
+            for (int i = 0; i < 8; ++i) w[i] = taps_v[8 * cg + i];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int t = 32 * hf + lane;
@@ -349,13 +363,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int r = 32 * chalf + i;
-                    Afw[t * 65 + r] = r < t ? bt * Dm[t * 65 + r] * v[i] : 0.f;
+                    Afw[t * pf::kTS + r] = r < t ? bt * Dm[t * 65 + r] * v[i] : 0.f;
                 }
             }
         }
         tc::fence_before_sync();
         __syncthreads();
-        pf::unit_lower_inverse<kPrepThreads>(Af, reinterpret_cast<float*>(sm + kTf), reinterpret_cast<float*>(sm + kXf));
+        pf::unit_lower_inverse<kPrepThreads>(Af, reinterpret_cast<float*>(sm + kTf), reinterpret_cast<float*>(sm + kDm));
         // T diag(beta) and T diag(beta e^Gam): thread -> row tid%64, 16 columns
         {
             const float* Tf = reinterpret_cast<const float*>(sm + kTf);
@@ -366,7 +380,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int r = r0 + 8 * g8 + i;
-                    const float tb = Tf[tr * 65 + r] * beta_s[r];
+                    const float tb = (r >> 4) <= (tr >> 4) ? Tf[tr * pf::kTS + r] * beta_s[r] : 0.f;   // T is lower
                     a8[i] = tb;
                     b8[i] = tb * egam_s[r];
                 }

@@ -72,64 +72,129 @@ __device__ __forceinline__ void st_out4(__nv_bfloat16* p, const float (&y)[4]) {
         make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
 }
 
-// (I + A)^{-1} for a strictly lower 64 x 64 A (fp32, row stride 65), by a
-// block of kThreads >= 192 threads: the four 16 x 16 diagonal blocks by forward
-// substitution (column c of block b per thread, each solved value folded into
-// the rows below it at once), then the off-diagonal blocks level by level,
-// T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, four adjacent columns of one row per
-// thread.  Xf is fp32 scratch [3][16][16].  Ends with a block barrier.
+// acc[x][0..3] += sum_{m<16} ax[m] b[m * bs + 0..3] for the rows a0, a1
+// (a0, a1, b and bs * 4 bytes 16-byte aligned)
+__device__ __forceinline__ void mac16x2x4(const float* a0, const float* a1, const float* b, int bs, float (&acc)[2][4]) {
+#pragma unroll
+    for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 u = *reinterpret_cast<const float4*>(a0 + 4 * m4);
+        const float4 v = *reinterpret_cast<const float4*>(a1 + 4 * m4);
+        const float au[4] = {u.x, u.y, u.z, u.w}, av[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+            const float4 bv = *reinterpret_cast<const float4*>(b + (4 * m4 + mm) * bs);
+            const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[0][e] = fmaf(au[mm], bb[e], acc[0][e]);
+                acc[1][e] = fmaf(av[mm], bb[e], acc[1][e]);
+            }
+        }
+    }
+}
+
+// (I + A)^{-1} for a strictly lower 64 x 64 A, by a block of 256 threads, in
+// 16 x 16 blocks.  A and T are fp32 with row stride kTS (16-byte rows).
+//   1. D_b = (I + A_bb)^{-1}, the diagonal blocks of T, by forward substitution:
+//      column c of block b per thread, with the lower triangle of A_bb in its
+//      registers, each solved value folded into the rows below it at once.
+//   2. Ahat_ij = D_i A_ij for the six blocks below the diagonal.
+//   3. T_ij = -sum_{k=j}^{i-1} Ahat_ik T_kj (from (I + A_ii) T_ij = -sum_{k<i}
+//      A_ik T_kj), block diagonal by block diagonal; each step also forms the
+//      sums over k that the next one can already take, so that every step has
+//      work for most threads: step a gives T10, T21, T32 and Q20 = Ahat20 D0,
+//      Q31 = Ahat31 D1, Q30 = Ahat30 D0; step b gives T20 = -(Q20 + Ahat21 T10),
+//      T31 = -(Q31 + Ahat32 T21), R30 = Q30 + Ahat31 T10; step c gives
+//      T30 = -(R30 + Ahat32 T20).
+// In 2 and 3 a thread computes rows r and r + 8, columns 4c .. 4c + 3 of a
+// block, from 16-byte shared-memory loads (no bank conflicts at row strides
+// kTS and 20).  The strictly upper blocks of T are not written (callers treat
+// them as zero).  Hf is fp32 scratch for nine 16 x 16 blocks of row stride 20
+// (11520 bytes).  Ends with a block barrier.
+constexpr int kTS = 68;
 template <int kThreads>
-__device__ void unit_lower_inverse(const float* Af, float* Tf, float* Xf) {
+__device__ void unit_lower_inverse(const float* Af, float* Tf, float* Hf) {
+    static_assert(kThreads == 256, "tilings below assume 256 threads");
+    constexpr int kHS = 20;                  // row stride of a scratch block
     const int tid = threadIdx.x;
     if (tid < 64) {
-        const int b = tid >> 4, c = tid & 15, o = 16 * b;
+        const int o = 16 * (tid >> 4), c = tid & 15;
+        float a[16][16];   // a[t][m] = A_bb[t][m] for m < t (in 16-byte pieces; the rest unused)
+#pragma unroll
+        for (int t = 1; t < 16; ++t)
+#pragma unroll
+            for (int m4 = 0; 4 * m4 < t; ++m4) {
+                const float4 v = *reinterpret_cast<const float4*>(Af + (o + t) * kTS + o + 4 * m4);
+                a[t][4 * m4] = v.x; a[t][4 * m4 + 1] = v.y; a[t][4 * m4 + 2] = v.z; a[t][4 * m4 + 3] = v.w;
+            }
         float x[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) x[t] = t == c ? 1.f : 0.f;
 #pragma unroll
         for (int r = 0; r < 15; ++r)
 #pragma unroll
-            for (int t = r + 1; t < 16; ++t) x[t] = fmaf(-Af[(o + t) * 65 + o + r], x[r], x[t]);
+            for (int t = r + 1; t < 16; ++t) x[t] = fmaf(-a[t][r], x[r], x[t]);
 #pragma unroll
-        for (int t = 0; t < 16; ++t) Tf[(o + t) * 65 + o + c] = x[t];
-    }
-    for (int e = tid; e < 64 * 64; e += kThreads) {
-        const int i = e >> 6, j = e & 63;
-        if ((i >> 4) < (j >> 4)) Tf[i * 65 + j] = 0.f;
+        for (int t = 0; t < 16; ++t) Tf[(o + t) * kTS + o + c] = x[t];
     }
     __syncthreads();
-    for (int d = 1; d < 4; ++d) {
-        const int nb = 4 - d;
-        if (tid < nb * 64) {
-            const int bi = d + (tid >> 6), bj = bi - d, rr = (tid >> 2) & 15, cc = (tid & 3) * 4;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int k = bj; k < bi; ++k)
+    // scratch blocks: Ahat (1,0) (2,0) (2,1) (3,0) (3,1) (3,2) at 0..5; Q20, Q31, Q30 / R30 at 6..8
+    auto hb = [&](int k) { return Hf + k * 16 * kHS; };
+    auto ah = [](int i, int j) { return i * (i - 1) / 2 + j; };
+    const int q = tid & 31, r = q >> 2, c4 = 4 * (q & 3);   // rows r, r + 8 and columns c4 .. c4+3 of a block
+    auto tblk = [&](int i, int j) { return Tf + (16 * i) * kTS + 16 * j; };
+    auto mac = [&](const float* a, int as, const float* b, int bs, float (&acc)[2][4]) {
+        mac16x2x4(a + r * as, a + (r + 8) * as, b + c4, bs, acc);
+    };
+    auto store = [&](float* dst, int stride, const float (&v)[2][4], float sg) {
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float a = Af[(16 * bi + rr) * 65 + 16 * k + m];
-                    const float* tr = Tf + (16 * k + m) * 65 + 16 * bj + cc;
+        for (int x = 0; x < 2; ++x)
+            *reinterpret_cast<float4*>(dst + (r + 8 * x) * stride + c4) =
+                make_float4(sg * v[x][0], sg * v[x][1], sg * v[x][2], sg * v[x][3]);
+    };
+    auto load = [&](const float* src, float (&v)[2][4]) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[q] = fmaf(a, tr[q], acc[q]);
-                }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) Xf[(tid >> 6) * 256 + rr * 16 + cc + q] = acc[q];
+        for (int x = 0; x < 2; ++x) {
+            const float4 f = *reinterpret_cast<const float4*>(src + (r + 8 * x) * kHS + c4);
+            v[x][0] = f.x; v[x][1] = f.y; v[x][2] = f.z; v[x][3] = f.w;
         }
-        __syncthreads();
-        if (tid < nb * 64) {
-            const int bi = d + (tid >> 6), bj = bi - d, rr = (tid >> 2) & 15, cc = (tid & 3) * 4;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float a = Tf[(16 * bi + rr) * 65 + 16 * bi + m];
-                const float* xr = Xf + (tid >> 6) * 256 + m * 16 + cc;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[q] = fmaf(a, xr[q], acc[q]);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) Tf[(16 * bi + rr) * 65 + 16 * bj + cc + q] = -acc[q];
-        }
-        __syncthreads();
+    };
+    // 2. Ahat_ij = D_i A_ij: items 0..191 (block = item / 32)
+    if (tid < 6 * 32) {
+        const int k = tid >> 5, i = k < 1 ? 1 : k < 3 ? 2 : 3, j = k - i * (i - 1) / 2;
+        float acc[2][4] = {};
+        mac(tblk(i, i), kTS, Af + (16 * i) * kTS + 16 * j, kTS, acc);
+        store(hb(k), kHS, acc, 1.f);
     }
+    __syncthreads();
+    // 3a. T10, T21, T32 and Q20, Q31, Q30
+    if (tid < 6 * 32) {
+        // Ahat block (i, j) times D_j: (1,0) (2,1) (3,2) give T blocks, (2,0) (3,1) (3,0) the Q sums
+        const int k = tid >> 5, i = k < 3 ? k + 1 : (k == 3 ? 2 : 3), j = k < 3 ? k : (k == 4 ? 1 : 0);
+        float acc[2][4] = {};
+        mac(hb(ah(i, j)), kHS, tblk(j, j), kTS, acc);
+        if (k < 3) store(tblk(i, j), kTS, acc, -1.f);
+        else store(hb(3 + k), kHS, acc, 1.f);
+    }
+    __syncthreads();
+    // 3b. T20 = -(Q20 + Ahat21 T10), T31 = -(Q31 + Ahat32 T21), R30 = Q30 + Ahat31 T10
+    if (tid < 3 * 32) {
+        const int k = tid >> 5, i = k ? 3 : 2, kk = k == 1 ? 2 : 1, j = k == 1 ? 1 : 0;
+        float acc[2][4];
+        load(hb(6 + k), acc);
+        mac(hb(ah(i, kk)), kHS, tblk(kk, j), kTS, acc);
+        if (k < 2) store(tblk(i, j), kTS, acc, -1.f);
+        else store(hb(8), kHS, acc, 1.f);
+    }
+    __syncthreads();
+    // 3c. T30 = -(R30 + Ahat32 T20)
+    if (tid < 32) {
+        float acc[2][4];
+        load(hb(8), acc);
+        mac(hb(ah(3, 2)), kHS, tblk(2, 0), kTS, acc);
+        store(tblk(3, 0), kTS, acc, -1.f);
+    }
+    __syncthreads();
 }
 
 }  // namespace pf
