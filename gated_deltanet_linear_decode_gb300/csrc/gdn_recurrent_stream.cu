@@ -13,9 +13,12 @@
 // every item a bulk asynchronous copy (cp.async.bulk, completion counted on an
 // mbarrier) lands the head's 128 x 128 state tile and its inputs -- the raw
 // rows of its q/k/v channels, z, conv taps -- in one of two shared-memory
-// stages, two items ahead of the compute.  On arrival the state goes to
-// registers (warp w owns rows 16w..16w+15, lane = 4 consecutive columns) and
-// the small inputs to a private area, so the stage is refilled at once.
+// stages, two items ahead of the compute.  A producer warp issues the copies
+// (issuing a bulk copy takes the issuing thread about as long as the copy
+// engine needs for it, so it is kept off the compute warps).  On arrival the
+// state goes to registers (warp w owns rows 16w..16w+15, lane = 4 consecutive
+// columns) and the small inputs to a private area, and the stage is handed
+// back to the producer at once.
 //
 // S.k and S.q of a warp's 16 rows (32 partial sums per lane) are reduced with
 // one transposed butterfly (31 shuffles).  Decode and verify share this code,
@@ -28,8 +31,13 @@ namespace gdn {
 
 namespace {
 
-constexpr int kSThreads = 256;     // 8 warps x 16 rows
+constexpr int kSThreads = 256;     // compute: 8 warps x 16 rows
+constexpr int kProducerWarp = kSThreads / 32;
+constexpr int kLaunchThreads = kSThreads + 32;
 constexpr int kStages = 2;
+
+// Barrier among the compute warps only (the producer warp never joins it).
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSThreads) : "memory"); }
 
 __device__ __forceinline__ float conv4(float4 w, float x0, float x1, float x2, float cur) {
     return fmaf(w.w, cur, fmaf(w.z, x2, fmaf(w.y, x1, w.x * x0)));
@@ -57,7 +65,7 @@ struct StageLayout {
 };
 
 template <typename Tact, typename Tout>
-__global__ void __launch_bounds__(kSThreads, 1)
+__global__ void __launch_bounds__(kLaunchThreads, 1)
 recurrent_stream_kernel(const RecParams p) {
     extern __shared__ __align__(128) uint8_t sm[];
     constexpr int es = sizeof(Tact);
@@ -76,10 +84,14 @@ recurrent_stream_kernel(const RecParams p) {
     float* part = red + 16;                                                       // [8]
     float* gates = part + 8;                                                      // [K][2]
     float* nw_s = gates + 2 * kMaxK;                                              // [128]
-    uint64_t* full = reinterpret_cast<uint64_t*>(nw_s + 128);                     // [kStages]
+    uint64_t* full = reinterpret_cast<uint64_t*>(nw_s + 128);                     // [kStages] stage landed
+    uint64_t* empty = full + kStages;                                              // [kStages] stage copied out
 
     if (tid == 0)
-        for (int st = 0; st < kStages; ++st) tc::mbar_init(&full[st], 1);
+        for (int st = 0; st < kStages; ++st) {
+            tc::mbar_init(&full[st], 1);
+            tc::mbar_init(&empty[st], 1);
+        }
     if (tid < kD) nw_s[tid] = p.norm_w[tid];
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
@@ -115,8 +127,19 @@ recurrent_stream_kernel(const RecParams p) {
         for (int t = 0; t < K; ++t) bulk_g2s(base + L.zr + t * seg, zin + static_cast<size_t>(t) * HvD, seg, mb);
     };
 
-    if (tid == 0)
-        for (int i = 0; i < kStages && i < n_items; ++i) issue(i);
+    if (warp == kProducerWarp) {
+        // ================= producer: item i into stage i % kStages once item i - kStages has left it
+        if (lane == 0)
+            for (int i = 0; i < n_items; ++i) {
+                const int st = i % kStages;
+                if (i >= kStages && !tc::mbar_wait(&empty[st], ((i / kStages) - 1) & 1, 1 << 22)) {
+                    const int g = item_group(i);
+                    if (p.dev_status) atomicOr(p.dev_status + (g / p.Hk) * p.Hv + g % p.Hk, 16);
+                }
+                issue(i);
+            }
+        return;
+    }
 
     float4 sreg[16];
     for (int i = 0; i < n_items; ++i) {
@@ -144,8 +167,8 @@ recurrent_stream_kernel(const RecParams p) {
             gates[2 * tid] = sigmoidf_(b_raw);
             gates[2 * tid + 1] = a_ssm * softplusf_(a_raw + a_dt);
         }
-        __syncthreads();
-        if (tid == 0 && i + kStages < n_items) issue(i + kStages);
+        compute_sync();
+        if (tid == 0) tc::mbar_arrive(&empty[i % kStages]);   // the stage may be refilled
 
         const float4* cw = reinterpret_cast<const float4*>(cur);                      // [384] taps
         const Tact* xr = reinterpret_cast<const Tact*>(cur + (L.xr - 65536));          // [K+3][384]
@@ -163,11 +186,11 @@ recurrent_stream_kernel(const RecParams p) {
                     v_s[t * kD + tid] =
                         siluf_(conv4(wv, to_f(xr[t * 384 + 256 + tid]), to_f(xr[(t + 1) * 384 + 256 + tid]),
                                      to_f(xr[(t + 2) * 384 + 256 + tid]), to_f(xr[(t + 3) * 384 + 256 + tid])));
-                __syncthreads();
+                compute_sync();
                 const float* rd = red + (warp >> 2) * 8;
                 const float nrm = sqrtf((rd[0] + rd[1]) + (rd[2] + rd[3]));
                 qk_s[t * 256 + tid] = val / fmaxf(nrm, p.eps);
-                __syncthreads();
+                compute_sync();
             }
         }
 
@@ -213,7 +236,7 @@ recurrent_stream_kernel(const RecParams p) {
             }
             if (lane & 1) o_s[warp * 16 + my_row] = o;
             if (lane == 0) part[warp] = ps;
-            __syncthreads();
+            compute_sync();
             // ---- step 8: gated RMSNorm, thread c < 128 -> output j = c
             const size_t row = static_cast<size_t>(b) * K + t;
             if (tid < kD) {
@@ -243,7 +266,7 @@ recurrent_stream_kernel(const RecParams p) {
 #pragma unroll
                 for (int q = 0; q < 3; ++q) cout[q * C + ch] = xr[(t + 1 + q) * 384 + tid];
             }
-            __syncthreads();
+            compute_sync();
         }
     }
 }
@@ -254,7 +277,7 @@ size_t recurrent_stream_smem(int K, int act_dtype) {
     const int es = act_dtype == 1 ? 2 : 4;
     const StageLayout L(K, es);
     const size_t cur = ((L.bytes - 65536 + 15) & ~static_cast<size_t>(15));
-    const size_t misc = (static_cast<size_t>(K) * 384 + 128 + 16 + 8 + 2 * kMaxK + 128) * 4 + kStages * 8;
+    const size_t misc = (static_cast<size_t>(K) * 384 + 128 + 16 + 8 + 2 * kMaxK + 128) * 4 + 2 * kStages * 8;
     return kStages * static_cast<size_t>(L.bytes) + cur + misc;
 }
 
@@ -263,7 +286,7 @@ cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_d
     auto go = [&](auto kernel) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        kernel<<<grid, kSThreads, smem, stream>>>(p);
+        kernel<<<grid, kLaunchThreads, smem, stream>>>(p);
         return cudaGetLastError();
     };
     if (act_dtype == 1)
