@@ -361,9 +361,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
             } else {
                 const float bt = beta_s[t];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int r = 32 * chalf + i;
-                    Afw[t * pf::kTS + r] = r < t ? bt * Dm[t * 65 + r] * v[i] : 0.f;
+                for (int i = 0; i < 32; i += 4) {   // 16-byte stores: a row per lane, no bank conflicts
+                    float a4[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int r = 32 * chalf + i + k;
+                        a4[k] = r < t ? bt * Dm[t * 65 + r] * v[i + k] : 0.f;
+                    }
+                    *reinterpret_cast<float4*>(Afw + t * pf::kTS + 32 * chalf + i) = make_float4(a4[0], a4[1], a4[2], a4[3]);
                 }
             }
         }
@@ -377,10 +382,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
 #pragma unroll
             for (int g8 = 0; g8 < 2; ++g8) {
                 float a8[8], b8[8];
+                const bool lower = (r0 >> 4) <= (tr >> 4);   // T is block lower triangular
+                float t8[8] = {};
+                if (lower) {   // 16-byte loads: a row per lane, no bank conflicts
+                    const float4 u = *reinterpret_cast<const float4*>(Tf + tr * pf::kTS + r0 + 8 * g8);
+                    const float4 w = *reinterpret_cast<const float4*>(Tf + tr * pf::kTS + r0 + 8 * g8 + 4);
+                    t8[0] = u.x; t8[1] = u.y; t8[2] = u.z; t8[3] = u.w; t8[4] = w.x; t8[5] = w.y; t8[6] = w.z; t8[7] = w.w;
+                }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int r = r0 + 8 * g8 + i;
-                    const float tb = (r >> 4) <= (tr >> 4) ? Tf[tr * pf::kTS + r] * beta_s[r] : 0.f;   // T is lower
+                    const float tb = t8[i] * beta_s[r];
                     a8[i] = tb;
                     b8[i] = tb * egam_s[r];
                 }
