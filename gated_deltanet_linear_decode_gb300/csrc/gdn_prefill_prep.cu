@@ -130,16 +130,16 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
     static_assert(kPrepThreads == 256, "one q/k channel's taps per thread");
     tc::cp_async16(sm + kTb + 16 * tid,
                    reinterpret_cast<const float4*>(p.conv_w) + ((tid >> 7) * Hk * kD + kh * kD + (tid & 127)));
-    // v-head h's raw rows and conv taps
-    auto stage_v = [&](int h) {
-        for (int e = tid; e < nrow * 16; e += kPrepThreads) {
+    // v-head h's raw rows and conv taps, by threads idx = 0 .. cnt-1
+    auto stage_v = [&](int h, int idx, int cnt) {
+        for (int e = idx; e < nrow * 16; e += cnt) {
             const int rr = e >> 4, cg = e & 15;
             stage16(sm + kXv + (cg * kXrows + rr) * 16, c0 - 3 + rr, 2 * Hk * kD + h * kD + 8 * cg);
         }
-        if (tid < kD)
-            tc::cp_async16(sm + taps_v_off(G) + 16 * tid, reinterpret_cast<const float4*>(p.conv_w) + (2 * Hk * kD + h * kD + tid));
+        for (int c = idx; c < kD; c += cnt)
+            tc::cp_async16(sm + taps_v_off(G) + 16 * c, reinterpret_cast<const float4*>(p.conv_w) + (2 * Hk * kD + h * kD + c));
     };
-    stage_v(kh);
+    stage_v(kh, tid, kPrepThreads);
 
     // ---- gates of every v-head of the group while the rows land: beta, g, e^g; then
     // warp g scans head g's g in fp64 into Gam, e^Gam and e^{Gam_last - Gam}
@@ -288,7 +288,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
             }
         }
         __syncthreads();
-        if (g + 1 < G) stage_v(h + Hk);   // next v-head's raw rows load behind this head's work
         // decay matrix e^{Gam_t - Gam_r} (r <= t, else 0): one exponential at the right end
         // of the thread's 16 columns, then leftwards e^{Gam_t - Gam_{r-1}} = e^{Gam_t - Gam_r} e^{g_r};
         // e^Gam and e^{Gam_last - Gam_t} -> record
@@ -374,7 +373,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         }
         tc::fence_before_sync();
         __syncthreads();
-        pf::unit_lower_inverse<kPrepThreads>(Af, reinterpret_cast<float*>(sm + kTf), reinterpret_cast<float*>(sm + kDm));
+        // the next v-head's raw rows start loading while the diagonal blocks are solved
+        pf::unit_lower_inverse<kPrepThreads>(Af, reinterpret_cast<float*>(sm + kTf), reinterpret_cast<float*>(sm + kDm),
+                                             [&](int i) {
+                                                 if (g + 1 < G) stage_v(h + Hk, i, kPrepThreads - 64);
+                                             });
         // T diag(beta) and T diag(beta e^Gam): thread -> row tid%64, 16 columns
         {
             const float* Tf = reinterpret_cast<const float*>(sm + kTf);

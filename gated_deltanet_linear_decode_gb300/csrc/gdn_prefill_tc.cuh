@@ -110,10 +110,12 @@ __device__ __forceinline__ void mac16x2x4(const float* a0, const float* a1, cons
 // block, from 16-byte shared-memory loads (no bank conflicts at row strides
 // kTS and 20).  The strictly upper blocks of T are not written (callers treat
 // them as zero).  Hf is fp32 scratch for nine 16 x 16 blocks of row stride 20
-// (11520 bytes).  Ends with a block barrier.
+// (11520 bytes).  While threads 0-63 solve the diagonal blocks, threads
+// 64 .. kThreads-1 run side(i) with i = tid - 64 (work of the caller's that
+// needs no barrier of its own).  Ends with a block barrier.
 constexpr int kTS = 68;
-template <int kThreads>
-__device__ void unit_lower_inverse(const float* Af, float* Tf, float* Hf) {
+template <int kThreads, typename Side>
+__device__ void unit_lower_inverse(const float* Af, float* Tf, float* Hf, Side&& side) {
     static_assert(kThreads == 256, "tilings below assume 256 threads");
     constexpr int kHS = 20;                  // row stride of a scratch block
     const int tid = threadIdx.x;
@@ -136,6 +138,8 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* Hf) {
             for (int t = r + 1; t < 16; ++t) x[t] = fmaf(-a[t][r], x[r], x[t]);
 #pragma unroll
         for (int t = 0; t < 16; ++t) Tf[(o + t) * kTS + o + c] = x[t];
+    } else {
+        side(tid - 64);
     }
     __syncthreads();
     // scratch blocks: Ahat (1,0) (2,0) (2,1) (3,0) (3,1) (3,2) at 0..5; Q20, Q31, Q30 / R30 at 6..8
