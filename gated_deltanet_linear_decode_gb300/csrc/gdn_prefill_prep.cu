@@ -7,12 +7,13 @@
 // One CTA of 8 warps per (chunk, q/k head kh).  While the chunk's raw rows and
 // conv taps land it computes the gates of every v-head h with h mod H_k = kh
 // (tiled heads): beta, g, Gam (fp64 scan), e^Gam, e^{Gam_last-Gam}.  It computes
-// q_hat and k_hat of the chunk once and the raw products [Q; K] K^T once on the
+// q_hat and k_hat of the chunk once -- and from them, while they are in
+// registers, Q' = diag(e^Gam) Q and K' = diag(e^{Gam_last-Gam}) K of every one
+// of those v-heads -> records -- and the raw products [Q; K] K^T once on the
 // tensor cores, then for each of those v-heads:
 //   decay matrix e^{Gam_t-Gam_r};
 //   P = decay (.) Q K^T (r <= t) -> record, A = beta decay (.) K K^T (r < t);
 //   T = (I + A)^{-1} on the CUDA cores (fp32);
-//   Q' = diag(e^Gam) Q and K' = diag(e^{Gam_last-Gam}) K -> record;
 //   U^T = V^T (T diag beta)^T, W^T = K^T (T diag(beta e^Gam))^T on the tensor
 //   cores (fp16 hi/lo split, three MMAs per product) -> record.
 // The records (layouts in gdn_prefill_tc.cuh) feed the state pass.
@@ -229,9 +230,26 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
                 for (int i = 0; i < 8; ++i) val[hf][gq][i] *= inv;
                 uint4 vh, vl;
                 tc::split8(val[hf][gq], vh, vl);
-                const uint32_t so = tc::cl_off(64 * sec + t, 8 * ((4 * warp + gq) & 15), 128);
+                const int ch = 8 * ((4 * warp + gq) & 15);
+                const uint32_t so = tc::cl_off(64 * sec + t, ch, 128);
                 *reinterpret_cast<uint4*>(sm + kQKs + so) = vh;
                 *reinterpret_cast<uint4*>(sm + kQKs + 32768 + so) = vl;
+                // Q' = diag(e^Gam) Q and K' = diag(e^{Gam_last - Gam}) K of every v-head of the
+                // group -> fp16 hi/lo records (the gates are known by now)
+                const uint32_t go = tc::cl_off(t, ch, 64);
+#pragma unroll 1
+                for (int g = 0; g < G; ++g) {
+                    const float e = gate(g, sec == 0 ? kEgam : kElast)[t];
+                    float sv[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) sv[i] = e * val[hf][gq][i];
+                    uint4 oh, ol;
+                    tc::split8(sv, oh, ol);
+                    uint8_t* dst = p.ws_v + (static_cast<size_t>(gc) * Hv + kh + g * Hk) * pf::kVRec +
+                                   (sec == 0 ? pf::kRecQhi : pf::kRecKhi);
+                    *reinterpret_cast<uint4*>(dst + go) = oh;
+                    *reinterpret_cast<uint4*>(dst + 16384 + go) = ol;
+                }
             }
         }
     }
@@ -304,35 +322,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
             if (tid < kChunk) {
                 reinterpret_cast<float*>(vrec + pf::kRecEgam)[tid] = egam_s[tid];
                 reinterpret_cast<float*>(vrec + pf::kRecElast)[tid] = elast_s[tid];
-            }
-        }
-        // Q' = diag(e^Gam) Q and K' = diag(e^{Gam_last - Gam}) K from the hi/lo operands -> fp16
-        // hi/lo records (thread: token tid%64, 32 indices, of Q then of K)
-#pragma unroll 1
-        for (int qk = 0; qk < 2; ++qk) {
-            const int tt = tid & 63;
-            const float e = qk == 0 ? egam_s[tt] : elast_s[tt];
-            uint8_t* dst = vrec + (qk == 0 ? pf::kRecQhi : pf::kRecKhi);
-#pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8) {
-                const int i0 = 32 * (tid >> 6) + 8 * g8;
-                const uint32_t so = tc::cl_off(64 * qk + tt, i0, 128);
-                const uint4 qh = *reinterpret_cast<const uint4*>(sm + kQKs + so);
-                const uint4 ql = *reinterpret_cast<const uint4*>(sm + kQKs + 32768 + so);
-                const uint32_t hw[4] = {qh.x, qh.y, qh.z, qh.w}, lw[4] = {ql.x, ql.y, ql.z, ql.w};
-                float qv[8];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 h2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[k]));
-                    const float2 l2 = __half22float2(*reinterpret_cast<const __half2*>(&lw[k]));
-                    qv[2 * k] = fmaf(e, h2.x, e * l2.x);
-                    qv[2 * k + 1] = fmaf(e, h2.y, e * l2.y);
-                }
-                uint4 oh, ol;
-                tc::split8(qv, oh, ol);
-                const uint32_t go = tc::cl_off(tt, i0, 64);
-                *reinterpret_cast<uint4*>(dst + go) = oh;
-                *reinterpret_cast<uint4*>(dst + 16384 + go) = ol;
             }
         }
         __syncthreads();
