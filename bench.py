@@ -230,7 +230,10 @@ class Workload:
         g, i = self.gdn, self.p_in
         g.gdn_prefill_chunked(self.p_dims, self.p_w, self.cu_h, self.cu_d, i["x"], i["z"], i["a_raw"], i["b_raw"],
                               self.p_conv, self.p_S, self.p_out, zero_init=True, workspace=self.p_ws)
-        return 2
+        # chunk table + (preparation + state pass) per segment + conv-state update; the library cuts
+        # n chunks into two segments from n = 64 on
+        n = int(((self.cu_h[1:] - self.cu_h[:-1] + 63) // 64).sum())
+        return 2 + 2 * (2 if n >= 64 else 1)
 
     def decode(self):
         g, i = self.gdn, self.d_in

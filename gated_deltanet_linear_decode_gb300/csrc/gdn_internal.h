@@ -75,6 +75,7 @@ struct PrefillParams {
     void* workspace;
     // tensor-core prefill: chunk table and records inside the workspace
     int n_chunks;            // total chunks over all sequences
+    int chunk_lo, chunk_hi;  // global chunk range of this launch of the two kernels
     int* chunk_base;         // device [n_seq+1]
     uint8_t* ws_v;           // v-head records, [n_chunks][Hv]
 };

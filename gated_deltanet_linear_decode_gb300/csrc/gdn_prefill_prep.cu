@@ -57,7 +57,7 @@ constexpr int kWaitLimit = 1 << 22;
 __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t sm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int gc = blockIdx.x, kh = blockIdx.y;
+    const int gc = p.chunk_lo + static_cast<int>(blockIdx.x), kh = blockIdx.y;
     const int Hk = p.Hk, Hv = p.Hv, C = p.C;
 
     // sequence of this chunk: the last s with chunk_base[s] <= gc (a non-empty one)
@@ -487,12 +487,12 @@ cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_chunk_prep(const PrefillParams& p, cudaStream_t stream) {
-    if (p.n_chunks == 0) return cudaSuccess;
+    if (p.chunk_hi <= p.chunk_lo) return cudaSuccess;
     const uint32_t smem = prep_smem(p.Hv / p.Hk);
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    chunk_prep_kernel<<<dim3(static_cast<unsigned>(p.n_chunks), static_cast<unsigned>(p.Hk)), kPrepThreads, smem,
+    chunk_prep_kernel<<<dim3(static_cast<unsigned>(p.chunk_hi - p.chunk_lo), static_cast<unsigned>(p.Hk)), kPrepThreads, smem,
                         stream>>>(p);
     return cudaGetLastError();
 }

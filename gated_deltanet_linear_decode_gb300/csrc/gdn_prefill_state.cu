@@ -72,9 +72,22 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
     extern __shared__ __align__(1024) uint8_t sm[];
     const int s = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = p.cu_seqlens[s], L = p.cu_seqlens[s + 1] - t0;
-    const int cbase = p.chunk_base[s], nch = p.chunk_base[s + 1] - cbase;
     const int Hv = p.Hv, HvD = Hv * kD;
+    // this launch's chunks of sequence s: [cb, ce) of its own; the state comes in and goes out
+    // through S (a launch that starts the sequence takes zeros instead under zero_init)
+    const int cbase_s = p.chunk_base[s], nch_s = p.chunk_base[s + 1] - cbase_s;
+    const int cb = max(0, p.chunk_lo - cbase_s), ce = min(nch_s, p.chunk_hi - cbase_s);
+    float* Sg = p.S + (static_cast<size_t>(s) * Hv + h) * kD * kD;
+    if (cb >= ce) {
+        // an empty sequence ends with its initial state: zeros under zero_init (written by the first launch)
+        if (nch_s == 0 && p.zero_init && p.chunk_lo == 0)
+            for (int e = tid; e < kD * kD / 4; e += blockDim.x) reinterpret_cast<float4*>(Sg)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    const bool zero_init = p.zero_init && cb == 0;
+    const int cbase = cbase_s + cb, nch = ce - cb;
+    const int t0 = p.cu_seqlens[s] + kChunk * cb;
+    const int L = min(p.cu_seqlens[s + 1] - t0, kChunk * nch);
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBar);
     static_assert(8 * kNumBars + 8 <= 176, "mbarrier area");
@@ -118,7 +131,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
         return false;
     };
 
-    float* Sg = p.S + (static_cast<size_t>(s) * Hv + h) * kD * kD;
     const uint8_t* vrec0 = p.ws_v + (static_cast<size_t>(cbase) * Hv + h) * pf::kVRec;
     auto vrec = [&](int c) { return vrec0 + static_cast<size_t>(c) * Hv * pf::kVRec; };
 
@@ -134,7 +146,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
             const int c = 2 * chalf + cc;
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
-                const float4 f = p.zero_init ? make_float4(0.f, 0.f, 0.f, 0.f)
+                const float4 f = zero_init ? make_float4(0.f, 0.f, 0.f, 0.f)
                                              : *reinterpret_cast<const float4*>(Sg + row * kD + 32 * c + i);
                 v[i] = f.x; v[i + 1] = f.y; v[i + 2] = f.z; v[i + 3] = f.w;
             }
