@@ -18,7 +18,9 @@
 //   o_t  = O[:, t] / sqrt(128)  -> gated RMSNorm -> out
 // Warp roles, meeting only at mbarriers:
 //   warps 0-7   convert: S -> fp16 hi/lo (and the decay of S), Dacc -> D hi/lo
-//   warps 8-11  epilogue: O -> o -> gated RMSNorm -> out, up to two chunks behind
+//   warps 8-11  epilogue: O -> shared memory (row j per thread), then token-major:
+//               o -> gated RMSNorm -> out, a thread owning one token and 64 v-rows
+//               (z and out move in 16-byte pieces); up to two chunks behind
 //               (O is double-buffered in tensor memory; z is staged by cp.async)
 //   warp 12     control: one lane issues the MMAs
 //   warp 13     copies: one lane issues the bulk copies of the records, each as
@@ -42,9 +44,11 @@ constexpr uint32_t kQs = 0;           // Q' hi +0, lo +16384       (64 t x 128 i
 constexpr uint32_t kKs = 32768;       // K' hi +0, lo +16384       (64 t x 128 i, canonical 64 rows)
 constexpr uint32_t kWs = 65536;       // W^T hi                   (128 i x 64 t, canonical 128 rows)
 constexpr uint32_t kPs = 81920;       // P hi +0, lo +8192         (64 t x 64 r, canonical 64 rows)
-constexpr uint32_t kZs = 98304;       // z of even / odd chunks, bf16 [2][64 t][128 j]
-constexpr uint32_t kRs = 131072;      // RMS partial sums [2][4][64] fp32
-constexpr uint32_t kBar = 133120;     // mbarriers, then the TMEM base and the error flag
+constexpr int kOStride = 68;          // floats per v-row of the staged O (64 tokens + 4: no bank conflicts)
+constexpr uint32_t kOst = 98304;      // the chunk's O, fp32 [128 j][kOStride], for the token-major epilogue
+constexpr uint32_t kRs = kOst + 128 * kOStride * 4;   // per-token partial sums of O^2 [2][64] fp32
+constexpr uint32_t kNw = kRs + 512;   // norm_w [128] fp32
+constexpr uint32_t kBar = kNw + 512;  // mbarriers, then the TMEM base and the error flag
 constexpr uint32_t kStateSmem = kBar + 176;
 static_assert(kStateSmem <= 232448, "shared memory of the state pass exceeds 227 KB");
 
@@ -55,8 +59,7 @@ enum : int {
     kODone0, kODone1,                  // O of even / odd chunks complete
     kSReady, kDReady,                  // converters wrote the S / D operands (256 arrivals)
     kEpi0, kEpi1,                      // epilogue done with the O buffer of even / odd chunks (128 arrivals)
-    kRsReady,                          // epilogue wrote its per-token partial sums (128 arrivals)
-    kZReady,                           // the epilogue's copies of a chunk's z landed (128 arrivals)
+    kESync,                            // the epilogue warps' own barrier (128 arrivals, once per use)
     kDrain,                            // error path: every MMA issued so far retired
     kNumBars
 };
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t cnt = 1;
             if (i == kSReady || i == kDReady) cnt = kConvThreads;
-            if (i == kEpi0 || i == kEpi1 || i == kRsReady || i == kZReady) cnt = kEpiThreads;
+            if (i == kEpi0 || i == kEpi1 || i == kESync) cnt = kEpiThreads;
             tc::mbar_init(bars + i, cnt);
         }
         *err_s = 0;
@@ -326,96 +329,84 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
             }
         }
     } else {   // warps kConvWarps .. kConvWarps + kEpiWarps - 1
-        // ================= epilogue: thread = v-row j, the 64 tokens of a chunk in blocks of 16
+        // ================= epilogue
         const int eq = warp - kConvWarps;   // lane quarter
         const int j = eq * 32 + lane, e = tid - kConvThreads;
+        const int tt = e & 63, jh = e >> 6;   // token-major part: token tt, v-rows 64 jh ..
         const uint32_t te = tmem + (static_cast<uint32_t>(eq * 32) << 16);
+        float* Ost = reinterpret_cast<float*>(sm + kOst);
         float* Rs = reinterpret_cast<float*>(sm + kRs);
-        const unsigned short* zs0 = reinterpret_cast<const unsigned short*>(sm + kZs) + j;
-        const float wj = p.norm_w[j];
-        const __nv_bfloat16* zh = static_cast<const __nv_bfloat16*>(p.z) + h * kD;
-        Tout* __restrict__ outj = static_cast<Tout*>(p.out) + h * kD + j;
-        float* __restrict__ prej = p.prenorm ? p.prenorm + h * kD + j : nullptr;
+        float* nw = reinterpret_cast<float*>(sm + kNw);
+        nw[e] = p.norm_w[e];
+        const __nv_bfloat16* zh = static_cast<const __nv_bfloat16*>(p.z) + h * kD + 64 * jh;
         const bool check = (p.flags & kFlagCheckFinite) != 0;
-        // chunk c's z rows (256 bytes of head h each) into z buffer c % 2 by 16-byte
-        // asynchronous copies, zero past the sequence; they arrive on kZReady
-        auto stage_z = [&](int c) {
-            const int n = min(kChunk, L - c * kChunk);
-            const __nv_bfloat16* src = zh + static_cast<size_t>(t0 + c * kChunk) * HvD;
-            uint8_t* dst = sm + kZs + 16384 * (c & 1);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int piece = e + kEpiThreads * k, rr = piece >> 4, c16 = piece & 15;
-                const bool valid = rr < n;
-                tc::cp_async16_zfill(dst + rr * 256 + c16 * 16, src + static_cast<size_t>(valid ? rr : 0) * HvD + c16 * 8,
-                                     valid ? 16u : 0u);
-            }
-            tc::cp_async_mbar_arrive(bars + kZReady);
+        uint32_t es_phase = 0;
+        auto epi_sync = [&]() -> bool {   // bounded barrier of the 128 epilogue threads
+            tc::mbar_arrive(bars + kESync);
+            const bool r = wait(kESync, es_phase);
+            es_phase ^= 1u;
+            return r;
         };
-        if (nch > 0) stage_z(0);
-        bool ok = true;
+        bool ok = epi_sync();   // norm_w staged
         for (int c = 0; c < nch && ok; ++c) {
-            const uint32_t b = c & 1;   // O, partial-sum and z buffer
-            const unsigned short* zs = zs0 + 8192 * b;
+            const uint32_t b = c & 1;   // O buffer
             const int c0 = c * kChunk, n = min(kChunk, L - c0);
-            const size_t row0 = static_cast<size_t>(t0 + c0);
-            if (c + 1 < nch && e < 2 * min(kChunk, L - c0 - kChunk))   // next chunk's z toward L2: a half row per thread
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(zh + (row0 + kChunk + (e >> 1)) * HvD + 64 * (e & 1)));
-            if (!(ok = wait(kODone0 + b, (c >> 1) & 1) && wait(kZReady, c & 1))) break;
+            const bool valid = tt < n;
+            const size_t rowt = static_cast<size_t>(t0 + c0 + tt);
+            // this thread's z (token tt, v-rows 64 jh ..): 128 bytes, loaded ahead of the wait
+            uint4 zq[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                zq[k] = valid ? __ldg(reinterpret_cast<const uint4*>(zh + rowt * HvD) + k) : make_uint4(0, 0, 0, 0);
+            if (!(ok = wait(kODone0 + b, (c >> 1) & 1))) break;
             tc::fence_after_sync();
-            // pass 1: per-token partial sums of o^2 over this warp's 32 rows (o = O / sqrt(128))
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                float v1[16];
-                tc::tmem_ld16(te + kColO + 64 * b + 16 * q, v1);
+            {   // O row j (64 tokens) -> registers -> shared memory; the O buffer is then free
+                float v[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v1[i] *= v1[i] * (kInvSqrtD * kInvSqrtD);
-                const float ssum = reduce16_transposed(v1);
-                if (lane < 16) Rs[(b * 4 + eq) * 64 + 16 * q + lane] = ssum;
-            }
-            tc::mbar_arrive(bars + kRsReady);
-            if (!(ok = wait(kRsReady, c & 1))) break;
-            // every epilogue thread is past pass 2 of chunk c - 1, so z buffer (c + 1) % 2 is free
-            if (c + 1 < nch) stage_z(c + 1);
-            // 1/sqrt(mean o^2 + eps) of tokens lane and 32 + lane
-            const float* rb = Rs + b * 256;
-            const float rs_a = rsqrtf(((rb[lane] + rb[64 + lane]) + (rb[128 + lane] + rb[192 + lane])) * (1.0f / kD) + p.eps);
-            const float rs_b = rsqrtf(((rb[32 + lane] + rb[96 + lane]) + (rb[160 + lane] + rb[224 + lane])) * (1.0f / kD) + p.eps);
-            // pass 2: y = o * rs * norm_w silu(z); all 16 values first, then the stores
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                float v1[16], v2[16];
-                tc::tmem_ld16(te + kColO + 64 * b + 16 * q, v1);
-                const float rsq = q < 2 ? rs_a : rs_b;
+                for (int hf = 0; hf < 2; ++hf) {
+                    tc::tmem_ld32(te + kColO + 64 * b + 32 * hf, v);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    v1[i] *= kInvSqrtD;
-                    const float g = wj * pf::silu_fast(__uint_as_float(static_cast<uint32_t>(zs[(16 * q + i) * kD]) << 16));
-                    v2[i] = v1[i] * __shfl_sync(0xffffffffu, rsq, (16 * q + i) & 31) * g;
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<float4*>(Ost + j * kOStride + 32 * hf + 4 * q) =
+                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
-                Tout* oq = outj + (row0 + 16 * q) * HvD;
-                float* pq = prej ? prej + (row0 + 16 * q) * HvD : nullptr;
-                const int nq = n - 16 * q;
-                if (nq >= 16) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) st_out(oq + static_cast<size_t>(i) * HvD, v2[i]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (i < nq) st_out(oq + static_cast<size_t>(i) * HvD, v2[i]);
-                }
-                if (check)
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) bad |= i < nq && nonfinite_bits(v2[i]);
-                if (pq)
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (i < nq) pq[static_cast<size_t>(i) * HvD] = v1[i];
             }
             tc::fence_before_sync();
             tc::mbar_arrive(bars + kEpi0 + b);
+            if (!(ok = epi_sync())) break;   // O staged
+            // token-major: partial sum of O^2 over v-rows 64 jh .. of token tt
+            const float* oc = Ost + 64 * jh * kOStride + tt;
+            float ss = 0.f;
+#pragma unroll 16
+            for (int r = 0; r < 64; ++r) ss = fmaf(oc[r * kOStride], oc[r * kOStride], ss);
+            Rs[jh * 64 + tt] = ss;
+            if (!(ok = epi_sync())) break;   // partial sums written
+            // o = O / sqrt(128); y = o / sqrt(mean(o^2) + eps) * norm_w * silu(z)
+            const float rs =
+                rsqrtf((Rs[tt] + Rs[64 + tt]) * (kInvSqrtD * kInvSqrtD / kD) + p.eps) * kInvSqrtD;
+            if (valid) {
+                Tout* op = static_cast<Tout*>(p.out) + rowt * HvD + h * kD + 64 * jh;
+                float* pp = p.prenorm ? p.prenorm + rowt * HvD + h * kD + 64 * jh : nullptr;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    float zf[8], o[8], y[8];
+                    pf::bf16x8_to_f32(zq[k], zf);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        o[i] = oc[(8 * k + i) * kOStride];
+                        y[i] = o[i] * rs * nw[64 * jh + 8 * k + i] * pf::silu_fast(zf[i]);
+                        if (check) bad |= nonfinite_bits(y[i]);
+                    }
+                    pf::st_out8(op + 8 * k, y);
+                    if (pp)
+#pragma unroll
+                        for (int i = 0; i < 8; i += 4)
+                            *reinterpret_cast<float4*>(pp + 8 * k + i) = make_float4(
+                                o[i] * kInvSqrtD, o[i + 1] * kInvSqrtD, o[i + 2] * kInvSqrtD, o[i + 3] * kInvSqrtD);
+                }
+            }
+            if (!(ok = epi_sync())) break;   // every thread is done with the staged O and the partial sums
         }
-        tc::cp_async_drain();   // no copy of this thread may land after the CTA exits (error path)
     }
 
     tc::fence_before_sync();

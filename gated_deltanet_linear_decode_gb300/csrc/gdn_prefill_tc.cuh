@@ -63,6 +63,19 @@ __device__ __forceinline__ void bf16x4_to_f32(uint2 u, float* f) {
     f[2] = __uint_as_float(u.y << 16); f[3] = __uint_as_float(u.y & 0xffff0000u);
 }
 
+__device__ __forceinline__ void st_out8(float* p, const float* y) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(y[0], y[1], y[2], y[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(y[4], y[5], y[6], y[7]);
+}
+__device__ __forceinline__ void st_out8(__nv_bfloat16* p, const float* y) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(y[2 * i], y[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
 __device__ __forceinline__ void st_out4(float* p, const float (&y)[4]) {
     *reinterpret_cast<float4*>(p) = make_float4(y[0], y[1], y[2], y[3]);
 }
