@@ -219,6 +219,11 @@ class Workload:
         self.v_ckS = torch.empty(B, K, vc.Hv, 128, 128, device=dev)
         self.v_out = torch.empty(B * K, vc.Hv * 128, device=dev, dtype=torch.bfloat16)
         self.acc = vc.accept_len.to(dev)
+        # the same verify + commit on a state ring (R = K + 1 slots, slot 0 live at the start)
+        self.r_S = torch.zeros(B, K + 1, vc.Hv, 128, 128, device=dev)
+        self.r_S[:, 0] = vc.S0.to(dev)
+        self.r_cur = torch.zeros(B, device=dev, dtype=torch.int32)
+        self.r_conv = vc.conv0.to(dev)
         self.h_pout = torch.empty(self.p_out.shape, dtype=torch.bfloat16).pin_memory()
         self.h_dout = torch.empty(self.d_out.shape, dtype=torch.bfloat16).pin_memory()
         self.h_vout = torch.empty(self.v_out.shape, dtype=torch.bfloat16).pin_memory()
@@ -246,6 +251,13 @@ class Workload:
         g.gdn_verify_k(self.d_dims, self.d_w, self.vc.K, i["x"], i["z"], i["a_raw"], i["b_raw"], self.d_conv,
                        self.d_S, self.v_ckc, self.v_ckS, self.v_out)
         g.gdn_commit(self.d_dims, self.vc.K, self.acc, self.v_ckc, self.v_ckS, self.d_conv, self.d_S)
+        return 2
+
+    def verify_ring(self):
+        g, i = self.gdn, self.v_in
+        g.gdn_verify_k_ring(self.d_dims, self.d_w, self.vc.K, i["x"], i["z"], i["a_raw"], i["b_raw"], self.r_conv,
+                            self.r_S, self.r_cur, self.v_ckc, self.v_out)
+        g.gdn_commit_ring(self.d_dims, self.vc.K, self.vc.K + 1, self.acc, self.v_ckc, self.r_conv, self.r_cur)
         return 2
 
     def h2d(self):
@@ -321,6 +333,18 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
 
+    # outside the step: the verify + commit pair on a state ring, where the commit moves no state
+    ring_ms = []
+    for it in range(args.warmup + max(1, args.steps)):
+        wl.flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        wl.verify_ring()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            ring_ms.append(e0.elapsed_time(e1))
+
     tot_ms = sum(step_ms)
     tot_ms = _max_over_ranks(tot_ms, world)
     e2e_tot = _max_over_ranks(sum(e2e_ms), world)
@@ -345,6 +369,10 @@ def run_gpu(args, rank, world):
     v_roof = {"bound": "hbm", "achieved": vb / (vm / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
               "frac": vb / (vm / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes_verify_only": vb,
               "note": "time includes the commit copy"}
+    rm = statistics.mean(ring_ms)
+    r_roof = {"bound": "hbm", "achieved": vb / (rm / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+              "frac": vb / (rm / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes": vb,
+              "note": "ring commit: conv rows and slot index only; timed outside the step"}
     dominant = max((pm, "prefill", p_roof), (dm, "decode", d_roof), (vm, "verify", v_roof))[1:]
     h2d, d2h = wl.io_bytes()
     line = {
@@ -359,6 +387,7 @@ def run_gpu(args, rank, world):
             "prefill_T8192": {"tokens_per_s": pc.T / (pm / 1e3), "ms": pm, "roofline": p_roof},
             "decode_B64": {"tokens_per_s": dc.N / (dm / 1e3), "ms": dm, "roofline": d_roof},
             "verify_B64_K3_commit": {"tokens_per_s": vc.N * vc.K / (vm / 1e3), "ms": vm, "roofline": v_roof},
+            "verify_B64_K3_commit_ring": {"tokens_per_s": vc.N * vc.K / (rm / 1e3), "ms": rm, "roofline": r_roof},
         },
         "e2e": {"value": world * tok_step * len(e2e_ms) / (e2e_tot / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

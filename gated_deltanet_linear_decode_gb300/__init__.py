@@ -24,7 +24,8 @@ __all__ = [
     "GdnError", "GdnDims", "GdnWeights", "make_dims", "make_weights", "library",
     "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step",
     "gdn_verify_k", "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked",
-    "gdn_prefill_chunked_static", "PREFILL_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "HEAD_DIM",
+    "gdn_prefill_chunked_static", "gdn_verify_k_ring", "gdn_commit_ring", "gdn_decode_step_ring",
+    "PREFILL_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "HEAD_DIM",
 ]
 
 HEAD_DIM = 128
@@ -36,7 +37,7 @@ PREFILL_STATIC_SCRATCH_BYTES = 128 * 1024 * 1024   # GDN_PREFILL_STATIC_SCRATCH_
 EXPORTED_SYMBOLS = (
     "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step",
     "gdn_verify_k", "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked",
-    "gdn_prefill_chunked_static",
+    "gdn_prefill_chunked_static", "gdn_verify_k_ring", "gdn_commit_ring", "gdn_decode_step_ring",
 )
 
 
@@ -82,6 +83,9 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         "gdn_prefill_workspace_bytes": (SZ, [D, I32, ctypes.c_int64]),
         "gdn_prefill_chunked": (ctypes.c_int, [D, W, I32, P, P, P, P, P, P, P, P, I32, P, P, P, SZ, P, P]),
         "gdn_prefill_chunked_static": (ctypes.c_int, [D, W, I32, P, P, P, P, P, P, P, P, I32, P, P, P, P]),
+        "gdn_verify_k_ring": (ctypes.c_int, [D, W, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P]),
+        "gdn_commit_ring": (ctypes.c_int, [D, I32, I32, I32, P, P, P, P, P]),
+        "gdn_decode_step_ring": (ctypes.c_int, [D, W, I32, I32, P, P, P, P, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -224,6 +228,54 @@ def gdn_commit(dims: GdnDims, K: int, accept_len, conv_ckpt, S_ckpt, conv_state,
     _need(S, torch.float32, (B, dims.H_v, HEAD_DIM, HEAD_DIM))
     _check("gdn_commit", library().gdn_commit(
         ctypes.byref(dims), B, K, _ptr(accept_len), _ptr(conv_ckpt), _ptr(S_ckpt), _ptr(conv_state), _ptr(S),
+        _stream(stream)))
+
+
+def gdn_verify_k_ring(dims: GdnDims, w: Weights, K: int, x, z, a_raw, b_raw, conv_state, S_ring, ring_cur,
+                      conv_ckpt, out, prenorm_out=None, dev_status=None, stream=None) -> None:
+    """Verify walk on the live slots of a state ring S_ring [B][R][H_v][128][128]; checkpoint p goes to
+    slot (ring_cur[b] + 1 + p) % R."""
+    B, R = S_ring.shape[0], S_ring.shape[1]
+    C, HvD = HEAD_DIM * (2 * dims.H_k + dims.H_v), dims.H_v * HEAD_DIM
+    a = _act(dims)
+    _need(x, a, (B * K, C)); _need(z, a, (B * K, HvD)); _need(a_raw, a, (B * K, dims.H_v))
+    _need(b_raw, a, (B * K, dims.H_v)); _need(conv_state, a, (B, 3, C))
+    _need(S_ring, torch.float32, (B, R, dims.H_v, HEAD_DIM, HEAD_DIM)); _need(ring_cur, torch.int32, (B,))
+    _need(conv_ckpt, a, (B, K, 3, C)); _need(out, _out(dims), (B * K, HvD))
+    _need(prenorm_out, torch.float32, (B * K, HvD), optional=True)
+    _need(dev_status, torch.int32, (B * dims.H_v,), optional=True)
+    _check("gdn_verify_k_ring", library().gdn_verify_k_ring(
+        ctypes.byref(dims), ctypes.byref(w.struct()), B, K, R, _ptr(x), _ptr(z), _ptr(a_raw), _ptr(b_raw),
+        _ptr(conv_state), _ptr(S_ring), _ptr(ring_cur), _ptr(conv_ckpt), _ptr(out), _ptr(prenorm_out),
+        _ptr(dev_status), _stream(stream)))
+
+
+def gdn_commit_ring(dims: GdnDims, K: int, R: int, accept_len, conv_ckpt, conv_state, ring_cur, stream=None) -> None:
+    """Make checkpoint accept_len[b]-1 of a ring verify the live state (slot index and conv rows only)."""
+    B = conv_state.shape[0]
+    C = HEAD_DIM * (2 * dims.H_k + dims.H_v)
+    a = _act(dims)
+    _need(accept_len, torch.int32, (B,)); _need(conv_ckpt, a, (B, K, 3, C)); _need(conv_state, a, (B, 3, C))
+    _need(ring_cur, torch.int32, (B,))
+    _check("gdn_commit_ring", library().gdn_commit_ring(
+        ctypes.byref(dims), B, K, R, _ptr(accept_len), _ptr(conv_ckpt), _ptr(conv_state), _ptr(ring_cur),
+        _stream(stream)))
+
+
+def gdn_decode_step_ring(dims: GdnDims, w: Weights, x, z, a_raw, b_raw, conv_state, S_ring, ring_cur, out,
+                         prenorm_out=None, dev_status=None, stream=None) -> None:
+    """One recurrent step on the live slot of each sequence of a state ring, in place."""
+    B, R = S_ring.shape[0], S_ring.shape[1]
+    C, HvD = HEAD_DIM * (2 * dims.H_k + dims.H_v), dims.H_v * HEAD_DIM
+    a = _act(dims)
+    _need(x, a, (B, C)); _need(z, a, (B, HvD)); _need(a_raw, a, (B, dims.H_v)); _need(b_raw, a, (B, dims.H_v))
+    _need(conv_state, a, (B, 3, C)); _need(S_ring, torch.float32, (B, R, dims.H_v, HEAD_DIM, HEAD_DIM))
+    _need(ring_cur, torch.int32, (B,)); _need(out, _out(dims), (B, HvD))
+    _need(prenorm_out, torch.float32, (B, HvD), optional=True)
+    _need(dev_status, torch.int32, (B * dims.H_v,), optional=True)
+    _check("gdn_decode_step_ring", library().gdn_decode_step_ring(
+        ctypes.byref(dims), ctypes.byref(w.struct()), B, R, _ptr(x), _ptr(z), _ptr(a_raw), _ptr(b_raw),
+        _ptr(conv_state), _ptr(S_ring), _ptr(ring_cur), _ptr(out), _ptr(prenorm_out), _ptr(dev_status),
         _stream(stream)))
 
 

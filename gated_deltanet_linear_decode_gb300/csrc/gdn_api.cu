@@ -133,18 +133,21 @@ gdn_status gdn_conv_state_init(const gdn_dims* dims, int32_t n_seq, void* conv_s
     return cuda_status(gdn::launch_conv_init(conv_state, prefix, bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// ring_cur != nullptr: S_in == S_out is a state ring [B][R][H_v][128][128] (see gdn_verify_k_ring).
 static gdn_status recurrent_common(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t K,
                                    const void* x, const void* z, const void* a_raw, const void* b_raw,
                                    const void* conv_in, const float* S_in, void* conv_out, float* S_out,
                                    bool verify, void* out, float* prenorm_out, int32_t* dev_status,
-                                   gdn_stream_t stream) {
+                                   gdn_stream_t stream, const int32_t* ring_cur = nullptr, int32_t R = 0) {
     gdn_status s = check_dims(dims);
     if (s != GDN_OK) return s;
     if (B < 0 || K < 1 || K > GDN_MAX_VERIFY_K) return GDN_E_INVALID_ARG;
+    if (ring_cur && (R < (verify ? K + 1 : 1) || R > GDN_MAX_VERIFY_K + 1)) return GDN_E_INVALID_ARG;
     if (B == 0) return GDN_OK;
     if ((s = check_weights(w)) != GDN_OK) return s;
     if ((s = check_ptrs({x, z, a_raw, b_raw, conv_in, S_in, conv_out, S_out, out}, {prenorm_out, dev_status})) != GDN_OK)
         return s;
+    if (ring_cur && (s = check_ptrs({ring_cur}, {})) != GDN_OK) return s;
     const int Hk = dims->H_k, Hv = dims->H_v;
     const size_t C = static_cast<size_t>(kD) * (2 * Hk + Hv);
     const size_t ea = act_size(dims->act_dtype), eo = act_size(dims->out_dtype);
@@ -152,12 +155,15 @@ static gdn_status recurrent_common(const gdn_dims* dims, const gdn_weights* w, i
     const size_t HvD = static_cast<size_t>(Hv) * kD;
     const size_t S_bytes = static_cast<size_t>(B) * Hv * kD * kD * 4;
     const size_t cv_bytes = static_cast<size_t>(B) * 3 * C * ea;
+    // a ring is read and written in one buffer (like the in-place decode state)
+    const size_t S_out_bytes = ring_cur ? S_bytes * R : (verify ? S_bytes * K : S_bytes);
     const Range ins[] = {{x, T * C * ea}, {z, T * HvD * ea}, {a_raw, T * Hv * ea}, {b_raw, T * Hv * ea},
                          {w->conv_w, C * 16}, {w->dt_bias, Hv * 4u}, {w->ssm_a, Hv * 4u}, {w->norm_w, kD * 4u},
-                         {verify ? conv_in : nullptr, cv_bytes}, {verify ? S_in : nullptr, S_bytes}};
+                         {verify ? conv_in : nullptr, cv_bytes}, {verify && !ring_cur ? S_in : nullptr, S_bytes},
+                         {ring_cur, B * 4u}};
     const Range outs[] = {{out, T * HvD * eo}, {prenorm_out, T * HvD * 4}, {dev_status, B * Hv * 4u},
-                          {conv_out, verify ? cv_bytes * K : cv_bytes}, {S_out, verify ? S_bytes * K : S_bytes}};
-    if (any_overlap(outs, 5, ins, 10)) return GDN_E_INVALID_ARG;
+                          {conv_out, verify ? cv_bytes * K : cv_bytes}, {S_out, S_out_bytes}};
+    if (any_overlap(outs, 5, ins, 11)) return GDN_E_INVALID_ARG;
 
     gdn::RecParams p{};
     const int r = Hv / Hk;
@@ -178,6 +184,7 @@ static gdn_status recurrent_common(const gdn_dims* dims, const gdn_weights* w, i
         p.S_out_b = static_cast<long long>(Hv) * kD * kD; p.S_out_p = 0;
     }
     p.out = out; p.prenorm = prenorm_out; p.dev_status = dev_status;
+    p.ring_cur = ring_cur; p.ring_R = R; p.ring_shift = verify ? 1 : 0;
     int grid = 0;
     if (use_stream_kernel(B, Hk, K, dims->act_dtype, &grid))
         return cuda_status(gdn::launch_recurrent_stream(p, dims->act_dtype, dims->out_dtype, grid,
@@ -217,6 +224,43 @@ gdn_status gdn_commit(const gdn_dims* dims, int32_t B, int32_t K, const int32_t*
     const Range ins[] = {{accept_len, B * 4u}, {conv_ckpt, p.conv_bytes * B * K}, {S_ckpt, p.S_elems * 4 * B * K}};
     const Range outs[] = {{conv_state, p.conv_bytes * B}, {S, p.S_elems * 4 * B}};
     if (any_overlap(outs, 2, ins, 3)) return GDN_E_INVALID_ARG;
+    return cuda_status(gdn::launch_commit(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_decode_step_ring(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t R, const void* x,
+                                const void* z, const void* a_raw, const void* b_raw, void* conv_state, float* S_ring,
+                                const int32_t* ring_cur, void* out, float* prenorm_out, int32_t* dev_status,
+                                gdn_stream_t stream) {
+    if (!ring_cur) return GDN_E_INVALID_ARG;
+    return recurrent_common(dims, w, B, 1, x, z, a_raw, b_raw, conv_state, S_ring, conv_state, S_ring, false, out,
+                            prenorm_out, dev_status, stream, ring_cur, R);
+}
+
+gdn_status gdn_verify_k_ring(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t K, int32_t R,
+                             const void* x, const void* z, const void* a_raw, const void* b_raw,
+                             const void* conv_state, float* S_ring, const int32_t* ring_cur, void* conv_ckpt,
+                             void* out, float* prenorm_out, int32_t* dev_status, gdn_stream_t stream) {
+    if (!ring_cur) return GDN_E_INVALID_ARG;
+    return recurrent_common(dims, w, B, K, x, z, a_raw, b_raw, conv_state, S_ring, conv_ckpt, S_ring, true, out,
+                            prenorm_out, dev_status, stream, ring_cur, R);
+}
+
+gdn_status gdn_commit_ring(const gdn_dims* dims, int32_t B, int32_t K, int32_t R, const int32_t* accept_len,
+                           const void* conv_ckpt, void* conv_state, int32_t* ring_cur, gdn_stream_t stream) {
+    gdn_status s = check_dims(dims);
+    if (s != GDN_OK) return s;
+    if (B < 0 || K < 1 || K > GDN_MAX_VERIFY_K || R < K + 1 || R > GDN_MAX_VERIFY_K + 1) return GDN_E_INVALID_ARG;
+    if (B == 0) return GDN_OK;
+    if ((s = check_ptrs({accept_len, conv_ckpt, conv_state, ring_cur}, {})) != GDN_OK) return s;
+    const size_t C = static_cast<size_t>(kD) * (2 * dims->H_k + dims->H_v);
+    gdn::CommitParams p{};
+    p.B = B; p.K = K; p.accept_len = accept_len; p.conv_ckpt = conv_ckpt; p.conv_state = conv_state;
+    p.ring_cur = ring_cur; p.ring_R = R;
+    p.S_elems = static_cast<size_t>(dims->H_v) * kD * kD;
+    p.conv_bytes = 3 * C * act_size(dims->act_dtype);
+    const Range ins[] = {{accept_len, B * 4u}, {conv_ckpt, p.conv_bytes * B * K}};
+    const Range outs[] = {{conv_state, p.conv_bytes * B}, {ring_cur, B * 4u}};
+    if (any_overlap(outs, 2, ins, 2)) return GDN_E_INVALID_ARG;
     return cuda_status(gdn::launch_commit(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -36,10 +36,31 @@ struct RecParams {
     void* out;              // [B*K][Hv*128]
     float* prenorm;         // optional, [B*K][Hv*128]
     int* dev_status;        // optional, [B*Hv]
+    // state ring (ring_cur != nullptr): S_in == S_out is [B][ring_R][Hv][128][128]; sequence b
+    // reads slot ring_cur[b] and writes position t to slot (ring_cur[b] + ring_shift + t) % ring_R
+    const int* ring_cur;
+    int ring_R, ring_shift;
 };
+
+#ifdef __CUDACC__
+// The state a sequence starts from, and where the state after its position t goes.
+__device__ __forceinline__ const float* rec_state_in(const RecParams& p, int b) {
+    const size_t plane = static_cast<size_t>(p.Hv) * 128 * 128;
+    return p.ring_cur ? p.S_in + (static_cast<size_t>(b) * p.ring_R + p.ring_cur[b]) * plane
+                      : p.S_in + static_cast<size_t>(b) * plane;
+}
+__device__ __forceinline__ float* rec_state_out(const RecParams& p, int b, int t) {
+    const size_t plane = static_cast<size_t>(p.Hv) * 128 * 128;
+    if (p.ring_cur)
+        return p.S_out + (static_cast<size_t>(b) * p.ring_R + (p.ring_cur[b] + p.ring_shift + t) % p.ring_R) * plane;
+    return p.S_out + static_cast<size_t>(b) * p.S_out_b + static_cast<size_t>(t) * p.S_out_p;
+}
+#endif
 
 struct CommitParams {
     int B, K;
+    int* ring_cur;          // ring commit: advance slot indices [B] (S, S_ckpt unused)
+    int ring_R;
     const int* accept_len;  // [B]
     const void* conv_ckpt;  // [B][K][3][C]
     const float* S_ckpt;    // [B][K][Hv][128][128]

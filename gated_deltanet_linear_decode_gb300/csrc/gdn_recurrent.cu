@@ -69,8 +69,7 @@ recurrent_kernel(const RecParams p) {
     __shared__ float rms_part[kMaxK];
 
     // ---- state rows: issue the 128-bit loads before anything else
-    const size_t head_off = (static_cast<size_t>(b) * p.Hv + h) * kD * kD;
-    const float* Sin = p.S_in + head_off + static_cast<size_t>(j0) * kD;
+    const float* Sin = rec_state_in(p, b) + static_cast<size_t>(h) * kD * kD + static_cast<size_t>(j0) * kD;
     float4 s[8];
 #pragma unroll
     for (int rr = 0; rr < 8; ++rr)
@@ -164,8 +163,7 @@ recurrent_kernel(const RecParams p) {
         }
         // state out: in place for a decode step, checkpoint t for a verify walk
         {
-            float* Sout = p.S_out + static_cast<size_t>(b) * p.S_out_b + static_cast<size_t>(t) * p.S_out_p +
-                          static_cast<size_t>(h) * kD * kD + static_cast<size_t>(j0) * kD;
+            float* Sout = rec_state_out(p, b, t) + static_cast<size_t>(h) * kD * kD + static_cast<size_t>(j0) * kD;
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr) {
                 st_f4(Sout + static_cast<size_t>(warp * 8 + rr) * kD + 4 * lane, s[rr]);
@@ -226,6 +224,16 @@ __global__ void commit_kernel(const CommitParams p) {
     const int b = blockIdx.y;
     const int n = p.accept_len[b];
     if (n < 1 || n > p.K) return;
+    if (p.ring_cur) {   // ring: the accepted checkpoint's slot becomes the live one; only the conv rows move
+        const uint4* csrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.conv_ckpt) +
+                                                           (static_cast<size_t>(b) * p.K + (n - 1)) * p.conv_bytes);
+        uint4* cdst = reinterpret_cast<uint4*>(static_cast<char*>(p.conv_state) + static_cast<size_t>(b) * p.conv_bytes);
+        for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < p.conv_bytes / 16;
+             i += static_cast<size_t>(gridDim.x) * blockDim.x)
+            cdst[i] = csrc[i];
+        if (blockIdx.x == 0 && threadIdx.x == 0) p.ring_cur[b] = (p.ring_cur[b] + n) % p.ring_R;
+        return;
+    }
     const float4* Ssrc = reinterpret_cast<const float4*>(p.S_ckpt + (static_cast<size_t>(b) * p.K + (n - 1)) * p.S_elems);
     float4* Sdst = reinterpret_cast<float4*>(p.S + static_cast<size_t>(b) * p.S_elems);
     const size_t nS = p.S_elems / 4;
@@ -293,7 +301,7 @@ cudaError_t launch_recurrent(const RecParams& p, int act_dtype, int out_dtype, i
 }
 
 cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream) {
-    const size_t per = p.S_elems / 4;
+    const size_t per = p.ring_cur ? p.conv_bytes / 16 : p.S_elems / 4;   // a ring moves the conv rows only
     unsigned bx = static_cast<unsigned>((per + 255) / 256);
     if (bx > 64) bx = 64;
     if (bx < 1) bx = 1;

@@ -109,7 +109,7 @@ recurrent_stream_kernel(const RecParams p) {
         const uint32_t base = tc::smem_u32(sm + (i % kStages) * L.bytes);
         const uint32_t seg = 128 * es;   // one head's channels of one row
         mbar_expect_tx(mb, L.bytes);
-        const float* Sh = p.S_in + (static_cast<size_t>(b) * p.Hv + h) * kD * kD;
+        const float* Sh = rec_state_in(p, b) + static_cast<size_t>(h) * kD * kD;
         for (int q = 0; q < 4; ++q) bulk_g2s(base + q * 16384, Sh + q * 4096, 16384, mb);
         bulk_g2s(base + L.cw, p.conv_w + 4 * (kh * kD), 128 * 16, mb);
         bulk_g2s(base + L.cw + 128 * 16, p.conv_w + 4 * (p.Hk * kD + kh * kD), 128 * 16, mb);
@@ -202,7 +202,7 @@ recurrent_stream_kernel(const RecParams p) {
             const float kq = warp_sum(fmaf(kk.w, qq.w, fmaf(kk.z, qq.z, fmaf(kk.y, qq.y, kk.x * qq.x))));
             const float beta = gates[2 * t];
             const float eg = expf(gates[2 * t + 1]);
-            float* Sout = p.S_out + static_cast<size_t>(b) * p.S_out_b + static_cast<size_t>(t) * p.S_out_p +
+            float* Sout = rec_state_out(p, b, t) +
                           (static_cast<size_t>(h) * kD + warp * 16) * kD;
             // partial S.k and S.q of my 16 rows: slot 2rr = row rr . k, slot 2rr+1 = row rr . q
             float pv[32];

@@ -30,7 +30,10 @@
  * Conventions (all entry points):
  *   - Every pointer argument except the gdn_dims / gdn_weights structs and the
  *     cu_seqlens_host array is DEVICE memory, allocated and owned by the
- *     caller.  The library allocates nothing and keeps no state between calls.
+ *     caller.  The library allocates no memory.  Between calls it keeps one
+ *     auxiliary CUDA stream per device (created on first use by
+ *     gdn_prefill_chunked, which overlaps its two kernels on it) and the fixed
+ *     scratch array of gdn_prefill_chunked_static.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  A non-GDN_OK return from argument validation means
  *     nothing was enqueued.  GDN_E_CUDA reports a launch error.
@@ -159,6 +162,48 @@ gdn_status gdn_verify_k(const gdn_dims* dims, const gdn_weights* w, int32_t B, i
 gdn_status gdn_commit(const gdn_dims* dims, int32_t B, int32_t K, const int32_t* accept_len,
                       const void* conv_ckpt, const float* S_ckpt, void* conv_state, float* S,
                       gdn_stream_t stream);
+
+/*
+ * State ring for speculative decoding, with a commit that copies no state.
+ * The pages keep a state plane per drafted position so that a verify walk can
+ * roll back (the page's "Drafting" section; the NEXTN.md page's "GDN
+ * rollback"); gdn_verify_k + gdn_commit copy the accepted plane back into S.
+ * With a ring the accepted plane becomes the live state where it lies.
+ *   S_ring   [B][R][H_v][128][128] fp32: R state slots per sequence
+ *   ring_cur [B] int32 on the device: the live slot of each sequence, in 0..R-1
+ * A caller starts from slot 0 holding the state (e.g. after a prefill into it)
+ * and ring_cur all zero.
+ *
+ * gdn_verify_k_ring -- gdn_verify_k on the live slots: reads slot ring_cur[b],
+ * writes checkpoint p to slot (ring_cur[b] + 1 + p) % R (K + 1 <= R <=
+ * GDN_MAX_VERIFY_K + 1, so the live slot is never overwritten).  conv_state is
+ * read and conv_ckpt [B][K][3][C] written as in gdn_verify_k; checkpoints,
+ * outputs and conv checkpoints are bit-identical to gdn_verify_k's.
+ */
+gdn_status gdn_verify_k_ring(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t K, int32_t R,
+                             const void* x, const void* z, const void* a_raw, const void* b_raw,
+                             const void* conv_state, float* S_ring, const int32_t* ring_cur, void* conv_ckpt,
+                             void* out, float* prenorm_out, int32_t* dev_status, gdn_stream_t stream);
+
+/*
+ * gdn_commit_ring -- after gdn_verify_k_ring, accept accept_len[b] positions
+ * (device int32 [B], each in 1..K): copies conv checkpoint accept_len[b]-1 into
+ * conv_state[b] and sets ring_cur[b] = (ring_cur[b] + accept_len[b]) % R, the
+ * slot of that state checkpoint.  A value outside 1..K leaves the sequence
+ * untouched.  K and R as in the verify.
+ */
+gdn_status gdn_commit_ring(const gdn_dims* dims, int32_t B, int32_t K, int32_t R, const int32_t* accept_len,
+                           const void* conv_ckpt, void* conv_state, int32_t* ring_cur, gdn_stream_t stream);
+
+/*
+ * gdn_decode_step_ring -- gdn_decode_step on the live slot of each sequence of
+ * a ring (1 <= R <= GDN_MAX_VERIFY_K + 1), updated in place; bit-identical to
+ * gdn_decode_step on that state.
+ */
+gdn_status gdn_decode_step_ring(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t R, const void* x,
+                                const void* z, const void* a_raw, const void* b_raw, void* conv_state, float* S_ring,
+                                const int32_t* ring_cur, void* out, float* prenorm_out, int32_t* dev_status,
+                                gdn_stream_t stream);
 
 /*
  * gdn_prefill_workspace_bytes -- device scratch that gdn_prefill_chunked needs

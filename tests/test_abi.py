@@ -122,6 +122,34 @@ def test_verify_and_commit_validation():
     assert L.gdn_commit(ctypes.byref(d), 2, 3, base[0], base[1], base[2], base[3] + 4, base[4], None) == 3
 
 
+def test_ring_validation():
+    d = _dims()
+    w = _w()
+    L = gdn.library()
+    base = [FAKE * (i + 1) * 0x100 for i in range(12)]
+    # verify: B, K, R, x, z, a, b, conv_state, S_ring, ring_cur, conv_ckpt, out, prenorm, status, stream
+    ok = L.gdn_verify_k_ring(ctypes.byref(d), ctypes.byref(w), 0, 3, 4, *base[:9], None, None, None)
+    assert ok == 0                                                    # B = 0: no-op
+    for R in (3, 18):                                                 # R < K + 1, R > 17
+        assert L.gdn_verify_k_ring(ctypes.byref(d), ctypes.byref(w), 2, 3, R, *base[:9], None, None, None) == 1
+    args = base[:9]
+    args[6] = None                                                    # no ring_cur
+    assert L.gdn_verify_k_ring(ctypes.byref(d), ctypes.byref(w), 2, 3, 4, *args, None, None, None) == 1
+    args = base[:9]
+    args[7] = args[5]                                                 # conv_ckpt on S_ring
+    assert L.gdn_verify_k_ring(ctypes.byref(d), ctypes.byref(w), 2, 3, 4, *args, None, None, None) == 1
+    # commit: B, K, R, accept_len, conv_ckpt, conv_state, ring_cur
+    assert L.gdn_commit_ring(ctypes.byref(d), 2, 3, 3, *base[:4], None) == 1          # R < K + 1
+    assert L.gdn_commit_ring(ctypes.byref(d), 2, 3, 4, base[0], base[1], base[2], None, None) == 1
+    assert L.gdn_commit_ring(ctypes.byref(d), 2, 3, 4, base[0], base[1], base[1], base[3], None) == 1
+    assert L.gdn_commit_ring(ctypes.byref(d), 0, 3, 4, *base[:4], None) == 0
+    # decode: B, R, x, z, a, b, conv_state, S_ring, ring_cur, out, prenorm, status, stream
+    assert L.gdn_decode_step_ring(ctypes.byref(d), ctypes.byref(w), 2, 0, *base[:8], None, None, None) == 1
+    args = base[:8]
+    args[6] = None
+    assert L.gdn_decode_step_ring(ctypes.byref(d), ctypes.byref(w), 2, 2, *args, None, None, None) == 1
+
+
 def test_prefill_validation():
     d = _dims(Hk=16, Hv=48)
     w = _w()
