@@ -20,6 +20,10 @@ the timed region.  Under torchrun (N > 1) each rank runs its own replica (no
 collective on the data path: the layer shards by sequence and head) and the
 slowest rank's time is used.
 
+"extras" (skipped with --no-extras) times the two other configurations outside
+the step: decode at batch 1 as 1000 in-place steps captured in one CUDA graph,
+and the packed varlen prefill (8 sequences, T=65536, nonzero initial state).
+
 --impl reference times the CPU oracle (fp64, OpenMP) on the host cores on a
 bounded sample of the same step.
 """
@@ -50,13 +54,13 @@ L2_FLUSH_BYTES = 256 << 20
 
 
 # ------------------------------------------------------------------ algorithmic work
-def prefill_bytes(T, Hk, Hv, out_bytes=2, act_bytes=2, init_state=False):
+def prefill_bytes(T, Hk, Hv, out_bytes=2, act_bytes=2, init_state=False, n_seq=1):
     C = 128 * (2 * Hk + Hv)
     HvD = Hv * 128
     b = T * C * act_bytes + T * HvD * act_bytes + 2 * T * Hv * act_bytes + T * HvD * out_bytes
-    b += Hv * 128 * 128 * 4 + 3 * C * act_bytes                 # final S and conv state written
+    b += n_seq * (Hv * 128 * 128 * 4 + 3 * C * act_bytes)       # final S and conv state written
     if init_state:
-        b += Hv * 128 * 128 * 4 + 3 * C * act_bytes             # initial state read
+        b += n_seq * (Hv * 128 * 128 * 4 + 3 * C * act_bytes)   # initial state read
     b += C * 16 + Hv * 8 + 128 * 4                              # weights
     return b
 
@@ -398,6 +402,99 @@ def run_gpu(args, rank, world):
     return line
 
 
+def run_extras(dev, warmup, reps):
+    """The two other timed configurations, outside the step: decode at batch 1
+    (1000 in-place steps captured in one CUDA graph; the 4.5 MB working set
+    stays in L2, so its bandwidth is not an HBM figure) and the packed varlen
+    prefill (8 sequences, T=65536, nonzero initial state, L2 flushed)."""
+    import gated_deltanet_linear_decode_gb300 as gdn
+    hbm, _, _ = peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    out = {}
+
+    def timed(fn, flush_l2):
+        ms = []
+        for it in range(warmup + reps):
+            if flush_l2:
+                flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= warmup:
+                ms.append(e0.elapsed_time(e1))
+        return statistics.mean(ms)
+
+    # decode B=1, 1000 steps per graph replay
+    c = gdn_inputs.decode_b1()
+    d = gdn.make_dims(c.Hk, c.Hv, torch.bfloat16, torch.bfloat16)
+    w = gdn.make_weights(c.conv_w, c.dt_bias, c.ssm_a, c.norm_w, device=dev)
+    i = {k: getattr(c, k).to(dev) for k in ("x", "z", "a_raw", "b_raw")}
+    conv, S = c.conv0.to(dev), c.S0.to(dev)
+    o = torch.empty(1, c.Hv * 128, device=dev, dtype=torch.bfloat16)
+    n_steps = 1000
+    step = lambda: gdn.gdn_decode_step(d, w, i["x"], i["z"], i["a_raw"], i["b_raw"], conv, S, o)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(n_steps):
+            step()
+    torch.cuda.synchronize()
+    gm = timed(graph.replay, False)
+    b1 = decode_bytes(1, c.Hk, c.Hv)
+    out["decode_B1_graph_1000"] = {"tokens_per_s": n_steps / (gm / 1e3), "us_per_step": 1e3 * gm / n_steps,
+                                   "launches_per_replay": n_steps, "bytes_per_step": b1,
+                                   "achieved_GBps": b1 * n_steps / (gm / 1e3) / 1e9,
+                                   "note": "state resident in L2 across steps; not an HBM roofline"}
+    del graph
+
+    # packed varlen prefill, 8 sequences, T=65536
+    c = gdn_inputs.varlen_t65536()
+    d = gdn.make_dims(c.Hk, c.Hv, torch.bfloat16, torch.bfloat16)
+    w = gdn.make_weights(c.conv_w, c.dt_bias, c.ssm_a, c.norm_w, device=dev)
+    i = {k: getattr(c, k).to(dev) for k in ("x", "z", "a_raw", "b_raw")}
+    cu_h = c.cu_seqlens.to(torch.int32)
+    cu_d = cu_h.to(dev)
+    conv0, S0 = c.conv0.to(dev), c.S0.to(dev)
+    conv, S = conv0.clone(), S0.clone()
+    po = torch.empty(c.T, c.Hv * 128, device=dev, dtype=torch.bfloat16)
+    nws = gdn.gdn_prefill_workspace_bytes(d, c.N, c.T)
+    ws = torch.empty(max(nws, 16), device=dev, dtype=torch.uint8)
+
+    def call():
+        conv.copy_(conv0)
+        S.copy_(S0)
+        e0.record(stream)
+        gdn.gdn_prefill_chunked(d, w, cu_h, cu_d, i["x"], i["z"], i["a_raw"], i["b_raw"], conv, S, po,
+                                zero_init=False, workspace=ws)
+        e1.record(stream)
+
+    ms = []
+    for it in range(warmup + reps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        call()
+        torch.cuda.synchronize()
+        if it >= warmup:
+            ms.append(e0.elapsed_time(e1))
+    vm = statistics.mean(ms)
+    vb = prefill_bytes(c.T, c.Hk, c.Hv, init_state=True, n_seq=c.N)
+    out["prefill_varlen_N8_T65536"] = {"tokens_per_s": c.T / (vm / 1e3), "ms": vm,
+                                       "lengths": [int(v) for v in (cu_h[1:] - cu_h[:-1])],
+                                       "roofline": {"bound": "hbm", "achieved": vb / (vm / 1e3) / 1e9,
+                                                    "peak": hbm, "unit": "GB/s",
+                                                    "frac": vb / (vm / 1e3) / 1e9 / hbm,
+                                                    "algorithmic_bytes": vb}}
+    return out
+
+
 def run_part(args):
     """Warm-up then timed launches of one part only (profiling aid)."""
     dev = torch.device("cuda", 0)
@@ -499,6 +596,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the batch-1 graph decode and the varlen T=65536 prefill (timed outside the step)")
     ap.add_argument("--only", choices=["prefill", "decode", "verify"], default=None,
                     help="run only one part of the step (for profiling); no JSON line")
     args = ap.parse_args()
@@ -516,6 +615,9 @@ def main():
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         torch.distributed.init_process_group("nccl")
     line = run_gpu(args, rank, world)
+    if rank == 0 and not args.no_extras:
+        line["extras"] = run_extras(torch.device("cuda", torch.cuda.current_device()), max(args.warmup, 1),
+                                    max(1, min(args.steps, 5)))
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()

@@ -25,7 +25,7 @@ __all__ = [
     "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step",
     "gdn_verify_k", "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked",
     "gdn_prefill_chunked_static", "gdn_verify_k_ring", "gdn_commit_ring", "gdn_decode_step_ring",
-    "PREFILL_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "HEAD_DIM",
+    "gdn_state_faults", "gdn_state_reset", "PREFILL_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "HEAD_DIM",
 ]
 
 HEAD_DIM = 128
@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step",
     "gdn_verify_k", "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked",
     "gdn_prefill_chunked_static", "gdn_verify_k_ring", "gdn_commit_ring", "gdn_decode_step_ring",
+    "gdn_state_faults", "gdn_state_reset",
 )
 
 
@@ -86,6 +87,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         "gdn_verify_k_ring": (ctypes.c_int, [D, W, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P]),
         "gdn_commit_ring": (ctypes.c_int, [D, I32, I32, I32, P, P, P, P, P]),
         "gdn_decode_step_ring": (ctypes.c_int, [D, W, I32, I32, P, P, P, P, P, P, P, P, P, P, P]),
+        "gdn_state_faults": (ctypes.c_int, [D, I32, P, I32, P, P]),
+        "gdn_state_reset": (ctypes.c_int, [D, I32, I32, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -277,6 +280,33 @@ def gdn_decode_step_ring(dims: GdnDims, w: Weights, x, z, a_raw, b_raw, conv_sta
         ctypes.byref(dims), ctypes.byref(w.struct()), B, R, _ptr(x), _ptr(z), _ptr(a_raw), _ptr(b_raw),
         _ptr(conv_state), _ptr(S_ring), _ptr(ring_cur), _ptr(out), _ptr(prenorm_out), _ptr(dev_status),
         _stream(stream)))
+
+
+def gdn_state_faults(dims: GdnDims, dev_status, cap: int, report=None, stream=None):
+    """Summary of the non-finite status words: int32 [2 + 2*cap] on the device holding the exact
+    count of faulted (sequence, v-head) pairs, the listed count, then (n*H_v + h, bits) pairs."""
+    if dev_status.numel() % dims.H_v:
+        raise ValueError("dev_status must hold N*H_v words")
+    _need(dev_status, torch.int32, (dev_status.numel(),))
+    if report is None:
+        report = torch.zeros(2 + 2 * cap, dtype=torch.int32, device=dev_status.device)
+    _need(report, torch.int32, (2 + 2 * cap,))
+    _check("gdn_state_faults", library().gdn_state_faults(
+        ctypes.byref(dims), dev_status.numel() // dims.H_v, _ptr(dev_status), cap, _ptr(report), _stream(stream)))
+    return report
+
+
+def gdn_state_reset(dims: GdnDims, S, dev_status, conv_state=None, ring_cur=None, stream=None) -> None:
+    """Zero the state of every faulted (sequence, v-head) -- the live ring slot when ring_cur is
+    given -- and the conv rows of their sequences when conv_state is given; clear dev_status."""
+    N = S.shape[0]
+    R = S.shape[1] if ring_cur is not None else 0
+    shape = (N, R, dims.H_v, HEAD_DIM, HEAD_DIM) if ring_cur is not None else (N, dims.H_v, HEAD_DIM, HEAD_DIM)
+    _need(S, torch.float32, shape); _need(dev_status, torch.int32, (N * dims.H_v,))
+    _need(ring_cur, torch.int32, (N,), optional=True)
+    _need(conv_state, _act(dims), (N, 3, HEAD_DIM * (2 * dims.H_k + dims.H_v)), optional=True)
+    _check("gdn_state_reset", library().gdn_state_reset(
+        ctypes.byref(dims), N, R, _ptr(S), _ptr(ring_cur), _ptr(conv_state), _ptr(dev_status), _stream(stream)))
 
 
 def gdn_prefill_workspace_bytes(dims: GdnDims, n_seq: int, T_total: int) -> int:

@@ -264,6 +264,39 @@ gdn_status gdn_commit_ring(const gdn_dims* dims, int32_t B, int32_t K, int32_t R
     return cuda_status(gdn::launch_commit(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+gdn_status gdn_state_faults(const gdn_dims* dims, int32_t N, const int32_t* dev_status, int32_t cap,
+                            int32_t* report, gdn_stream_t stream) {
+    gdn_status s = check_dims(dims);
+    if (s != GDN_OK) return s;
+    if (N < 0 || cap < 0 || static_cast<int64_t>(N) * dims->H_v > INT32_MAX) return GDN_E_INVALID_ARG;
+    if ((s = check_ptrs({dev_status, report}, {})) != GDN_OK) return s;
+    const size_t n = static_cast<size_t>(N) * dims->H_v;
+    const Range ins[] = {{dev_status, n * 4}};
+    const Range outs[] = {{report, (2 + 2 * static_cast<size_t>(cap)) * 4}};
+    if (any_overlap(outs, 1, ins, 1)) return GDN_E_INVALID_ARG;
+    return cuda_status(gdn::launch_state_faults(dev_status, static_cast<int>(n), cap, report,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_state_reset(const gdn_dims* dims, int32_t N, int32_t R, float* S, const int32_t* ring_cur,
+                           void* conv_state, int32_t* dev_status, gdn_stream_t stream) {
+    gdn_status s = check_dims(dims);
+    if (s != GDN_OK) return s;
+    if (N < 0 || R < 0 || R > GDN_MAX_VERIFY_K + 1 || (R > 0) != (ring_cur != nullptr)) return GDN_E_INVALID_ARG;
+    if (N == 0) return GDN_OK;
+    if ((s = check_ptrs({S, dev_status}, {ring_cur, conv_state})) != GDN_OK) return s;
+    gdn::ResetParams p{};
+    p.N = N; p.Hv = dims->H_v; p.R = R; p.S = S; p.ring_cur = ring_cur; p.conv_state = conv_state;
+    p.conv_bytes = 3 * static_cast<size_t>(kD) * (2 * dims->H_k + dims->H_v) * act_size(dims->act_dtype);
+    p.dev_status = dev_status;
+    const size_t S_bytes = static_cast<size_t>(N) * (R > 0 ? R : 1) * dims->H_v * kD * kD * 4;
+    const Range ins[] = {{ring_cur, N * 4u}};
+    const Range outs[] = {{S, S_bytes}, {conv_state, conv_state ? p.conv_bytes * N : 0},
+                          {dev_status, static_cast<size_t>(N) * dims->H_v * 4}};
+    if (any_overlap(outs, 3, ins, 1)) return GDN_E_INVALID_ARG;
+    return cuda_status(gdn::launch_state_reset(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t n_seq, int64_t T_total) {
     if (check_dims(dims) != GDN_OK || n_seq < 0 || T_total < 0) return 0;
     return gdn::prefill_workspace_bytes(dims->H_k, dims->H_v, n_seq, T_total, dims->act_dtype, dims->flags);

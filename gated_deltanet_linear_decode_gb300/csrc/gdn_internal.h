@@ -113,5 +113,16 @@ size_t recurrent_stream_smem(int K, int act_dtype);
 cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_dtype, int grid, cudaStream_t stream);
 cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream);
 cudaError_t launch_conv_init(void* dst, const void* src, size_t bytes, cudaStream_t stream);
+// Non-finite guard: summary of the status words, and the reset of the faulted states.
+cudaError_t launch_state_faults(const int* dev_status, int n, int cap, int* report, cudaStream_t stream);
+struct ResetParams {
+    int N, Hv, R;            // R = 0: plain S [N][Hv][128][128]; else a ring [N][R][Hv][128][128]
+    float* S;
+    const int* ring_cur;     // [N] live slot (rings only)
+    void* conv_state;        // [N][conv_bytes] or null
+    size_t conv_bytes;
+    const int* dev_status;   // [N*Hv]
+};
+cudaError_t launch_state_reset(const ResetParams& p, cudaStream_t stream);
 
 }  // namespace gdn

@@ -256,6 +256,66 @@ __global__ void conv_init_kernel(uint4* dst, const uint4* src, size_t n16) {
         dst[i] = src ? src[i] : make_uint4(0, 0, 0, 0);
 }
 
+// Status summary: the exact count of nonzero words, and the first `cap` of them
+// (index, bits) in increasing index order.  One block of 1024 threads walks the
+// words in tiles; a ballot per warp and a prefix over the warps give each
+// faulted word its rank.
+__global__ void __launch_bounds__(1024) state_faults_kernel(const int* st, int n, int cap, int* rep) {
+    __shared__ int warp_cnt[32];
+    __shared__ int base;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) base = 0;
+    __syncthreads();
+    for (int start = 0; start < n; start += 1024) {
+        const int i = start + tid;
+        const int v = i < n ? st[i] : 0;
+        const unsigned m = __ballot_sync(0xffffffffu, v != 0);
+        if (lane == 0) warp_cnt[warp] = __popc(m);
+        __syncthreads();
+        int pos = base + __popc(m & ((1u << lane) - 1u));
+        for (int w = 0; w < warp; ++w) pos += warp_cnt[w];
+        if (v != 0 && pos < cap) {
+            rep[2 + 2 * pos] = i;
+            rep[3 + 2 * pos] = v;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int t = 0;
+            for (int w = 0; w < 32; ++w) t += warp_cnt[w];
+            base += t;
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        rep[0] = base;
+        rep[1] = min(base, cap);
+    }
+}
+
+// Reset of the faulted states: block (n, h) zeroes the live plane of (n, h) when
+// its status word is nonzero, and its share of the conv rows of sequence n when
+// any head of n is faulted.  The status words are read only; the host clears
+// them after this kernel.
+__global__ void state_reset_kernel(const ResetParams p) {
+    const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int* st = p.dev_status + static_cast<size_t>(n) * p.Hv;
+    if (st[h] != 0) {
+        const size_t slot = p.R > 0 ? static_cast<size_t>(n) * p.R + p.ring_cur[n] : static_cast<size_t>(n);
+        float4* plane = reinterpret_cast<float4*>(p.S + ((slot * p.Hv) + h) * kD * kD);
+        for (int e = tid; e < kD * kD / 4; e += blockDim.x) plane[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (p.conv_state) {
+        int any = 0;
+        for (int j = tid; j < p.Hv; j += blockDim.x) any |= st[j];
+        if (__syncthreads_or(any)) {
+            uint4* c = reinterpret_cast<uint4*>(static_cast<char*>(p.conv_state) + static_cast<size_t>(n) * p.conv_bytes);
+            for (size_t e = static_cast<size_t>(h) * blockDim.x + tid; e < p.conv_bytes / 16;
+                 e += static_cast<size_t>(p.Hv) * blockDim.x)
+                c[e] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
 template <typename Tact, typename Tout>
 cudaError_t launch_rec_t(const RecParams& p, int rpc, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
@@ -316,6 +376,18 @@ cudaError_t launch_conv_init(void* dst, const void* src, size_t bytes, cudaStrea
     if (blocks < 1) blocks = 1;
     conv_init_kernel<<<blocks, 256, 0, stream>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16);
     return cudaGetLastError();
+}
+
+cudaError_t launch_state_faults(const int* dev_status, int n, int cap, int* report, cudaStream_t stream) {
+    state_faults_kernel<<<1, 1024, 0, stream>>>(dev_status, n, cap, report);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_reset(const ResetParams& p, cudaStream_t stream) {
+    state_reset_kernel<<<dim3(p.N, p.Hv), 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return cudaMemsetAsync(const_cast<int*>(p.dev_status), 0, static_cast<size_t>(p.N) * p.Hv * sizeof(int), stream);
 }
 
 }  // namespace gdn

@@ -206,6 +206,38 @@ gdn_status gdn_decode_step_ring(const gdn_dims* dims, const gdn_weights* w, int3
                                 gdn_stream_t stream);
 
 /*
+ * Non-finite state guard (the home-server page's GDN state faults: a
+ * non-finite recurrent state for one slot and two heads that stayed in the
+ * cached state and was re-seeded on every later turn, while a report cap for
+ * the life of the process had already silenced the fault reports).  The
+ * detection is the dev_status word per (sequence, v-head) described above,
+ * which every kernel ORs into under GDN_FLAG_CHECK_FINITE and which nothing
+ * caps; these two calls read and act on those words.
+ *
+ * gdn_state_faults -- summarise dev_status [N*H_v] into report, int32
+ * [2 + 2*cap] on the device: report[0] = the number of nonzero words (always
+ * exact), report[1] = min(report[0], cap), then for i < report[1]:
+ * report[2+2i] = n*H_v + h and report[3+2i] = its status bits, in increasing
+ * index order.  The cap bounds only the listing.  dev_status is not changed.
+ * GDN_E_INVALID_ARG for N < 0, cap < 0, N*H_v > INT32_MAX or overlapping
+ * buffers.
+ */
+gdn_status gdn_state_faults(const gdn_dims* dims, int32_t N, const int32_t* dev_status, int32_t cap,
+                            int32_t* report, gdn_stream_t stream);
+
+/*
+ * gdn_state_reset -- zero the recurrent state of every (n, h) whose
+ * dev_status word is nonzero: the plane S[n][h], or with a state ring
+ * (R >= 1 and ring_cur given) the live plane S_ring[n][ring_cur[n]][h]; when
+ * conv_state is not NULL, also the conv rows of every sequence with at least
+ * one such head.  Every dev_status word is then 0.  States of the other heads
+ * and sequences are not touched.  R = 0 with ring_cur NULL for a plain
+ * S [N][H_v][128][128]; anything else is GDN_E_INVALID_ARG.
+ */
+gdn_status gdn_state_reset(const gdn_dims* dims, int32_t N, int32_t R, float* S, const int32_t* ring_cur,
+                           void* conv_state, int32_t* dev_status, gdn_stream_t stream);
+
+/*
  * gdn_prefill_workspace_bytes -- device scratch that gdn_prefill_chunked needs
  * for n_seq sequences totalling T_total tokens (0 if none).
  */

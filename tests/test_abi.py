@@ -150,6 +150,24 @@ def test_ring_validation():
     assert L.gdn_decode_step_ring(ctypes.byref(d), ctypes.byref(w), 2, 2, *args, None, None, None) == 1
 
 
+def test_guard_validation():
+    d = _dims()
+    L = gdn.library()
+    a, b, c = FAKE * 0x100, FAKE * 0x200, FAKE * 0x300
+    assert L.gdn_state_faults(ctypes.byref(d), -1, a, 4, b, None) == 1
+    assert L.gdn_state_faults(ctypes.byref(d), 2, a, -1, b, None) == 1
+    assert L.gdn_state_faults(ctypes.byref(d), 2, None, 4, b, None) == 1
+    assert L.gdn_state_faults(ctypes.byref(d), 2, a, 4, a + 16, None) == 1          # report overlaps the words
+    assert L.gdn_state_faults(ctypes.byref(d), 2, a, 4, b + 4, None) == 3
+    # reset: N, R, S, ring_cur, conv_state, dev_status
+    assert L.gdn_state_reset(ctypes.byref(d), 2, 2, a, None, None, b, None) == 1     # R without ring_cur
+    assert L.gdn_state_reset(ctypes.byref(d), 2, 0, a, c, None, b, None) == 1        # ring_cur without R
+    assert L.gdn_state_reset(ctypes.byref(d), 2, 18, a, c, None, b, None) == 1
+    assert L.gdn_state_reset(ctypes.byref(d), 0, 0, a, None, None, b, None) == 0     # no-op
+    assert L.gdn_state_reset(ctypes.byref(d), 2, 0, a, None, None, a + 64, None) == 1   # status inside S
+    assert L.gdn_state_reset(ctypes.byref(d), 2, 0, None, None, None, b, None) == 1
+
+
 def test_prefill_validation():
     d = _dims(Hk=16, Hv=48)
     w = _w()
