@@ -65,9 +65,9 @@ def prefill_bytes(T, Hk, Hv, out_bytes=2, act_bytes=2, init_state=False, n_seq=1
     return b
 
 
-def decode_bytes(B, Hk, Hv, K=1, act_bytes=2, out_bytes=2, ckpt=False):
+def decode_bytes(B, Hk, Hv, K=1, act_bytes=2, out_bytes=2, ckpt=False, state_bytes=4):
     C = 128 * (2 * Hk + Hv)
-    per_seq = 2 * Hv * 128 * 128 * 4 if not ckpt else Hv * 128 * 128 * 4 * (1 + K)
+    per_seq = 2 * Hv * 128 * 128 * state_bytes if not ckpt else Hv * 128 * 128 * state_bytes * (1 + K)
     per_seq += (3 * C * act_bytes) * (2 if not ckpt else 1 + K)
     per_seq += K * (C + Hv * 128 + 2 * Hv) * act_bytes + K * Hv * 128 * out_bytes
     return B * per_seq + C * 16 + Hv * 8 + 128 * 4
@@ -406,7 +406,8 @@ def run_extras(dev, warmup, reps):
     """The two other timed configurations, outside the step: decode at batch 1
     (1000 in-place steps captured in one CUDA graph; the 4.5 MB working set
     stays in L2, so its bandwidth is not an HBM figure) and the packed varlen
-    prefill (8 sequences, T=65536, nonzero initial state, L2 flushed)."""
+    prefill (8 sequences, T=65536, nonzero initial state, L2 flushed); and the
+    B=64 decode with a bf16 state (L2 flushed)."""
     import gated_deltanet_linear_decode_gb300 as gdn
     hbm, _, _ = peaks()
     stream = torch.cuda.current_stream()
@@ -454,6 +455,21 @@ def run_extras(dev, warmup, reps):
                                    "achieved_GBps": b1 * n_steps / (gm / 1e3) / 1e9,
                                    "note": "state resident in L2 across steps; not an HBM roofline"}
     del graph
+
+    # decode B=64 with the state stored as bf16 (same inputs as the step's decode)
+    c = gdn_inputs.decode_b64()
+    d = gdn.make_dims(c.Hk, c.Hv, torch.bfloat16, torch.bfloat16, state_dtype=torch.bfloat16)
+    w = gdn.make_weights(c.conv_w, c.dt_bias, c.ssm_a, c.norm_w, device=dev)
+    i = {k: getattr(c, k).to(dev) for k in ("x", "z", "a_raw", "b_raw")}
+    conv, S = c.conv0.to(dev), c.S0.to(dev).to(torch.bfloat16)
+    o = torch.empty(c.N, c.Hv * 128, device=dev, dtype=torch.bfloat16)
+    bm = timed(lambda: gdn.gdn_decode_step(d, w, i["x"], i["z"], i["a_raw"], i["b_raw"], conv, S, o), True)
+    bb = decode_bytes(c.N, c.Hk, c.Hv, state_bytes=2)
+    out["decode_B64_state_bf16"] = {"tokens_per_s": c.N / (bm / 1e3), "us": 1e3 * bm,
+                                    "roofline": {"bound": "hbm", "achieved": bb / (bm / 1e3) / 1e9, "peak": hbm,
+                                                 "unit": "GB/s", "frac": bb / (bm / 1e3) / 1e9 / hbm,
+                                                 "algorithmic_bytes": bb}}
+    del S, conv
 
     # packed varlen prefill, 8 sequences, T=65536
     c = gdn_inputs.varlen_t65536()

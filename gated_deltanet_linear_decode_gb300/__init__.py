@@ -32,6 +32,7 @@ HEAD_DIM = 128
 GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_CHECK_FINITE = 1
 GDN_FLAG_PREFILL_FP32 = 2
+GDN_FLAG_STATE_BF16 = 4
 PREFILL_STATIC_SCRATCH_BYTES = 128 * 1024 * 1024   # GDN_PREFILL_STATIC_SCRATCH_BYTES
 
 EXPORTED_SYMBOLS = (
@@ -120,8 +121,12 @@ def _dt(t: torch.dtype) -> int:
 
 
 def make_dims(Hk: int, Hv: int, act_dtype=torch.bfloat16, out_dtype=torch.float32, eps: float = 1e-6,
-              check_finite: bool = False, prefill_fp32: bool = False) -> GdnDims:
+              check_finite: bool = False, prefill_fp32: bool = False, state_dtype=torch.float32) -> GdnDims:
+    """state_dtype torch.bfloat16 selects GDN_FLAG_STATE_BF16 (bf16 activations only)."""
+    if state_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("state_dtype must be torch.float32 or torch.bfloat16")
     flags = (GDN_FLAG_CHECK_FINITE if check_finite else 0) | (GDN_FLAG_PREFILL_FP32 if prefill_fp32 else 0)
+    flags |= GDN_FLAG_STATE_BF16 if state_dtype == torch.bfloat16 else 0
     return GdnDims(Hk, Hv, eps, _dt(act_dtype), _dt(out_dtype), flags)
 
 
@@ -173,6 +178,10 @@ def _act(d: GdnDims):
     return torch.bfloat16 if d.act_dtype == GDN_BF16 else torch.float32
 
 
+def _st(d: GdnDims):
+    return torch.bfloat16 if d.flags & GDN_FLAG_STATE_BF16 else torch.float32
+
+
 def _out(d: GdnDims):
     return torch.bfloat16 if d.out_dtype == GDN_BF16 else torch.float32
 
@@ -195,7 +204,7 @@ def gdn_decode_step(dims: GdnDims, w: Weights, x, z, a_raw, b_raw, conv_state, S
     C, HvD = HEAD_DIM * (2 * dims.H_k + dims.H_v), dims.H_v * HEAD_DIM
     a = _act(dims)
     _need(x, a, (B, C)); _need(z, a, (B, HvD)); _need(a_raw, a, (B, dims.H_v)); _need(b_raw, a, (B, dims.H_v))
-    _need(conv_state, a, (B, 3, C)); _need(S, torch.float32, (B, dims.H_v, HEAD_DIM, HEAD_DIM))
+    _need(conv_state, a, (B, 3, C)); _need(S, _st(dims), (B, dims.H_v, HEAD_DIM, HEAD_DIM))
     _need(out, _out(dims), (B, HvD)); _need(prenorm_out, torch.float32, (B, HvD), optional=True)
     _need(dev_status, torch.int32, (B * dims.H_v,), optional=True)
     _check("gdn_decode_step", library().gdn_decode_step(
@@ -211,8 +220,8 @@ def gdn_verify_k(dims: GdnDims, w: Weights, K: int, x, z, a_raw, b_raw, conv_sta
     a = _act(dims)
     _need(x, a, (B * K, C)); _need(z, a, (B * K, HvD)); _need(a_raw, a, (B * K, dims.H_v))
     _need(b_raw, a, (B * K, dims.H_v)); _need(conv_state, a, (B, 3, C))
-    _need(S, torch.float32, (B, dims.H_v, HEAD_DIM, HEAD_DIM)); _need(conv_ckpt, a, (B, K, 3, C))
-    _need(S_ckpt, torch.float32, (B, K, dims.H_v, HEAD_DIM, HEAD_DIM)); _need(out, _out(dims), (B * K, HvD))
+    _need(S, _st(dims), (B, dims.H_v, HEAD_DIM, HEAD_DIM)); _need(conv_ckpt, a, (B, K, 3, C))
+    _need(S_ckpt, _st(dims), (B, K, dims.H_v, HEAD_DIM, HEAD_DIM)); _need(out, _out(dims), (B * K, HvD))
     _need(prenorm_out, torch.float32, (B * K, HvD), optional=True)
     _need(dev_status, torch.int32, (B * dims.H_v,), optional=True)
     _check("gdn_verify_k", library().gdn_verify_k(
@@ -227,8 +236,8 @@ def gdn_commit(dims: GdnDims, K: int, accept_len, conv_ckpt, S_ckpt, conv_state,
     C = HEAD_DIM * (2 * dims.H_k + dims.H_v)
     a = _act(dims)
     _need(accept_len, torch.int32, (B,)); _need(conv_ckpt, a, (B, K, 3, C))
-    _need(S_ckpt, torch.float32, (B, K, dims.H_v, HEAD_DIM, HEAD_DIM)); _need(conv_state, a, (B, 3, C))
-    _need(S, torch.float32, (B, dims.H_v, HEAD_DIM, HEAD_DIM))
+    _need(S_ckpt, _st(dims), (B, K, dims.H_v, HEAD_DIM, HEAD_DIM)); _need(conv_state, a, (B, 3, C))
+    _need(S, _st(dims), (B, dims.H_v, HEAD_DIM, HEAD_DIM))
     _check("gdn_commit", library().gdn_commit(
         ctypes.byref(dims), B, K, _ptr(accept_len), _ptr(conv_ckpt), _ptr(S_ckpt), _ptr(conv_state), _ptr(S),
         _stream(stream)))
@@ -243,7 +252,7 @@ def gdn_verify_k_ring(dims: GdnDims, w: Weights, K: int, x, z, a_raw, b_raw, con
     a = _act(dims)
     _need(x, a, (B * K, C)); _need(z, a, (B * K, HvD)); _need(a_raw, a, (B * K, dims.H_v))
     _need(b_raw, a, (B * K, dims.H_v)); _need(conv_state, a, (B, 3, C))
-    _need(S_ring, torch.float32, (B, R, dims.H_v, HEAD_DIM, HEAD_DIM)); _need(ring_cur, torch.int32, (B,))
+    _need(S_ring, _st(dims), (B, R, dims.H_v, HEAD_DIM, HEAD_DIM)); _need(ring_cur, torch.int32, (B,))
     _need(conv_ckpt, a, (B, K, 3, C)); _need(out, _out(dims), (B * K, HvD))
     _need(prenorm_out, torch.float32, (B * K, HvD), optional=True)
     _need(dev_status, torch.int32, (B * dims.H_v,), optional=True)
@@ -272,7 +281,7 @@ def gdn_decode_step_ring(dims: GdnDims, w: Weights, x, z, a_raw, b_raw, conv_sta
     C, HvD = HEAD_DIM * (2 * dims.H_k + dims.H_v), dims.H_v * HEAD_DIM
     a = _act(dims)
     _need(x, a, (B, C)); _need(z, a, (B, HvD)); _need(a_raw, a, (B, dims.H_v)); _need(b_raw, a, (B, dims.H_v))
-    _need(conv_state, a, (B, 3, C)); _need(S_ring, torch.float32, (B, R, dims.H_v, HEAD_DIM, HEAD_DIM))
+    _need(conv_state, a, (B, 3, C)); _need(S_ring, _st(dims), (B, R, dims.H_v, HEAD_DIM, HEAD_DIM))
     _need(ring_cur, torch.int32, (B,)); _need(out, _out(dims), (B, HvD))
     _need(prenorm_out, torch.float32, (B, HvD), optional=True)
     _need(dev_status, torch.int32, (B * dims.H_v,), optional=True)
@@ -302,7 +311,7 @@ def gdn_state_reset(dims: GdnDims, S, dev_status, conv_state=None, ring_cur=None
     N = S.shape[0]
     R = S.shape[1] if ring_cur is not None else 0
     shape = (N, R, dims.H_v, HEAD_DIM, HEAD_DIM) if ring_cur is not None else (N, dims.H_v, HEAD_DIM, HEAD_DIM)
-    _need(S, torch.float32, shape); _need(dev_status, torch.int32, (N * dims.H_v,))
+    _need(S, _st(dims), shape); _need(dev_status, torch.int32, (N * dims.H_v,))
     _need(ring_cur, torch.int32, (N,), optional=True)
     _need(conv_state, _act(dims), (N, 3, HEAD_DIM * (2 * dims.H_k + dims.H_v)), optional=True)
     _check("gdn_state_reset", library().gdn_state_reset(
@@ -328,7 +337,7 @@ def gdn_prefill_chunked(dims: GdnDims, w: Weights, cu_seqlens_host, cu_seqlens_d
     a = _act(dims)
     _need(cu_seqlens_dev, torch.int32, (N + 1,))
     _need(x, a, (T, C)); _need(z, a, (T, HvD)); _need(a_raw, a, (T, dims.H_v)); _need(b_raw, a, (T, dims.H_v))
-    _need(conv_state, a, (N, 3, C)); _need(S, torch.float32, (N, dims.H_v, HEAD_DIM, HEAD_DIM))
+    _need(conv_state, a, (N, 3, C)); _need(S, _st(dims), (N, dims.H_v, HEAD_DIM, HEAD_DIM))
     _need(out, _out(dims), (T, HvD)); _need(prenorm_out, torch.float32, (T, HvD), optional=True)
     _need(dev_status, torch.int32, (N * dims.H_v,), optional=True)
     need = gdn_prefill_workspace_bytes(dims, N, T)
@@ -362,7 +371,7 @@ def gdn_prefill_chunked_static(dims: GdnDims, w: Weights, cu_seqlens_host, cu_se
     a = _act(dims)
     _need(cu_seqlens_dev, torch.int32, (N + 1,))
     _need(x, a, (T, C)); _need(z, a, (T, HvD)); _need(a_raw, a, (T, dims.H_v)); _need(b_raw, a, (T, dims.H_v))
-    _need(conv_state, a, (N, 3, C)); _need(S, torch.float32, (N, dims.H_v, HEAD_DIM, HEAD_DIM))
+    _need(conv_state, a, (N, 3, C)); _need(S, _st(dims), (N, dims.H_v, HEAD_DIM, HEAD_DIM))
     _need(out, _out(dims), (T, HvD)); _need(prenorm_out, torch.float32, (T, HvD), optional=True)
     _need(dev_status, torch.int32, (N * dims.H_v,), optional=True)
     _check("gdn_prefill_chunked_static", library().gdn_prefill_chunked_static(

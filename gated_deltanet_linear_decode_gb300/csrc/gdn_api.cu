@@ -18,6 +18,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t act_size(int32_t dt) { return dt == GDN_BF16 ? 2 : 4; }
 
+// Bytes of one recurrent-state element (the storage type the flags select).
+size_t state_size(const gdn_dims* d) { return (d->flags & GDN_FLAG_STATE_BF16) ? 2 : 4; }
+
 struct Range {
     const void* p;
     size_t bytes;
@@ -49,8 +52,9 @@ gdn_status check_dims(const gdn_dims* d) {
     if ((d->act_dtype != GDN_F32 && d->act_dtype != GDN_BF16) ||
         (d->out_dtype != GDN_F32 && d->out_dtype != GDN_BF16))
         return GDN_E_INVALID_ARG;
-    if (d->flags & ~(GDN_FLAG_CHECK_FINITE | GDN_FLAG_PREFILL_FP32)) return GDN_E_INVALID_ARG;
+    if (d->flags & ~(GDN_FLAG_CHECK_FINITE | GDN_FLAG_PREFILL_FP32 | GDN_FLAG_STATE_BF16)) return GDN_E_INVALID_ARG;
     if (d->H_v / d->H_k > 16) return GDN_E_UNSUPPORTED;
+    if ((d->flags & GDN_FLAG_STATE_BF16) && d->act_dtype != GDN_BF16) return GDN_E_UNSUPPORTED;
     return GDN_OK;
 }
 
@@ -89,14 +93,14 @@ gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_E
 // least two (sequence, q/k-group) items per SM and its stages fit in shared
 // memory; the cluster kernel otherwise.  The choice depends on B, H_k and K
 // only, never on the data.
-bool use_stream_kernel(int B, int Hk, int K, int act_dtype, int* grid) {
+bool use_stream_kernel(int B, int Hk, int K, int act_dtype, bool state_bf16, int* grid) {
     int dev = 0, sms = 0, smem = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
     const long long items = static_cast<long long>(B) * Hk;
     if (items < 2LL * sms) return false;
-    if (gdn::recurrent_stream_smem(K, act_dtype) > static_cast<size_t>(smem)) return false;
+    if (gdn::recurrent_stream_smem(K, act_dtype, state_bf16) > static_cast<size_t>(smem)) return false;
     *grid = sms;
     return true;
 }
@@ -136,7 +140,7 @@ gdn_status gdn_conv_state_init(const gdn_dims* dims, int32_t n_seq, void* conv_s
 // ring_cur != nullptr: S_in == S_out is a state ring [B][R][H_v][128][128] (see gdn_verify_k_ring).
 static gdn_status recurrent_common(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t K,
                                    const void* x, const void* z, const void* a_raw, const void* b_raw,
-                                   const void* conv_in, const float* S_in, void* conv_out, float* S_out,
+                                   const void* conv_in, const void* S_in, void* conv_out, void* S_out,
                                    bool verify, void* out, float* prenorm_out, int32_t* dev_status,
                                    gdn_stream_t stream, const int32_t* ring_cur = nullptr, int32_t R = 0) {
     gdn_status s = check_dims(dims);
@@ -153,7 +157,7 @@ static gdn_status recurrent_common(const gdn_dims* dims, const gdn_weights* w, i
     const size_t ea = act_size(dims->act_dtype), eo = act_size(dims->out_dtype);
     const size_t T = static_cast<size_t>(B) * K;
     const size_t HvD = static_cast<size_t>(Hv) * kD;
-    const size_t S_bytes = static_cast<size_t>(B) * Hv * kD * kD * 4;
+    const size_t S_bytes = static_cast<size_t>(B) * Hv * kD * kD * state_size(dims);
     const size_t cv_bytes = static_cast<size_t>(B) * 3 * C * ea;
     // a ring is read and written in one buffer (like the in-place decode state)
     const size_t S_out_bytes = ring_cur ? S_bytes * R : (verify ? S_bytes * K : S_bytes);
@@ -186,7 +190,7 @@ static gdn_status recurrent_common(const gdn_dims* dims, const gdn_weights* w, i
     p.out = out; p.prenorm = prenorm_out; p.dev_status = dev_status;
     p.ring_cur = ring_cur; p.ring_R = R; p.ring_shift = verify ? 1 : 0;
     int grid = 0;
-    if (use_stream_kernel(B, Hk, K, dims->act_dtype, &grid))
+    if (use_stream_kernel(B, Hk, K, dims->act_dtype, (dims->flags & GDN_FLAG_STATE_BF16) != 0, &grid))
         return cuda_status(gdn::launch_recurrent_stream(p, dims->act_dtype, dims->out_dtype, grid,
                                                         reinterpret_cast<cudaStream_t>(stream)));
     return cuda_status(gdn::launch_recurrent(p, dims->act_dtype, dims->out_dtype, rpc,
@@ -194,7 +198,7 @@ static gdn_status recurrent_common(const gdn_dims* dims, const gdn_weights* w, i
 }
 
 gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, int32_t B, const void* x, const void* z,
-                           const void* a_raw, const void* b_raw, void* conv_state, float* S, void* out,
+                           const void* a_raw, const void* b_raw, void* conv_state, void* S, void* out,
                            float* prenorm_out, int32_t* dev_status, gdn_stream_t stream) {
     return recurrent_common(dims, w, B, 1, x, z, a_raw, b_raw, conv_state, S, conv_state, S, false, out,
                             prenorm_out, dev_status, stream);
@@ -202,14 +206,14 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, int32_t B
 
 gdn_status gdn_verify_k(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t K, const void* x,
                         const void* z, const void* a_raw, const void* b_raw, const void* conv_state,
-                        const float* S, void* conv_ckpt, float* S_ckpt, void* out, float* prenorm_out,
+                        const void* S, void* conv_ckpt, void* S_ckpt, void* out, float* prenorm_out,
                         int32_t* dev_status, gdn_stream_t stream) {
     return recurrent_common(dims, w, B, K, x, z, a_raw, b_raw, conv_state, S, conv_ckpt, S_ckpt, true, out,
                             prenorm_out, dev_status, stream);
 }
 
 gdn_status gdn_commit(const gdn_dims* dims, int32_t B, int32_t K, const int32_t* accept_len, const void* conv_ckpt,
-                      const float* S_ckpt, void* conv_state, float* S, gdn_stream_t stream) {
+                      const void* S_ckpt, void* conv_state, void* S, gdn_stream_t stream) {
     gdn_status s = check_dims(dims);
     if (s != GDN_OK) return s;
     if (B < 0 || K < 1 || K > GDN_MAX_VERIFY_K) return GDN_E_INVALID_ARG;
@@ -219,16 +223,16 @@ gdn_status gdn_commit(const gdn_dims* dims, int32_t B, int32_t K, const int32_t*
     gdn::CommitParams p{};
     p.B = B; p.K = K; p.accept_len = accept_len; p.conv_ckpt = conv_ckpt; p.S_ckpt = S_ckpt;
     p.conv_state = conv_state; p.S = S;
-    p.S_elems = static_cast<size_t>(dims->H_v) * kD * kD;
+    p.S_bytes = static_cast<size_t>(dims->H_v) * kD * kD * state_size(dims);
     p.conv_bytes = 3 * C * act_size(dims->act_dtype);
-    const Range ins[] = {{accept_len, B * 4u}, {conv_ckpt, p.conv_bytes * B * K}, {S_ckpt, p.S_elems * 4 * B * K}};
-    const Range outs[] = {{conv_state, p.conv_bytes * B}, {S, p.S_elems * 4 * B}};
+    const Range ins[] = {{accept_len, B * 4u}, {conv_ckpt, p.conv_bytes * B * K}, {S_ckpt, p.S_bytes * B * K}};
+    const Range outs[] = {{conv_state, p.conv_bytes * B}, {S, p.S_bytes * B}};
     if (any_overlap(outs, 2, ins, 3)) return GDN_E_INVALID_ARG;
     return cuda_status(gdn::launch_commit(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gdn_status gdn_decode_step_ring(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t R, const void* x,
-                                const void* z, const void* a_raw, const void* b_raw, void* conv_state, float* S_ring,
+                                const void* z, const void* a_raw, const void* b_raw, void* conv_state, void* S_ring,
                                 const int32_t* ring_cur, void* out, float* prenorm_out, int32_t* dev_status,
                                 gdn_stream_t stream) {
     if (!ring_cur) return GDN_E_INVALID_ARG;
@@ -238,7 +242,7 @@ gdn_status gdn_decode_step_ring(const gdn_dims* dims, const gdn_weights* w, int3
 
 gdn_status gdn_verify_k_ring(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t K, int32_t R,
                              const void* x, const void* z, const void* a_raw, const void* b_raw,
-                             const void* conv_state, float* S_ring, const int32_t* ring_cur, void* conv_ckpt,
+                             const void* conv_state, void* S_ring, const int32_t* ring_cur, void* conv_ckpt,
                              void* out, float* prenorm_out, int32_t* dev_status, gdn_stream_t stream) {
     if (!ring_cur) return GDN_E_INVALID_ARG;
     return recurrent_common(dims, w, B, K, x, z, a_raw, b_raw, conv_state, S_ring, conv_ckpt, S_ring, true, out,
@@ -256,7 +260,7 @@ gdn_status gdn_commit_ring(const gdn_dims* dims, int32_t B, int32_t K, int32_t R
     gdn::CommitParams p{};
     p.B = B; p.K = K; p.accept_len = accept_len; p.conv_ckpt = conv_ckpt; p.conv_state = conv_state;
     p.ring_cur = ring_cur; p.ring_R = R;
-    p.S_elems = static_cast<size_t>(dims->H_v) * kD * kD;
+    p.S_bytes = static_cast<size_t>(dims->H_v) * kD * kD * state_size(dims);
     p.conv_bytes = 3 * C * act_size(dims->act_dtype);
     const Range ins[] = {{accept_len, B * 4u}, {conv_ckpt, p.conv_bytes * B * K}};
     const Range outs[] = {{conv_state, p.conv_bytes * B}, {ring_cur, B * 4u}};
@@ -278,7 +282,7 @@ gdn_status gdn_state_faults(const gdn_dims* dims, int32_t N, const int32_t* dev_
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
-gdn_status gdn_state_reset(const gdn_dims* dims, int32_t N, int32_t R, float* S, const int32_t* ring_cur,
+gdn_status gdn_state_reset(const gdn_dims* dims, int32_t N, int32_t R, void* S, const int32_t* ring_cur,
                            void* conv_state, int32_t* dev_status, gdn_stream_t stream) {
     gdn_status s = check_dims(dims);
     if (s != GDN_OK) return s;
@@ -287,9 +291,10 @@ gdn_status gdn_state_reset(const gdn_dims* dims, int32_t N, int32_t R, float* S,
     if ((s = check_ptrs({S, dev_status}, {ring_cur, conv_state})) != GDN_OK) return s;
     gdn::ResetParams p{};
     p.N = N; p.Hv = dims->H_v; p.R = R; p.S = S; p.ring_cur = ring_cur; p.conv_state = conv_state;
+    p.plane_bytes = static_cast<size_t>(kD) * kD * state_size(dims);
     p.conv_bytes = 3 * static_cast<size_t>(kD) * (2 * dims->H_k + dims->H_v) * act_size(dims->act_dtype);
     p.dev_status = dev_status;
-    const size_t S_bytes = static_cast<size_t>(N) * (R > 0 ? R : 1) * dims->H_v * kD * kD * 4;
+    const size_t S_bytes = static_cast<size_t>(N) * (R > 0 ? R : 1) * dims->H_v * p.plane_bytes;
     const Range ins[] = {{ring_cur, N * 4u}};
     const Range outs[] = {{S, S_bytes}, {conv_state, conv_state ? p.conv_bytes * N : 0},
                           {dev_status, static_cast<size_t>(N) * dims->H_v * 4}};
@@ -304,7 +309,7 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t n_seq, int64_t 
 
 gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, int32_t n_seq,
                                const int32_t* cu_seqlens_host, const int32_t* cu_seqlens_dev, const void* x,
-                               const void* z, const void* a_raw, const void* b_raw, void* conv_state, float* S,
+                               const void* z, const void* a_raw, const void* b_raw, void* conv_state, void* S,
                                int32_t zero_init, void* out, float* prenorm_out, void* workspace,
                                size_t workspace_bytes, int32_t* dev_status, gdn_stream_t stream) {
     gdn_status s = check_dims(dims);
@@ -335,7 +340,7 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, int32
                          {w->conv_w, C * 16}, {w->dt_bias, Hv * 4u}, {w->ssm_a, Hv * 4u}, {w->norm_w, kD * 4u},
                          {cu_seqlens_dev, (n_seq + 1) * 4u}};
     const Range outs[] = {{out, Tz * HvD * eo}, {prenorm_out, Tz * HvD * 4}, {dev_status, n_seq * Hv * 4u},
-                          {conv_state, n_seq * 3 * C * ea}, {S, static_cast<size_t>(n_seq) * Hv * kD * kD * 4},
+                          {conv_state, n_seq * 3 * C * ea}, {S, static_cast<size_t>(n_seq) * Hv * kD * kD * state_size(dims)},
                           {workspace, need}};
     if (any_overlap(outs, 6, ins, 9)) return GDN_E_INVALID_ARG;
 

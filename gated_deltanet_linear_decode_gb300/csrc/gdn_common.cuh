@@ -114,4 +114,47 @@ __device__ __forceinline__ void st_f4(float* p, float4 v) {
                  :: "l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
 }
 
+// ---------------------------------------------------------------- recurrent state storage
+// Four consecutive state elements <-> a float4, for the two storage types
+// (ld: a plain load through a generic pointer, global or shared memory).
+// bf16 -> fp32 is exact (the bf16 bits are the upper half of the fp32
+// pattern); fp32 -> bf16 rounds to nearest even.  round() gives the value a
+// store followed by a load would give, so a walk that keeps the state in
+// registers continues from exactly what a later call would read back.
+template <typename Ts>
+struct StateIO;
+
+template <>
+struct StateIO<float> {
+    __device__ static __forceinline__ float4 ld_stream(const float* p) { return ld_f4_stream(p); }
+    __device__ static __forceinline__ float4 ld(const void* p) { return *static_cast<const float4*>(p); }
+    __device__ static __forceinline__ float4 round(float4 v) { return v; }
+    __device__ static __forceinline__ void st(float* p, float4 v) { st_f4(p, v); }
+};
+
+template <>
+struct StateIO<__nv_bfloat16> {
+    __device__ static __forceinline__ uint32_t pack(float lo, float hi) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&v);
+    }
+    __device__ static __forceinline__ float4 unpack(uint32_t a, uint32_t b) {
+        return make_float4(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u), __uint_as_float(b << 16),
+                           __uint_as_float(b & 0xffff0000u));
+    }
+    __device__ static __forceinline__ float4 ld_stream(const __nv_bfloat16* p) {
+        uint32_t a, b;
+        asm volatile("ld.global.L1::no_allocate.v2.b32 {%0,%1}, [%2];" : "=r"(a), "=r"(b) : "l"(p));
+        return unpack(a, b);
+    }
+    __device__ static __forceinline__ float4 ld(const void* p) {
+        const uint2 v = *static_cast<const uint2*>(p);
+        return unpack(v.x, v.y);
+    }
+    __device__ static __forceinline__ float4 round(float4 v) { return unpack(pack(v.x, v.y), pack(v.z, v.w)); }
+    __device__ static __forceinline__ void st(__nv_bfloat16* p, float4 v) {
+        asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(pack(v.x, v.y)), "r"(pack(v.z, v.w)) : "memory");
+    }
+};
+
 }  // namespace gdn

@@ -10,6 +10,7 @@ namespace gdn {
 
 constexpr uint32_t kFlagCheckFinite = 1u;
 constexpr uint32_t kFlagForceSimt = 2u;   // GDN_FLAG_PREFILL_FP32
+constexpr uint32_t kFlagStateBf16 = 4u;   // GDN_FLAG_STATE_BF16: states stored as bf16
 
 // Recurrent walk (decode step when K == 1 and the outputs alias the states;
 // speculative verify when the outputs are the checkpoint planes).
@@ -28,9 +29,9 @@ struct RecParams {
     const float* ssm_a;     // [Hv]
     const float* norm_w;    // [128]
     const void* conv_in;    // [B][3][C]
-    const float* S_in;      // [B][Hv][128][128]
+    const void* S_in;       // [B][Hv][128][128], fp32 or bf16 (the kernel's state type)
     void* conv_out;         // element (b, t) at conv_out + b*conv_out_b + t*conv_out_p
-    float* S_out;           // state (b, t) at S_out + b*S_out_b + t*S_out_p
+    void* S_out;            // state (b, t) at S_out + b*S_out_b + t*S_out_p (elements)
     long long conv_out_b, conv_out_p;
     long long S_out_b, S_out_p;
     void* out;              // [B*K][Hv*128]
@@ -43,17 +44,21 @@ struct RecParams {
 };
 
 #ifdef __CUDACC__
-// The state a sequence starts from, and where the state after its position t goes.
-__device__ __forceinline__ const float* rec_state_in(const RecParams& p, int b) {
+// The state a sequence starts from, and where the state after its position t goes
+// (Ts: the element type of the state, float or __nv_bfloat16).
+template <typename Ts>
+__device__ __forceinline__ const Ts* rec_state_in(const RecParams& p, int b) {
     const size_t plane = static_cast<size_t>(p.Hv) * 128 * 128;
-    return p.ring_cur ? p.S_in + (static_cast<size_t>(b) * p.ring_R + p.ring_cur[b]) * plane
-                      : p.S_in + static_cast<size_t>(b) * plane;
+    const Ts* S = static_cast<const Ts*>(p.S_in);
+    return p.ring_cur ? S + (static_cast<size_t>(b) * p.ring_R + p.ring_cur[b]) * plane : S + static_cast<size_t>(b) * plane;
 }
-__device__ __forceinline__ float* rec_state_out(const RecParams& p, int b, int t) {
+template <typename Ts>
+__device__ __forceinline__ Ts* rec_state_out(const RecParams& p, int b, int t) {
     const size_t plane = static_cast<size_t>(p.Hv) * 128 * 128;
+    Ts* S = static_cast<Ts*>(p.S_out);
     if (p.ring_cur)
-        return p.S_out + (static_cast<size_t>(b) * p.ring_R + (p.ring_cur[b] + p.ring_shift + t) % p.ring_R) * plane;
-    return p.S_out + static_cast<size_t>(b) * p.S_out_b + static_cast<size_t>(t) * p.S_out_p;
+        return S + (static_cast<size_t>(b) * p.ring_R + (p.ring_cur[b] + p.ring_shift + t) % p.ring_R) * plane;
+    return S + static_cast<size_t>(b) * p.S_out_b + static_cast<size_t>(t) * p.S_out_p;
 }
 #endif
 
@@ -63,10 +68,10 @@ struct CommitParams {
     int ring_R;
     const int* accept_len;  // [B]
     const void* conv_ckpt;  // [B][K][3][C]
-    const float* S_ckpt;    // [B][K][Hv][128][128]
+    const void* S_ckpt;     // [B][K][Hv][128][128]
     void* conv_state;       // [B][3][C]
-    float* S;               // [B][Hv][128][128]
-    size_t S_elems;         // Hv*128*128
+    void* S;                // [B][Hv][128][128]
+    size_t S_bytes;         // Hv*128*128 * state element size
     size_t conv_bytes;      // 3*C*sizeof(act)
 };
 
@@ -89,7 +94,7 @@ struct PrefillParams {
     const float* ssm_a;
     const float* norm_w;
     void* conv_state;        // [n_seq][3][C] in/out
-    float* S;                // [n_seq][Hv][128][128] in/out
+    void* S;                 // [n_seq][Hv][128][128] in/out, fp32 (bf16 under kFlagStateBf16)
     void* out;
     float* prenorm;
     int* dev_status;
@@ -109,7 +114,7 @@ cudaError_t launch_prefill(const PrefillParams& p, int act_dtype, int out_dtype,
 
 cudaError_t launch_recurrent(const RecParams& p, int act_dtype, int out_dtype, int rows_per_cta,
                              cudaStream_t stream);
-size_t recurrent_stream_smem(int K, int act_dtype);
+size_t recurrent_stream_smem(int K, int act_dtype, bool state_bf16);
 cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_dtype, int grid, cudaStream_t stream);
 cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream);
 cudaError_t launch_conv_init(void* dst, const void* src, size_t bytes, cudaStream_t stream);
@@ -117,7 +122,8 @@ cudaError_t launch_conv_init(void* dst, const void* src, size_t bytes, cudaStrea
 cudaError_t launch_state_faults(const int* dev_status, int n, int cap, int* report, cudaStream_t stream);
 struct ResetParams {
     int N, Hv, R;            // R = 0: plain S [N][Hv][128][128]; else a ring [N][R][Hv][128][128]
-    float* S;
+    void* S;
+    size_t plane_bytes;      // 128*128 * state element size
     const int* ring_cur;     // [N] live slot (rings only)
     void* conv_state;        // [N][conv_bytes] or null
     size_t conv_bytes;

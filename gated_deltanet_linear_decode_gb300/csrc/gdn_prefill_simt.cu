@@ -92,10 +92,13 @@ prefill_simt_kernel(const PrefillParams p) {
     double* gam_s = reinterpret_cast<double*>(g_s + 64);   // [64]
 
     // ---- initial state
-    float* Sg = p.S + (static_cast<size_t>(s) * p.Hv + h) * kD * kD;
+    const bool sbf = (p.flags & kFlagStateBf16) != 0;
+    const size_t plane0 = (static_cast<size_t>(s) * p.Hv + h) * kD * kD;
+    float* Sg = static_cast<float*>(p.S) + plane0;                          // fp32 state
+    __nv_bfloat16* Sgb = static_cast<__nv_bfloat16*>(p.S) + plane0;         // bf16 state
     for (int e = tid; e < kD * kD; e += kThreads) {
         const int j = e >> 7, i = e & 127;
-        Ss[j * kLd + i] = p.zero_init ? 0.f : Sg[e];
+        Ss[j * kLd + i] = p.zero_init ? 0.f : (sbf ? __bfloat162float(Sgb[e]) : Sg[e]);
     }
 
     const Tact* x = static_cast<const Tact*>(p.x);
@@ -244,7 +247,10 @@ prefill_simt_kernel(const PrefillParams p) {
     bool bad_s = false;
     for (int e = tid; e < kD * kD; e += kThreads) {
         const float v = Ss[(e >> 7) * kLd + (e & 127)];
-        Sg[e] = v;
+        if (sbf)
+            Sgb[e] = __float2bfloat16_rn(v);
+        else
+            Sg[e] = v;
         if (p.flags & kFlagCheckFinite) bad_s |= nonfinite_bits(v);
     }
     if (p.dev_status && (p.flags & kFlagCheckFinite)) {
@@ -352,7 +358,8 @@ cudaError_t launch_tensor_core_prefill(const PrefillParams& p, int out_dtype, cu
     cudaError_t e = launch_chunk_table(p, stream);
     if (e != cudaSuccess) return e;
     const int nc = p.n_chunks;
-    int nseg = nc >= 64 ? 2 : 1;
+    // a bf16 state is rounded once, at the end: no segment boundary that would store it mid-sequence
+    int nseg = nc >= 64 && !(p.flags & kFlagStateBf16) ? 2 : 1;
     cudaStream_t side = nseg > 1 ? side_stream() : nullptr;
     if (!side) nseg = 1;
     if (nseg == 1) {

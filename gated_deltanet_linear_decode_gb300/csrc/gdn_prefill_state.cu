@@ -80,11 +80,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
     // through S (a launch that starts the sequence takes zeros instead under zero_init)
     const int cbase_s = p.chunk_base[s], nch_s = p.chunk_base[s + 1] - cbase_s;
     const int cb = max(0, p.chunk_lo - cbase_s), ce = min(nch_s, p.chunk_hi - cbase_s);
-    float* Sg = p.S + (static_cast<size_t>(s) * Hv + h) * kD * kD;
+    // the state plane of (s, h): fp32, or bf16 under kFlagStateBf16 (read into fp32, rounded once when stored)
+    const bool sbf = (p.flags & kFlagStateBf16) != 0;
+    const int ss = sbf ? 2 : 4;
+    uint8_t* Sg = static_cast<uint8_t*>(p.S) + (static_cast<size_t>(s) * Hv + h) * kD * kD * ss;
     if (cb >= ce) {
         // an empty sequence ends with its initial state: zeros under zero_init (written by the first launch)
         if (nch_s == 0 && p.zero_init && p.chunk_lo == 0)
-            for (int e = tid; e < kD * kD / 4; e += blockDim.x) reinterpret_cast<float4*>(Sg)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int e = tid; e < kD * kD * ss / 16; e += blockDim.x) reinterpret_cast<uint4*>(Sg)[e] = make_uint4(0, 0, 0, 0);
         return;
     }
     const bool zero_init = p.zero_init && cb == 0;
@@ -149,8 +152,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
             const int c = 2 * chalf + cc;
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
+                const uint8_t* src = Sg + (row * kD + 32 * c + i) * ss;
                 const float4 f = zero_init ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                             : *reinterpret_cast<const float4*>(Sg + row * kD + 32 * c + i);
+                                           : (sbf ? StateIO<__nv_bfloat16>::ld(src) : StateIO<float>::ld(src));
                 v[i] = f.x; v[i + 1] = f.y; v[i + 2] = f.z; v[i + 3] = f.w;
             }
             tc::tmem_st32(tl + kColS + 32 * c, v);
@@ -320,8 +324,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
                 tc::tmem_ld32(tl + kColS + 32 * col, v);
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
-                    *reinterpret_cast<float4*>(Sg + row * kD + 32 * col + i) =
-                        make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    uint8_t* dst = Sg + (row * kD + 32 * col + i) * ss;
+                    const float4 f = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    if (sbf)
+                        StateIO<__nv_bfloat16>::st(reinterpret_cast<__nv_bfloat16*>(dst), f);
+                    else
+                        StateIO<float>::st(reinterpret_cast<float*>(dst), f);
                     if (p.flags & kFlagCheckFinite)
                         bad |= nonfinite_bits(v[i]) | nonfinite_bits(v[i + 1]) | nonfinite_bits(v[i + 2]) |
                                nonfinite_bits(v[i + 3]);

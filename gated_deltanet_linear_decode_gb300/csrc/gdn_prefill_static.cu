@@ -44,7 +44,7 @@ cudaError_t scratch_address(void** addr) {
 extern "C" gdn_status gdn_prefill_chunked_static(const gdn_dims* dims, const gdn_weights* w, int32_t n_seq,
                                                  const int32_t* cu_seqlens_host, const int32_t* cu_seqlens_dev,
                                                  const void* x, const void* z, const void* a_raw, const void* b_raw,
-                                                 void* conv_state, float* S, int32_t zero_init, void* out,
+                                                 void* conv_state, void* S, int32_t zero_init, void* out,
                                                  float* prenorm_out, int32_t* dev_status, gdn_stream_t stream) {
     if (!dims || n_seq < 0 || !cu_seqlens_host) return GDN_E_INVALID_ARG;
     const size_t need = gdn_prefill_workspace_bytes(dims, n_seq, cu_seqlens_host[n_seq]);

@@ -44,7 +44,7 @@ __device__ __forceinline__ float conv4(float4 w, float x0, float x1, float x2, f
 #define GDN_REC_MIN_BLOCKS 8   // 8 CTAs of 128 threads per SM (64 registers)
 #endif
 
-template <typename Tact, typename Tout, int RPC>
+template <typename Tact, typename Tout, typename Ts, int RPC>
 __global__ void __launch_bounds__(RPC * 4, (GDN_REC_MIN_BLOCKS * 32 / RPC) > 0 ? (GDN_REC_MIN_BLOCKS * 32 / RPC) : 1)
 recurrent_kernel(const RecParams p) {
     constexpr int NT = RPC * 4;      // threads
@@ -69,11 +69,11 @@ recurrent_kernel(const RecParams p) {
     __shared__ float rms_part[kMaxK];
 
     // ---- state rows: issue the 128-bit loads before anything else
-    const float* Sin = rec_state_in(p, b) + static_cast<size_t>(h) * kD * kD + static_cast<size_t>(j0) * kD;
+    const Ts* Sin = rec_state_in<Ts>(p, b) + static_cast<size_t>(h) * kD * kD + static_cast<size_t>(j0) * kD;
     float4 s[8];
 #pragma unroll
     for (int rr = 0; rr < 8; ++rr)
-        s[rr] = ld_f4_stream(Sin + static_cast<size_t>(warp * 8 + rr) * kD + 4 * lane);
+        s[rr] = StateIO<Ts>::ld_stream(Sin + static_cast<size_t>(warp * 8 + rr) * kD + 4 * lane);
 
     // ---- per-thread channel ownership: thread i < 128 owns q channel i and k
     // channel i of head kh; thread t < RPC owns v channel j0 + t of head h.
@@ -158,15 +158,15 @@ recurrent_kernel(const RecParams p) {
             nv.y = fmaf(d, kk.y, eg * sv.y);
             nv.z = fmaf(d, kk.z, eg * sv.z);
             nv.w = fmaf(d, kk.w, eg * sv.w);
-            s[rr] = nv;
+            s[rr] = StateIO<Ts>::round(nv);                  // what the stored state reads back as
             o[rr] = fmaf(d, kq, eg * pq) * kInvSqrtD;        // o = S_new.q / sqrt(128)
         }
         // state out: in place for a decode step, checkpoint t for a verify walk
         {
-            float* Sout = rec_state_out(p, b, t) + static_cast<size_t>(h) * kD * kD + static_cast<size_t>(j0) * kD;
+            Ts* Sout = rec_state_out<Ts>(p, b, t) + static_cast<size_t>(h) * kD * kD + static_cast<size_t>(j0) * kD;
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr) {
-                st_f4(Sout + static_cast<size_t>(warp * 8 + rr) * kD + 4 * lane, s[rr]);
+                StateIO<Ts>::st(Sout + static_cast<size_t>(warp * 8 + rr) * kD + 4 * lane, s[rr]);
                 if (status && (nonfinite_bits(s[rr].x) | nonfinite_bits(s[rr].y) | nonfinite_bits(s[rr].z) |
                                nonfinite_bits(s[rr].w)))
                     atomicOr(status, 1);
@@ -234,9 +234,10 @@ __global__ void commit_kernel(const CommitParams p) {
         if (blockIdx.x == 0 && threadIdx.x == 0) p.ring_cur[b] = (p.ring_cur[b] + n) % p.ring_R;
         return;
     }
-    const float4* Ssrc = reinterpret_cast<const float4*>(p.S_ckpt + (static_cast<size_t>(b) * p.K + (n - 1)) * p.S_elems);
-    float4* Sdst = reinterpret_cast<float4*>(p.S + static_cast<size_t>(b) * p.S_elems);
-    const size_t nS = p.S_elems / 4;
+    const uint4* Ssrc = reinterpret_cast<const uint4*>(static_cast<const char*>(p.S_ckpt) +
+                                                       (static_cast<size_t>(b) * p.K + (n - 1)) * p.S_bytes);
+    uint4* Sdst = reinterpret_cast<uint4*>(static_cast<char*>(p.S) + static_cast<size_t>(b) * p.S_bytes);
+    const size_t nS = p.S_bytes / 16;
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < nS;
          i += static_cast<size_t>(gridDim.x) * blockDim.x)
         Sdst[i] = Ssrc[i];
@@ -301,8 +302,8 @@ __global__ void state_reset_kernel(const ResetParams p) {
     const int* st = p.dev_status + static_cast<size_t>(n) * p.Hv;
     if (st[h] != 0) {
         const size_t slot = p.R > 0 ? static_cast<size_t>(n) * p.R + p.ring_cur[n] : static_cast<size_t>(n);
-        float4* plane = reinterpret_cast<float4*>(p.S + ((slot * p.Hv) + h) * kD * kD);
-        for (int e = tid; e < kD * kD / 4; e += blockDim.x) plane[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        uint4* plane = reinterpret_cast<uint4*>(static_cast<char*>(p.S) + (slot * p.Hv + h) * p.plane_bytes);
+        for (size_t e = tid; e < p.plane_bytes / 16; e += blockDim.x) plane[e] = make_uint4(0, 0, 0, 0);
     }
     if (p.conv_state) {
         int any = 0;
@@ -316,7 +317,7 @@ __global__ void state_reset_kernel(const ResetParams p) {
     }
 }
 
-template <typename Tact, typename Tout>
+template <typename Tact, typename Tout, typename Ts>
 cudaError_t launch_rec_t(const RecParams& p, int rpc, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -332,17 +333,17 @@ cudaError_t launch_rec_t(const RecParams& p, int rpc, cudaStream_t stream) {
     cfg.stream = stream;
     switch (rpc) {
         case 32: {
-            auto k = recurrent_kernel<Tact, Tout, 32>;
+            auto k = recurrent_kernel<Tact, Tout, Ts, 32>;
             if (p.CS > 8) cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             return cudaLaunchKernelEx(&cfg, k, p);
         }
         case 64: {
-            auto k = recurrent_kernel<Tact, Tout, 64>;
+            auto k = recurrent_kernel<Tact, Tout, Ts, 64>;
             if (p.CS > 8) cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             return cudaLaunchKernelEx(&cfg, k, p);
         }
         default: {
-            auto k = recurrent_kernel<Tact, Tout, 128>;
+            auto k = recurrent_kernel<Tact, Tout, Ts, 128>;
             if (p.CS > 8) cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             return cudaLaunchKernelEx(&cfg, k, p);
         }
@@ -352,16 +353,16 @@ cudaError_t launch_rec_t(const RecParams& p, int rpc, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_recurrent(const RecParams& p, int act_dtype, int out_dtype, int rpc, cudaStream_t stream) {
-    if (act_dtype == 1) {
-        return out_dtype == 1 ? launch_rec_t<__nv_bfloat16, __nv_bfloat16>(p, rpc, stream)
-                              : launch_rec_t<__nv_bfloat16, float>(p, rpc, stream);
-    }
-    return out_dtype == 1 ? launch_rec_t<float, __nv_bfloat16>(p, rpc, stream)
-                          : launch_rec_t<float, float>(p, rpc, stream);
+    using bf = __nv_bfloat16;
+    if (p.flags & kFlagStateBf16)   // bf16 activations only (checked by the API)
+        return out_dtype == 1 ? launch_rec_t<bf, bf, bf>(p, rpc, stream) : launch_rec_t<bf, float, bf>(p, rpc, stream);
+    if (act_dtype == 1)
+        return out_dtype == 1 ? launch_rec_t<bf, bf, float>(p, rpc, stream) : launch_rec_t<bf, float, float>(p, rpc, stream);
+    return out_dtype == 1 ? launch_rec_t<float, bf, float>(p, rpc, stream) : launch_rec_t<float, float, float>(p, rpc, stream);
 }
 
 cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream) {
-    const size_t per = p.ring_cur ? p.conv_bytes / 16 : p.S_elems / 4;   // a ring moves the conv rows only
+    const size_t per = (p.ring_cur ? p.conv_bytes : p.S_bytes) / 16;   // a ring moves the conv rows only
     unsigned bx = static_cast<unsigned>((per + 255) / 256);
     if (bx > 64) bx = 64;
     if (bx < 1) bx = 1;

@@ -53,30 +53,31 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
                  : "memory");
 }
 
-// Byte layout of one stage (es = activation element size).
+// Byte layout of one stage (es = activation element size, ss = state element
+// size): the state tile first, then the small inputs.
 struct StageLayout {
     uint32_t cw, xr, zr, bytes;   // conv taps (q|k|v), raw rows [K+3][q|k|v], z rows [K]
-    __host__ __device__ StageLayout(int K, int es) {
-        cw = 65536;
+    __host__ __device__ StageLayout(int K, int es, int ss) {
+        cw = kD * kD * ss;
         xr = cw + 384 * 16;
         zr = xr + (K + 3) * 384 * es;
         bytes = zr + K * 128 * es;
     }
 };
 
-template <typename Tact, typename Tout>
+template <typename Tact, typename Tout, typename Ts>
 __global__ void __launch_bounds__(kLaunchThreads, 1)
 recurrent_stream_kernel(const RecParams p) {
     extern __shared__ __align__(128) uint8_t sm[];
-    constexpr int es = sizeof(Tact);
+    constexpr int es = sizeof(Tact), ss = sizeof(Ts);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = p.K, C = p.C, HvD = p.Hv * kD;
     const int r = p.Hv / p.Hk;
     const int n_groups = p.B * p.Hk;
-    const StageLayout L(K, es);
+    const StageLayout L(K, es, ss);
     // private copy of the current item's small inputs, after the stages
     uint8_t* cur = sm + kStages * L.bytes;
-    const uint32_t cur_bytes = L.bytes - 65536;
+    const uint32_t cur_bytes = L.bytes - L.cw;
     float* qk_s = reinterpret_cast<float*>(cur + ((cur_bytes + 15) & ~15u));   // [K][256] q_hat | k_hat
     float* v_s = qk_s + K * 256;                                                  // [K][128]
     float* o_s = v_s + K * 128;                                                   // [128]
@@ -109,8 +110,8 @@ recurrent_stream_kernel(const RecParams p) {
         const uint32_t base = tc::smem_u32(sm + (i % kStages) * L.bytes);
         const uint32_t seg = 128 * es;   // one head's channels of one row
         mbar_expect_tx(mb, L.bytes);
-        const float* Sh = rec_state_in(p, b) + static_cast<size_t>(h) * kD * kD;
-        for (int q = 0; q < 4; ++q) bulk_g2s(base + q * 16384, Sh + q * 4096, 16384, mb);
+        const Ts* Sh = rec_state_in<Ts>(p, b) + static_cast<size_t>(h) * kD * kD;
+        for (int q = 0; q < 4; ++q) bulk_g2s(base + q * 4096 * ss, Sh + q * 4096, 4096 * ss, mb);
         bulk_g2s(base + L.cw, p.conv_w + 4 * (kh * kD), 128 * 16, mb);
         bulk_g2s(base + L.cw + 128 * 16, p.conv_w + 4 * (p.Hk * kD + kh * kD), 128 * 16, mb);
         bulk_g2s(base + L.cw + 256 * 16, p.conv_w + 4 * (2 * p.Hk * kD + h * kD), 128 * 16, mb);
@@ -160,9 +161,9 @@ recurrent_stream_kernel(const RecParams p) {
         // state rows -> registers; small inputs -> private area
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr)
-            sreg[rr] = *reinterpret_cast<const float4*>(stg + (warp * 16 + rr) * 512 + 16 * lane);
+            sreg[rr] = StateIO<Ts>::ld(stg + ((warp * 16 + rr) * kD + 4 * lane) * ss);
         for (uint32_t e = tid * 16; e < cur_bytes; e += kSThreads * 16)
-            *reinterpret_cast<uint4*>(cur + e) = *reinterpret_cast<const uint4*>(stg + 65536 + e);
+            *reinterpret_cast<uint4*>(cur + e) = *reinterpret_cast<const uint4*>(stg + L.cw + e);
         if (tid < K) {
             gates[2 * tid] = sigmoidf_(b_raw);
             gates[2 * tid + 1] = a_ssm * softplusf_(a_raw + a_dt);
@@ -171,10 +172,20 @@ recurrent_stream_kernel(const RecParams p) {
         if (tid == 0) tc::mbar_arrive(&empty[i % kStages]);   // the stage may be refilled
 
         const float4* cw = reinterpret_cast<const float4*>(cur);                      // [384] taps
-        const Tact* xr = reinterpret_cast<const Tact*>(cur + (L.xr - 65536));          // [K+3][384]
-        const Tact* zr = reinterpret_cast<const Tact*>(cur + (L.zr - 65536));          // [K][128]
-        // ---- steps 1-4 for every token of the item: thread c < 256 owns q/k channel c, c < 128 v channel c
-        {
+        const Tact* xr = reinterpret_cast<const Tact*>(cur + (L.xr - L.cw));           // [K+3][384]
+        const Tact* zr = reinterpret_cast<const Tact*>(cur + (L.zr - L.cw));           // [K][128]
+        // ---- steps 1-4 for every token of the item: thread c < 256 owns q/k channel c, c < 128 v channel c.
+        // q_hat and k_hat belong to the group: the group's first head computes them, the others reuse them.
+        if (m > 0) {
+            if (tid < kD) {
+                const float4 wv = cw[256 + tid];
+                for (int t = 0; t < K; ++t)
+                    v_s[t * kD + tid] =
+                        siluf_(conv4(wv, to_f(xr[t * 384 + 256 + tid]), to_f(xr[(t + 1) * 384 + 256 + tid]),
+                                     to_f(xr[(t + 2) * 384 + 256 + tid]), to_f(xr[(t + 3) * 384 + 256 + tid])));
+            }
+            compute_sync();
+        } else {
             const float4 w = cw[tid];
             const float4 wv = tid < kD ? cw[256 + tid] : make_float4(0, 0, 0, 0);
             for (int t = 0; t < K; ++t) {
@@ -202,8 +213,7 @@ recurrent_stream_kernel(const RecParams p) {
             const float kq = warp_sum(fmaf(kk.w, qq.w, fmaf(kk.z, qq.z, fmaf(kk.y, qq.y, kk.x * qq.x))));
             const float beta = gates[2 * t];
             const float eg = expf(gates[2 * t + 1]);
-            float* Sout = rec_state_out(p, b, t) +
-                          (static_cast<size_t>(h) * kD + warp * 16) * kD;
+            Ts* Sout = rec_state_out<Ts>(p, b, t) + (static_cast<size_t>(h) * kD + warp * 16) * kD;
             // partial S.k and S.q of my 16 rows: slot 2rr = row rr . k, slot 2rr+1 = row rr . q
             float pv[32];
 #pragma unroll
@@ -229,8 +239,9 @@ recurrent_stream_kernel(const RecParams p) {
                 nv.y = fmaf(d, kk.y, eg * sv.y);
                 nv.z = fmaf(d, kk.z, eg * sv.z);
                 nv.w = fmaf(d, kk.w, eg * sv.w);
+                nv = StateIO<Ts>::round(nv);   // the next token continues from what a later call reads
                 sreg[rr] = nv;
-                st_f4(Sout + rr * kD + 4 * lane, nv);
+                StateIO<Ts>::st(Sout + rr * kD + 4 * lane, nv);
                 if (status && (nonfinite_bits(nv.x) | nonfinite_bits(nv.y) | nonfinite_bits(nv.z) | nonfinite_bits(nv.w)))
                     atomicOr(status, 1);
             }
@@ -273,26 +284,29 @@ recurrent_stream_kernel(const RecParams p) {
 
 }  // namespace
 
-size_t recurrent_stream_smem(int K, int act_dtype) {
+size_t recurrent_stream_smem(int K, int act_dtype, bool state_bf16) {
     const int es = act_dtype == 1 ? 2 : 4;
-    const StageLayout L(K, es);
-    const size_t cur = ((L.bytes - 65536 + 15) & ~static_cast<size_t>(15));
+    const StageLayout L(K, es, state_bf16 ? 2 : 4);
+    const size_t cur = ((L.bytes - L.cw + 15) & ~static_cast<size_t>(15));
     const size_t misc = (static_cast<size_t>(K) * 384 + 128 + 16 + 8 + 2 * kMaxK + 128) * 4 + 2 * kStages * 8;
     return kStages * static_cast<size_t>(L.bytes) + cur + misc;
 }
 
 cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_dtype, int grid, cudaStream_t stream) {
-    const size_t smem = recurrent_stream_smem(p.K, act_dtype);
+    const bool sbf = (p.flags & kFlagStateBf16) != 0;
+    const size_t smem = recurrent_stream_smem(p.K, act_dtype, sbf);
     auto go = [&](auto kernel) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         kernel<<<grid, kLaunchThreads, smem, stream>>>(p);
         return cudaGetLastError();
     };
+    using bf = __nv_bfloat16;
+    if (sbf)   // bf16 activations only (checked by the API)
+        return out_dtype == 1 ? go(recurrent_stream_kernel<bf, bf, bf>) : go(recurrent_stream_kernel<bf, float, bf>);
     if (act_dtype == 1)
-        return out_dtype == 1 ? go(recurrent_stream_kernel<__nv_bfloat16, __nv_bfloat16>)
-                              : go(recurrent_stream_kernel<__nv_bfloat16, float>);
-    return out_dtype == 1 ? go(recurrent_stream_kernel<float, __nv_bfloat16>) : go(recurrent_stream_kernel<float, float>);
+        return out_dtype == 1 ? go(recurrent_stream_kernel<bf, bf, float>) : go(recurrent_stream_kernel<bf, float, float>);
+    return out_dtype == 1 ? go(recurrent_stream_kernel<float, bf, float>) : go(recurrent_stream_kernel<float, float, float>);
 }
 
 }  // namespace gdn

@@ -44,8 +44,11 @@
  *       z, out      [T][H_v*128]          act dtype / out dtype
  *       a_raw,b_raw [T][H_v]              act dtype
  *       conv_state  [N][3][C]             act dtype (raw rows, oldest first)
- *       S           [N][H_v][128][128]    fp32, S[j][i]: j the v-row, i the
- *                                         k-index; "S.k" = sum_i S[j][i] k_i
+ *       S           [N][H_v][128][128]    fp32 (bf16 under GDN_FLAG_STATE_BF16),
+ *                                         S[j][i]: j the v-row, i the k-index;
+ *                                         "S.k" = sum_i S[j][i] k_i
+ *     Every state argument (S, S_ckpt, S_ring) has the element type the
+ *     flags select; the arithmetic is fp32 either way.
  *       conv_w      [C][4] fp32; dt_bias, ssm_a [H_v] fp32; norm_w [128] fp32
  *   - prenorm_out (optional, may be NULL) receives o before the gated norm,
  *     fp32 with out's layout.
@@ -89,6 +92,14 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
  * kernel instead of the tensor-core kernel (fp32 products end to end; slower).
  * fp32 activations always take that kernel. */
 #define GDN_FLAG_PREFILL_FP32 2u
+/* Recurrent state stored as bf16 instead of fp32 (the SGLang deployment on
+ * the home-server page pins bf16 mamba-state pools).  Every call reads the
+ * state into fp32, computes in fp32 exactly as with an fp32 state, and rounds
+ * to nearest-even only when it stores a state: a decode step, each verify
+ * checkpoint and the end of a prefill round once.  Halves the state bytes of
+ * the recurrent calls.  Requires act_dtype = GDN_BF16 (else
+ * GDN_E_UNSUPPORTED). */
+#define GDN_FLAG_STATE_BF16 4u
 
 typedef struct {
     int32_t H_k;        /* q/k heads (16 in both model sizes on the page)       */
@@ -133,7 +144,7 @@ gdn_status gdn_conv_state_init(const gdn_dims* dims, int32_t n_seq, void* conv_s
  */
 gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, int32_t B,
                            const void* x, const void* z, const void* a_raw, const void* b_raw,
-                           void* conv_state, float* S, void* out, float* prenorm_out,
+                           void* conv_state, void* S, void* out, float* prenorm_out,
                            int32_t* dev_status, gdn_stream_t stream);
 
 /*
@@ -150,7 +161,7 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, int32_t B
  */
 gdn_status gdn_verify_k(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t K,
                         const void* x, const void* z, const void* a_raw, const void* b_raw,
-                        const void* conv_state, const float* S, void* conv_ckpt, float* S_ckpt,
+                        const void* conv_state, const void* S, void* conv_ckpt, void* S_ckpt,
                         void* out, float* prenorm_out, int32_t* dev_status, gdn_stream_t stream);
 
 /*
@@ -160,7 +171,7 @@ gdn_status gdn_verify_k(const gdn_dims* dims, const gdn_weights* w, int32_t B, i
  *   range leaves the sequence's state untouched.
  */
 gdn_status gdn_commit(const gdn_dims* dims, int32_t B, int32_t K, const int32_t* accept_len,
-                      const void* conv_ckpt, const float* S_ckpt, void* conv_state, float* S,
+                      const void* conv_ckpt, const void* S_ckpt, void* conv_state, void* S,
                       gdn_stream_t stream);
 
 /*
@@ -182,7 +193,7 @@ gdn_status gdn_commit(const gdn_dims* dims, int32_t B, int32_t K, const int32_t*
  */
 gdn_status gdn_verify_k_ring(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t K, int32_t R,
                              const void* x, const void* z, const void* a_raw, const void* b_raw,
-                             const void* conv_state, float* S_ring, const int32_t* ring_cur, void* conv_ckpt,
+                             const void* conv_state, void* S_ring, const int32_t* ring_cur, void* conv_ckpt,
                              void* out, float* prenorm_out, int32_t* dev_status, gdn_stream_t stream);
 
 /*
@@ -201,7 +212,7 @@ gdn_status gdn_commit_ring(const gdn_dims* dims, int32_t B, int32_t K, int32_t R
  * gdn_decode_step on that state.
  */
 gdn_status gdn_decode_step_ring(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t R, const void* x,
-                                const void* z, const void* a_raw, const void* b_raw, void* conv_state, float* S_ring,
+                                const void* z, const void* a_raw, const void* b_raw, void* conv_state, void* S_ring,
                                 const int32_t* ring_cur, void* out, float* prenorm_out, int32_t* dev_status,
                                 gdn_stream_t stream);
 
@@ -234,7 +245,7 @@ gdn_status gdn_state_faults(const gdn_dims* dims, int32_t N, const int32_t* dev_
  * and sequences are not touched.  R = 0 with ring_cur NULL for a plain
  * S [N][H_v][128][128]; anything else is GDN_E_INVALID_ARG.
  */
-gdn_status gdn_state_reset(const gdn_dims* dims, int32_t N, int32_t R, float* S, const int32_t* ring_cur,
+gdn_status gdn_state_reset(const gdn_dims* dims, int32_t N, int32_t R, void* S, const int32_t* ring_cur,
                            void* conv_state, int32_t* dev_status, gdn_stream_t stream);
 
 /*
@@ -261,7 +272,7 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t n_seq, int64_t 
 gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, int32_t n_seq,
                                const int32_t* cu_seqlens_host, const int32_t* cu_seqlens_dev,
                                const void* x, const void* z, const void* a_raw, const void* b_raw,
-                               void* conv_state, float* S, int32_t zero_init, void* out,
+                               void* conv_state, void* S, int32_t zero_init, void* out,
                                float* prenorm_out, void* workspace, size_t workspace_bytes,
                                int32_t* dev_status, gdn_stream_t stream);
 
@@ -304,7 +315,7 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, int32
 gdn_status gdn_prefill_chunked_static(const gdn_dims* dims, const gdn_weights* w, int32_t n_seq,
                                       const int32_t* cu_seqlens_host, const int32_t* cu_seqlens_dev,
                                       const void* x, const void* z, const void* a_raw, const void* b_raw,
-                                      void* conv_state, float* S, int32_t zero_init, void* out,
+                                      void* conv_state, void* S, int32_t zero_init, void* out,
                                       float* prenorm_out, int32_t* dev_status, gdn_stream_t stream);
 
 #ifdef __cplusplus

@@ -22,9 +22,9 @@ def weights(case):
     return gdn.make_weights(case.conv_w, case.dt_bias, case.ssm_a, case.norm_w)
 
 
-def dims(case, out_dtype=torch.float32, check_finite=False, prefill_fp32=False):
+def dims(case, out_dtype=torch.float32, check_finite=False, prefill_fp32=False, state_dtype=torch.float32):
     return gdn.make_dims(case.Hk, case.Hv, case.act_dtype, out_dtype, check_finite=check_finite,
-                         prefill_fp32=prefill_fp32)
+                         prefill_fp32=prefill_fp32, state_dtype=state_dtype)
 
 
 def half_ulp_bf16(ref):

@@ -82,7 +82,8 @@ def _decode(d, w, B=4, x=FAKE, **kw):
     (None, 1),
     (_dims(Hk=0), 1), (_dims(Hv=0), 1), (_dims(Hk=16, Hv=40), 1),   # H_v % H_k != 0
     (_dims(eps=0.0), 1), (_dims(eps=float("nan")), 1), (_dims(act=7), 1), (_dims(out=-1), 1),
-    (_dims(flags=0x80), 1), (_dims(flags=4), 1), (_dims(Hk=1, Hv=17), 2),                 # ratio > 16: unsupported
+    (_dims(flags=0x80), 1), (_dims(flags=8), 1), (_dims(Hk=1, Hv=17), 2),                 # ratio > 16: unsupported
+    (_dims(act=0, flags=4), 2),                                                           # bf16 state, fp32 activations
 ])
 def test_decode_rejects_bad_dims(dims, status):
     if dims is None:

@@ -1,0 +1,189 @@
+"""GPU tests of the bf16 state variant (GDN_FLAG_STATE_BF16) against the fp64
+oracle, through the C ABI.
+
+Contract: the kernels read the state into fp32, compute exactly as with an
+fp32 state and round to bf16 (nearest even) only when they store a state.
+The oracle starts from the same bf16 values, so
+  * outputs meet the bars of the bf16-activation path (tests/gpu_util.py);
+  * every stored state element lies within one bf16 rounding of the oracle:
+    |S - S_ref| <= 2^-8 |S_ref| + 1e-5 max|S_ref| (half a bf16 ulp is at
+    most 2^-8 of the value; the second term covers the fp32 arithmetic);
+  * bookkeeping stays bit-exact: a verify walk continues from the rounded
+    state, so its checkpoints equal decode replays, and commit / ring moves
+    are exact.
+The drift over many steps (one rounding per step) is measured in
+test_drift_over_64_steps."""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_decode_gb300 as gdn
+import gdn_inputs
+import oracle
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+BF = torch.bfloat16
+
+
+def assert_one_rounding(S, ref):
+    S = S.float().cpu().numpy().astype(np.float64)
+    ref = np.asarray(ref, dtype=np.float64).reshape(S.shape)
+    err = np.abs(S - ref)
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-5 * np.abs(ref).max()
+    assert np.all(err <= bound), f"worst excess {float((err - bound).max()):.3e}"
+
+
+def _dims(c, out=torch.float32, **kw):
+    return G.dims(c, out, state_dtype=BF, **kw)
+
+
+@pytest.mark.parametrize("B,Hk,Hv", [(64, 16, 32), (3, 2, 4)])
+def test_decode_step(B, Hk, Hv):
+    c = gdn_inputs.make_case("sbf", Hk=Hk, Hv=Hv, B=B, K=1, seed=120 + B)
+    S0 = c.S0.to(BF)
+    d, w = _dims(c), G.weights(c)
+    conv, S = G.dev(c.conv0), G.dev(S0)
+    out = torch.empty(B, c.Hv * 128, device="cuda")
+    gdn.gdn_decode_step(d, w, G.dev(c.x), G.dev(c.z), G.dev(c.a_raw), G.dev(c.b_raw), conv, S, out)
+    torch.cuda.synchronize()
+    ref = oracle.forward(c.Hk, c.Hv, c.x, c.z, c.a_raw, c.b_raw, c.conv_w, c.dt_bias, c.ssm_a, c.norm_w, c.conv0,
+                         S0.float(), cu_seqlens=np.arange(B + 1))
+    G.assert_out_close(out, ref.out, BF)
+    assert S.dtype == BF
+    assert_one_rounding(S, ref.S)
+    assert G.conv_bits_equal(conv, ref.conv_state, BF)
+
+
+@pytest.mark.parametrize("B,Hk,Hv,K", [(64, 16, 32, 3), (3, 2, 4, 4)])
+def test_verify_checkpoints_equal_decode_replays_and_commit(B, Hk, Hv, K):
+    c = gdn_inputs.make_case("sbfv", Hk=Hk, Hv=Hv, B=B, K=K, seed=140 + B)
+    S0 = c.S0.to(BF)
+    d, w = _dims(c), G.weights(c)
+    conv0, S0d = G.dev(c.conv0), G.dev(S0)
+    ck_conv = torch.empty(B, K, 3, c.C, device="cuda", dtype=BF)
+    ck_S = torch.empty(B, K, c.Hv, 128, 128, device="cuda", dtype=BF)
+    out = torch.empty(B * K, c.Hv * 128, device="cuda")
+    gdn.gdn_verify_k(d, w, K, G.dev(c.x), G.dev(c.z), G.dev(c.a_raw), G.dev(c.b_raw), conv0, S0d, ck_conv, ck_S, out)
+    conv, S = conv0.clone(), S0d.clone()
+    xs, zs = c.x.view(B, K, -1), c.z.view(B, K, -1)
+    as_, bs = c.a_raw.view(B, K, -1), c.b_raw.view(B, K, -1)
+    for p in range(K):
+        o = torch.empty(B, c.Hv * 128, device="cuda")
+        gdn.gdn_decode_step(d, w, G.dev(xs[:, p]), G.dev(zs[:, p]), G.dev(as_[:, p]), G.dev(bs[:, p]), conv, S, o)
+        torch.cuda.synchronize()
+        assert torch.equal(ck_S[:, p], S) and torch.equal(ck_conv[:, p], conv)
+        assert torch.equal(out.view(B, K, -1)[:, p], o)
+    # position 0 is one rounding away from the oracle
+    ref = oracle.verify_checkpoints(c.Hk, c.Hv, c.x, c.z, c.a_raw, c.b_raw, c.conv_w, c.dt_bias, c.ssm_a, c.norm_w,
+                                    c.conv0, S0.float(), K)
+    assert_one_rounding(ck_S[:, 0], ref[2][:, 0])
+    acc = torch.randint(1, K + 1, (B,), generator=torch.Generator().manual_seed(B), dtype=torch.int32)
+    conv2, S2 = conv0.clone(), S0d.clone()
+    gdn.gdn_commit(d, K, acc.cuda(), ck_conv, ck_S, conv2, S2)
+    torch.cuda.synchronize()
+    for bb in range(B):
+        n = int(acc[bb])
+        assert torch.equal(S2[bb], ck_S[bb, n - 1]) and torch.equal(conv2[bb], ck_conv[bb, n - 1])
+
+
+def test_ring_equals_copy_path():
+    B, Hk, Hv, K, R, rounds = 64, 16, 32, 3, 4, 3
+    c = gdn_inputs.make_case("sbfr", Hk=Hk, Hv=Hv, B=B, K=rounds * K, seed=160)
+    d, w = _dims(c), G.weights(c)
+    S0 = G.dev(c.S0.to(BF))
+    conv, S = G.dev(c.conv0), S0.clone()
+    conv_r = G.dev(c.conv0)
+    S_ring = torch.zeros(B, R, c.Hv, 128, 128, device="cuda", dtype=BF)
+    S_ring[:, 0] = S0
+    cur = torch.zeros(B, dtype=torch.int32, device="cuda")
+    ck_conv = torch.empty(B, K, 3, c.C, device="cuda", dtype=BF)
+    ck_S = torch.empty(B, K, c.Hv, 128, 128, device="cuda", dtype=BF)
+    out, out_r, ck_conv_r = (torch.empty(B * K, c.Hv * 128, device="cuda"), torch.empty(B * K, c.Hv * 128,
+                             device="cuda"), torch.empty_like(ck_conv))
+    gen = torch.Generator().manual_seed(9)
+    for r in range(rounds):
+        sl = lambda t: G.dev(t.view(B, rounds * K, -1)[:, r * K:(r + 1) * K].reshape(B * K, -1))
+        x, z, a, b = sl(c.x), sl(c.z), sl(c.a_raw), sl(c.b_raw)
+        acc = torch.randint(1, K + 1, (B,), generator=gen, dtype=torch.int32).cuda()
+        gdn.gdn_verify_k(d, w, K, x, z, a, b, conv, S, ck_conv, ck_S, out)
+        gdn.gdn_commit(d, K, acc, ck_conv, ck_S, conv, S)
+        gdn.gdn_verify_k_ring(d, w, K, x, z, a, b, conv_r, S_ring, cur, ck_conv_r, out_r)
+        gdn.gdn_commit_ring(d, K, R, acc, ck_conv_r, conv_r, cur)
+        torch.cuda.synchronize()
+        assert torch.equal(out_r, out) and torch.equal(conv_r, conv)
+        live = S_ring[torch.arange(B, device="cuda"), cur.long()]
+        assert torch.equal(live, S)
+
+
+@pytest.mark.parametrize("prefill_fp32", [False, True])
+def test_prefill(prefill_fp32):
+    """Packed sequences with ragged tails and an empty one, nonzero initial
+    state; the tensor-core path and the fp32 CUDA-core path."""
+    c = gdn_inputs.make_case("sbfp", Hk=2, Hv=4, lengths=[300, 0, 77, 190], seed=180)
+    S0 = c.S0.to(BF)
+    d, w = _dims(c, prefill_fp32=prefill_fp32), G.weights(c)
+    cu = c.cu_seqlens.to(torch.int32)
+    conv, S = G.dev(c.conv0), G.dev(S0)
+    out = torch.empty(c.T, c.Hv * 128, device="cuda")
+    nws = gdn.gdn_prefill_workspace_bytes(d, c.N, c.T)
+    ws = torch.empty(max(nws, 16), device="cuda", dtype=torch.uint8)
+    gdn.gdn_prefill_chunked(d, w, cu, G.dev(cu), G.dev(c.x), G.dev(c.z), G.dev(c.a_raw), G.dev(c.b_raw), conv, S,
+                            out, zero_init=False, workspace=ws)
+    torch.cuda.synchronize()
+    ref = oracle.forward(c.Hk, c.Hv, c.x, c.z, c.a_raw, c.b_raw, c.conv_w, c.dt_bias, c.ssm_a, c.norm_w, c.conv0,
+                         S0.float(), cu_seqlens=c.cu_seqlens.numpy())
+    G.assert_out_close(out, ref.out, BF)
+    assert_one_rounding(S, ref.S)
+    assert G.conv_bits_equal(conv, ref.conv_state, BF)
+
+
+def test_prefill_long_sequence_rounds_once():
+    """65 chunks (where an fp32 state is carried between two launches): the
+    bf16 state is still rounded once, at the end."""
+    c = gdn_inputs.make_case("sbfl", Hk=2, Hv=4, lengths=[65 * 64], seed=181)
+    S0 = c.S0.to(BF)
+    d, w = _dims(c), G.weights(c)
+    cu = c.cu_seqlens.to(torch.int32)
+    conv, S = G.dev(c.conv0), G.dev(S0)
+    out = torch.empty(c.T, c.Hv * 128, device="cuda")
+    ws = torch.empty(gdn.gdn_prefill_workspace_bytes(d, c.N, c.T), device="cuda", dtype=torch.uint8)
+    gdn.gdn_prefill_chunked(d, w, cu, G.dev(cu), G.dev(c.x), G.dev(c.z), G.dev(c.a_raw), G.dev(c.b_raw), conv, S,
+                            out, zero_init=False, workspace=ws)
+    torch.cuda.synchronize()
+    ref = oracle.forward(c.Hk, c.Hv, c.x, c.z, c.a_raw, c.b_raw, c.conv_w, c.dt_bias, c.ssm_a, c.norm_w, c.conv0,
+                         S0.float(), cu_seqlens=c.cu_seqlens.numpy())
+    G.assert_out_close(out, ref.out, BF)
+    assert_one_rounding(S, ref.S)
+
+
+def test_drift_over_64_steps():
+    """64 decode steps from one bf16 state, against the fp64 oracle run as one
+    64-token recurrence: the fp32 state keeps the bf16-activation bars; the
+    bf16 state (one rounding per step) drifts, and the drift stays small."""
+    B, Hk, Hv, n = 4, 16, 32, 64
+    c = gdn_inputs.make_case("drift", Hk=Hk, Hv=Hv, lengths=[n] * B, seed=190)
+    S0 = c.S0.to(BF).float()
+    ref = oracle.forward(c.Hk, c.Hv, c.x, c.z, c.a_raw, c.b_raw, c.conv_w, c.dt_bias, c.ssm_a, c.norm_w, c.conv0,
+                         S0, cu_seqlens=c.cu_seqlens.numpy())
+    yref = ref.out.reshape(B, n, -1)
+    w = G.weights(c)
+    xs, zs = c.x.view(B, n, -1), c.z.view(B, n, -1)
+    as_, bs = c.a_raw.view(B, n, -1), c.b_raw.view(B, n, -1)
+    res = {}
+    for sd in (torch.float32, BF):
+        d = G.dims(c, torch.float32, state_dtype=sd)
+        conv, S = G.dev(c.conv0), G.dev(S0.to(sd))
+        errs = []
+        for t in range(n):
+            o = torch.empty(B, c.Hv * 128, device="cuda")
+            gdn.gdn_decode_step(d, w, G.dev(xs[:, t]), G.dev(zs[:, t]), G.dev(as_[:, t]), G.dev(bs[:, t]), conv, S, o)
+            errs.append(float(np.abs(o.cpu().numpy().astype(np.float64) - yref[:, t]).max()))
+        torch.cuda.synchronize()
+        res[sd] = (max(errs), G.state_rel_fro(S.float(), ref.S))
+    ymax = float(np.abs(yref).max())
+    print(f"\n64-step drift (max|y_ref| {ymax:.3f}): fp32 state max|dy| {res[torch.float32][0]:.3e} state rel "
+          f"{res[torch.float32][1]:.3e}; bf16 state max|dy| {res[BF][0]:.3e} state rel {res[BF][1]:.3e}")
+    assert res[torch.float32][0] <= 2e-3 and res[torch.float32][1] <= 1e-3
+    # measured on GB300: 5.9e-2 (0.3% of max|y_ref| = 18.7) and 3.3e-3; the bounds leave room for other seeds
+    assert res[BF][0] <= 1e-2 * ymax and res[BF][1] <= 1e-2
