@@ -81,13 +81,20 @@ def prefill_flops(T, Hv):
     return per * T * Hv
 
 
-def kernel_sources_hash() -> str:
-    """sha256 over the library's kernel sources and public header (sorted by name)."""
+# The sources that decide each part's kernels, launch shapes and memory traffic.
+_COMMON_SOURCES = ("gdn_api.cu", "gdn_common.cuh", "gdn_internal.h", "gdn_tc.cuh")
+PART_SOURCES = {
+    "prefill": _COMMON_SOURCES + ("gdn_prefill_prep.cu", "gdn_prefill_state.cu", "gdn_prefill_simt.cu",
+                                  "gdn_prefill_tc.cuh"),
+    "decode": _COMMON_SOURCES + ("gdn_recurrent.cu", "gdn_recurrent_stream.cu"),
+}
+
+
+def kernel_sources_hash(part: str) -> str:
+    """sha256 over the sources of one part (PART_SOURCES, in that order) and the public header."""
     import hashlib
-    root = os.path.dirname(os.path.abspath(__file__))
-    csrc = os.path.join(root, "gated_deltanet_linear_decode_gb300", "csrc")
-    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
-    files.append(os.path.join(root, "include", "gdn.h"))
+    csrc = os.path.join(ROOT, "gated_deltanet_linear_decode_gb300", "csrc")
+    files = [os.path.join(csrc, f) for f in PART_SOURCES[part]] + [os.path.join(ROOT, "include", "gdn.h")]
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.basename(f).encode())
@@ -98,16 +105,15 @@ def kernel_sources_hash() -> str:
 
 def measured_traffic() -> dict:
     """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum) recorded in
-    profiles/traffic.json, or {} when the kernel sources changed since they were taken."""
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "traffic.json")
+    profiles/traffic.json, for each part whose sources are unchanged since they were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return {}
-    if rec.get("kernel_sources_sha256") != kernel_sources_hash():
-        return {}
-    return {k: v["bytes"] for k, v in rec.get("parts", {}).items()}
+    return {k: v["bytes"] for k, v in rec.get("parts", {}).items()
+            if k in PART_SOURCES and v.get("sources_sha256") == kernel_sources_hash(k)}
 
 
 def peaks():
@@ -406,10 +412,11 @@ def run_extras(dev, warmup, reps):
     """The two other timed configurations, outside the step: decode at batch 1
     (1000 in-place steps captured in one CUDA graph; the 4.5 MB working set
     stays in L2, so its bandwidth is not an HBM figure) and the packed varlen
-    prefill (8 sequences, T=65536, nonzero initial state, L2 flushed); and the
-    B=64 decode with a bf16 state (L2 flushed)."""
+    prefill (8 sequences, T=65536, nonzero initial state, L2 flushed); the
+    B=64 decode with a bf16 state; and the projections either side of the
+    mixer at the prefill and decode sizes (L2 flushed)."""
     import gated_deltanet_linear_decode_gb300 as gdn
-    hbm, _, _ = peaks()
+    hbm, tf, _ = peaks()
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
     out = {}
@@ -470,6 +477,35 @@ def run_extras(dev, warmup, reps):
                                                  "unit": "GB/s", "frac": bb / (bm / 1e3) / 1e9 / hbm,
                                                  "algorithmic_bytes": bb}}
     del S, conv
+
+    # the projections either side of the mixer (cuBLASLt GEMMs): 27B dims over the T=8192 prefill
+    # (tensor-bound) and 35B dims over the B=64 decode batch (bound by reading the weights)
+    ws = torch.empty(32 << 20, device=dev, dtype=torch.uint8)
+    for name, T, H, Hk, Hv in (("proj_in_out_T8192_H5120", 8192, 5120, 16, 48),
+                               ("proj_in_out_B64_H2048", 64, 2048, 16, 32)):
+        c = gdn_inputs.make_proj_case(T=T, H=H, Hk=Hk, Hv=Hv, seed=7)
+        d = gdn.make_dims(Hk, Hv, torch.bfloat16, torch.bfloat16)
+        C, HvD = 128 * (2 * Hk + Hv), 128 * Hv
+        t = {k: getattr(c, k).to(dev) for k in ("hidden", "W_qkv", "W_z", "W_a", "W_b", "y", "W_out")}
+        bf = dict(device=dev, dtype=torch.bfloat16)
+        x, z = torch.empty(T, C, **bf), torch.empty(T, HvD, **bf)
+        a, b, po = torch.empty(T, Hv, **bf), torch.empty(T, Hv, **bf), torch.empty(T, H, **bf)
+
+        def proj():
+            gdn.gdn_in_proj(d, t["hidden"], t["W_qkv"], t["W_z"], t["W_a"], t["W_b"], x, z, a, b, workspace=ws)
+            gdn.gdn_out_proj(d, t["y"], t["W_out"], po, workspace=ws)
+
+        pm = timed(proj, True)
+        flops = 2.0 * T * H * (C + HvD + 2 * Hv) + 2.0 * T * HvD * H
+        wbytes = 2 * H * (C + HvD + 2 * Hv) + 2 * H * HvD
+        abytes = 2 * T * (H + C + HvD + 2 * Hv) + 2 * T * (HvD + H)
+        out[name] = {"ms": pm, "launches": 5, "tflops": flops / (pm / 1e3) / 1e12,
+                     "frac_of_bf16_peak": flops / (pm / 1e3) / 1e12 / tf,
+                     "GBps": (wbytes + abytes) / (pm / 1e3) / 1e9,
+                     "frac_of_hbm_peak": (wbytes + abytes) / (pm / 1e3) / 1e9 / hbm,
+                     "flops": flops, "bytes": wbytes + abytes}
+        del t, x, z, a, b, po
+    del ws
 
     # packed varlen prefill, 8 sequences, T=65536
     c = gdn_inputs.varlen_t65536()

@@ -25,7 +25,8 @@ __all__ = [
     "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step",
     "gdn_verify_k", "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked",
     "gdn_prefill_chunked_static", "gdn_verify_k_ring", "gdn_commit_ring", "gdn_decode_step_ring",
-    "gdn_state_faults", "gdn_state_reset", "PREFILL_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "HEAD_DIM",
+    "gdn_state_faults", "gdn_state_reset", "GdnInProjWeights", "gdn_in_proj", "gdn_out_proj",
+    "PREFILL_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "HEAD_DIM",
 ]
 
 HEAD_DIM = 128
@@ -39,7 +40,7 @@ EXPORTED_SYMBOLS = (
     "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step",
     "gdn_verify_k", "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked",
     "gdn_prefill_chunked_static", "gdn_verify_k_ring", "gdn_commit_ring", "gdn_decode_step_ring",
-    "gdn_state_faults", "gdn_state_reset",
+    "gdn_state_faults", "gdn_state_reset", "gdn_in_proj", "gdn_out_proj",
 )
 
 
@@ -57,6 +58,11 @@ class GdnDims(ctypes.Structure):
 class GdnWeights(ctypes.Structure):
     _fields_ = [("conv_w", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p), ("ssm_a", ctypes.c_void_p),
                 ("norm_w", ctypes.c_void_p)]
+
+
+class GdnInProjWeights(ctypes.Structure):
+    _fields_ = [("W_qkv", ctypes.c_void_p), ("W_z", ctypes.c_void_p), ("W_a", ctypes.c_void_p),
+                ("W_b", ctypes.c_void_p)]
 
 
 _lib = None
@@ -90,6 +96,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         "gdn_decode_step_ring": (ctypes.c_int, [D, W, I32, I32, P, P, P, P, P, P, P, P, P, P, P]),
         "gdn_state_faults": (ctypes.c_int, [D, I32, P, I32, P, P]),
         "gdn_state_reset": (ctypes.c_int, [D, I32, I32, P, P, P, P, P]),
+        "gdn_in_proj": (ctypes.c_int, [D, I32, I32, P, ctypes.POINTER(GdnInProjWeights), P, P, P, P, P, SZ, P]),
+        "gdn_out_proj": (ctypes.c_int, [D, I32, I32, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -316,6 +324,36 @@ def gdn_state_reset(dims: GdnDims, S, dev_status, conv_state=None, ring_cur=None
     _need(conv_state, _act(dims), (N, 3, HEAD_DIM * (2 * dims.H_k + dims.H_v)), optional=True)
     _check("gdn_state_reset", library().gdn_state_reset(
         ctypes.byref(dims), N, R, _ptr(S), _ptr(ring_cur), _ptr(conv_state), _ptr(dev_status), _stream(stream)))
+
+
+def gdn_in_proj(dims: GdnDims, hidden, W_qkv, W_z, W_a, W_b, x, z, a_raw, b_raw, workspace=None,
+                stream=None) -> None:
+    """attn_qkv / attn_gate / ssm_alpha / ssm_beta: hidden [T][H] bf16 -> x, z, a_raw, b_raw (bf16);
+    weights in the [out][in] layout (cuBLASLt GEMMs, fp32 accumulation)."""
+    T, H = hidden.shape
+    C, HvD = HEAD_DIM * (2 * dims.H_k + dims.H_v), dims.H_v * HEAD_DIM
+    bf = torch.bfloat16
+    _need(hidden, bf, (T, H)); _need(W_qkv, bf, (C, H)); _need(W_z, bf, (HvD, H))
+    _need(W_a, bf, (dims.H_v, H)); _need(W_b, bf, (dims.H_v, H))
+    _need(x, bf, (T, C)); _need(z, bf, (T, HvD)); _need(a_raw, bf, (T, dims.H_v)); _need(b_raw, bf, (T, dims.H_v))
+    _need(workspace, None, None, optional=True)
+    w = GdnInProjWeights(_ptr(W_qkv), _ptr(W_z), _ptr(W_a), _ptr(W_b))
+    nws = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("gdn_in_proj", library().gdn_in_proj(ctypes.byref(dims), T, H, _ptr(hidden), ctypes.byref(w), _ptr(x),
+                                                _ptr(z), _ptr(a_raw), _ptr(b_raw), _ptr(workspace), nws,
+                                                _stream(stream)))
+
+
+def gdn_out_proj(dims: GdnDims, y, W_out, out, workspace=None, stream=None) -> None:
+    """ssm_out: y [T][H_v*128] bf16 -> out [T][H] bf16, W_out [H][H_v*128]."""
+    T, HvD = y.shape
+    H = out.shape[1]
+    bf = torch.bfloat16
+    _need(y, bf, (T, dims.H_v * HEAD_DIM)); _need(W_out, bf, (H, HvD)); _need(out, bf, (T, H))
+    _need(workspace, None, None, optional=True)
+    nws = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("gdn_out_proj", library().gdn_out_proj(ctypes.byref(dims), T, H, _ptr(y), _ptr(W_out), _ptr(out),
+                                                  _ptr(workspace), nws, _stream(stream)))
 
 
 def gdn_prefill_workspace_bytes(dims: GdnDims, n_seq: int, T_total: int) -> int:

@@ -174,3 +174,34 @@ NAMED = {
     "decode_b64": decode_b64,
     "varlen_t65536": varlen_t65536,
 }
+
+
+@dataclass
+class ProjCase:
+    """Inputs of the projections either side of the mixer (all bf16, CPU): hidden [T][H],
+    W_qkv [C][H], W_z [Hv*128][H], W_a / W_b [Hv][H], y [T][Hv*128], W_out [H][Hv*128]."""
+    Hk: int
+    Hv: int
+    H: int
+    hidden: torch.Tensor
+    W_qkv: torch.Tensor
+    W_z: torch.Tensor
+    W_a: torch.Tensor
+    W_b: torch.Tensor
+    y: torch.Tensor
+    W_out: torch.Tensor
+
+
+def make_proj_case(*, T: int, H: int, Hk: int, Hv: int, seed: int = 0) -> ProjCase:
+    """hidden, y ~ N(0, 1); every weight ~ N(0, 1/sqrt(fan_in)).  Hidden sizes on the page:
+    5120 (27B, 16/48) and 2048 (35B-A3B, 16/32).  Draw order: hidden, W_qkv, W_z, W_a, W_b,
+    y, W_out."""
+    gen = torch.Generator().manual_seed(seed)
+    C, HvD = D * (2 * Hk + Hv), D * Hv
+    rn = lambda *s, std=1.0: (torch.randn(*s, generator=gen) * std).to(torch.bfloat16)
+    hidden = rn(T, H)
+    W_qkv, W_z = rn(C, H, std=H ** -0.5), rn(HvD, H, std=H ** -0.5)
+    W_a, W_b = rn(Hv, H, std=H ** -0.5), rn(Hv, H, std=H ** -0.5)
+    y = rn(T, HvD)
+    W_out = rn(H, HvD, std=HvD ** -0.5)
+    return ProjCase(Hk, Hv, H, hidden, W_qkv, W_z, W_a, W_b, y, W_out)

@@ -275,3 +275,20 @@ def chunk_forward(Hk, Hv, x, z, a_raw, b_raw, conv_w, dt_bias, ssm_a, norm_w,
         xx = np.concatenate([cst[s], _f32(x[t0:t1])], axis=0)
         cst[s] = xx[-3:]
     return Result(out, pre, St, cst, None)
+
+
+def in_proj(hidden, W_qkv, W_z, W_a, W_b):
+    """The projections in front of the mixer, fp64: the xwen CLAUDE.md page, "Architecture
+    cheat sheet", "Gated DeltaNet layer" -- the layer input through attn_qkv (the fused q|k|v
+    stream x), attn_gate (z), ssm_alpha (a_raw) and ssm_beta (b_raw).  Each weight is in the
+    [out][in] layout of a linear layer, so a projection is hidden . W^T (a library matmul, the
+    only step).  Returns (x, z, a_raw, b_raw).  Pinned by tests/test_oracle_pins.py (identity
+    and selector weights, brute-force sums on tiny inputs)."""
+    h = _f64(hidden)
+    return tuple(h @ _f64(W).T for W in (W_qkv, W_z, W_a, W_b))
+
+
+def out_proj(y, W_out):
+    """ssm_out after the gated RMSNorm (same page and paragraph): y . W_out^T in fp64.
+    Pinned with in_proj."""
+    return _f64(y) @ _f64(W_out).T

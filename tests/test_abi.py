@@ -1,5 +1,5 @@
 """The C-ABI library builds, loads and exports every entry point that
-include/gdn.h declares, and its host-side validation rejects bad arguments
+include/gdn.h and include/gdn_proj.h declare, and its host-side validation rejects bad arguments
 before anything reaches a device (CPU only: no call here launches a kernel)."""
 import ctypes
 import os
@@ -12,10 +12,11 @@ import gated_deltanet_linear_decode_gb300 as gdn
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gdn.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in ("gdn.h", "gdn_proj.h")]
 
 
 def declared_functions():
-    src = open(HEADER).read()
+    src = "".join(open(h).read() for h in HEADERS)
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", src)))
 
@@ -41,7 +42,8 @@ def test_library_exports_every_declared_symbol():
 
 def test_header_compiles_as_c():
     """The header is plain C (no CUDA or C++ types needed)."""
-    src = '#include "gdn.h"\nint main(void){ gdn_dims d; (void)d; return (int)GDN_OK; }\n'
+    src = ('#include "gdn.h"\n#include "gdn_proj.h"\n'
+           'int main(void){ gdn_dims d; gdn_in_proj_weights w; (void)d; (void)w; return (int)GDN_OK; }\n')
     r = subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.dirname(HEADER),
                         "-x", "c", "-"], input=src, text=True, capture_output=True)
     assert r.returncode == 0, r.stderr
@@ -167,6 +169,30 @@ def test_guard_validation():
     assert L.gdn_state_reset(ctypes.byref(d), 0, 0, a, None, None, b, None) == 0     # no-op
     assert L.gdn_state_reset(ctypes.byref(d), 2, 0, a, None, None, a + 64, None) == 1   # status inside S
     assert L.gdn_state_reset(ctypes.byref(d), 2, 0, None, None, None, b, None) == 1
+
+
+def test_projection_validation():
+    L = gdn.library()
+    d = _dims()                                    # bf16 activations, fp32 out
+    d_bf = _dims(out=1)
+    w = gdn.GdnInProjWeights(FAKE * 0x100, FAKE * 0x200, FAKE * 0x300, FAKE * 0x400)
+    outs = [FAKE * 0x500, FAKE * 0x600, FAKE * 0x700, FAKE * 0x800]
+    call = lambda dims, T, H, hid, ww, o=outs, ws=None, nws=0: L.gdn_in_proj(
+        ctypes.byref(dims), T, H, hid, ctypes.byref(ww) if ww is not None else None, *o, ws, nws, None)
+    assert call(d, 4, 2048, FAKE * 0x900, w) == 2                  # fp32 output type: unsupported
+    assert call(_dims(act=0, out=1), 4, 2048, FAKE * 0x900, w) == 2
+    assert call(d_bf, 0, 2048, FAKE * 0x900, w) == 0                # T = 0: no-op
+    assert call(d_bf, -1, 2048, FAKE * 0x900, w) == 1
+    assert call(d_bf, 4, 2047, FAKE * 0x900, w) == 1                # H not a multiple of 8
+    assert call(d_bf, 4, 2048, None, w) == 1
+    assert call(d_bf, 4, 2048, FAKE * 0x900, None) == 1
+    assert call(d_bf, 4, 2048, FAKE * 0x900 + 8, w) == 3
+    assert call(d_bf, 4, 2048, FAKE * 0x900, w, ws=None, nws=64) == 1   # workspace size without a workspace
+    assert call(d_bf, 4, 2048, outs[0], w) == 1                     # hidden overlaps x
+    assert L.gdn_out_proj(ctypes.byref(d_bf), 4, 2048, FAKE * 0x100, FAKE * 0x200, FAKE * 0x100, None, 0, None) == 1
+    assert L.gdn_out_proj(ctypes.byref(d_bf), 4, 2048, FAKE * 0x100, FAKE * 0x200, FAKE * 0x300 + 4, None, 0,
+                          None) == 3
+    assert L.gdn_out_proj(ctypes.byref(d), 4, 2048, FAKE * 0x100, FAKE * 0x200, FAKE * 0x300, None, 0, None) == 2
 
 
 def test_prefill_validation():
