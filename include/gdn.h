@@ -95,9 +95,10 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 /* Recurrent state stored as bf16 instead of fp32 (the SGLang deployment on
  * the home-server page pins bf16 mamba-state pools).  Every call reads the
  * state into fp32, computes in fp32 exactly as with an fp32 state, and rounds
- * to nearest-even only when it stores a state: a decode step, each verify
- * checkpoint and the end of a prefill round once.  Halves the state bytes of
- * the recurrent calls.  Requires act_dtype = GDN_BF16 (else
+ * to nearest-even only when it stores a state: after a decode step, at each
+ * verify checkpoint (the walk goes on from the rounded value, so checkpoints
+ * still equal decode replays bit for bit) and once at the end of a prefill.
+ * Halves the state bytes of the recurrent calls.  Requires act_dtype = GDN_BF16 (else
  * GDN_E_UNSUPPORTED). */
 #define GDN_FLAG_STATE_BF16 4u
 
@@ -180,7 +181,8 @@ gdn_status gdn_commit(const gdn_dims* dims, int32_t B, int32_t K, const int32_t*
  * roll back (the page's "Drafting" section; the NEXTN.md page's "GDN
  * rollback"); gdn_verify_k + gdn_commit copy the accepted plane back into S.
  * With a ring the accepted plane becomes the live state where it lies.
- *   S_ring   [B][R][H_v][128][128] fp32: R state slots per sequence
+ *   S_ring   [B][R][H_v][128][128] fp32 (bf16 under GDN_FLAG_STATE_BF16): R
+ *            state slots per sequence
  *   ring_cur [B] int32 on the device: the live slot of each sequence, in 0..R-1
  * A caller starts from slot 0 holding the state (e.g. after a prefill into it)
  * and ring_cur all zero.
