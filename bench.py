@@ -435,6 +435,21 @@ def run_extras(dev, warmup, reps):
                 ms.append(e0.elapsed_time(e1))
         return statistics.mean(ms)
 
+    def timed_graph(fn):
+        """fn captured once in a CUDA graph, its replays timed: device time without the host's
+        launch overhead (which is longer than these calls' device work)."""
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            fn()
+        torch.cuda.synchronize()
+        return timed(g.replay, True)
+
     # decode B=1, 1000 steps per graph replay
     c = gdn_inputs.decode_b1()
     d = gdn.make_dims(c.Hk, c.Hv, torch.bfloat16, torch.bfloat16)
@@ -470,7 +485,7 @@ def run_extras(dev, warmup, reps):
     i = {k: getattr(c, k).to(dev) for k in ("x", "z", "a_raw", "b_raw")}
     conv, S = c.conv0.to(dev), c.S0.to(dev).to(torch.bfloat16)
     o = torch.empty(c.N, c.Hv * 128, device=dev, dtype=torch.bfloat16)
-    bm = timed(lambda: gdn.gdn_decode_step(d, w, i["x"], i["z"], i["a_raw"], i["b_raw"], conv, S, o), True)
+    bm = timed_graph(lambda: gdn.gdn_decode_step(d, w, i["x"], i["z"], i["a_raw"], i["b_raw"], conv, S, o))
     bb = decode_bytes(c.N, c.Hk, c.Hv, state_bytes=2)
     out["decode_B64_state_bf16"] = {"tokens_per_s": c.N / (bm / 1e3), "us": 1e3 * bm,
                                     "roofline": {"bound": "hbm", "achieved": bb / (bm / 1e3) / 1e9, "peak": hbm,
@@ -495,11 +510,18 @@ def run_extras(dev, warmup, reps):
             gdn.gdn_in_proj(d, t["hidden"], t["W_qkv"], t["W_z"], t["W_a"], t["W_b"], x, z, a, b, workspace=ws)
             gdn.gdn_out_proj(d, t["y"], t["W_out"], po, workspace=ws)
 
-        pm = timed(proj, True)
+        pm = timed_graph(proj)
+
+        def torch_linear():   # the same five GEMMs through torch (cuBLAS), for comparison only
+            for W, o in ((t["W_qkv"], x), (t["W_z"], z), (t["W_a"], a), (t["W_b"], b)):
+                torch.matmul(t["hidden"], W.t(), out=o)
+            torch.matmul(t["y"], t["W_out"].t(), out=po)
+
+        cm = timed_graph(torch_linear)
         flops = 2.0 * T * H * (C + HvD + 2 * Hv) + 2.0 * T * HvD * H
         wbytes = 2 * H * (C + HvD + 2 * Hv) + 2 * H * HvD
         abytes = 2 * T * (H + C + HvD + 2 * Hv) + 2 * T * (HvD + H)
-        out[name] = {"ms": pm, "launches": 5, "tflops": flops / (pm / 1e3) / 1e12,
+        out[name] = {"ms": pm, "torch_cublas_ms": cm, "tflops": flops / (pm / 1e3) / 1e12,
                      "frac_of_bf16_peak": flops / (pm / 1e3) / 1e12 / tf,
                      "GBps": (wbytes + abytes) / (pm / 1e3) / 1e9,
                      "frac_of_hbm_peak": (wbytes + abytes) / (pm / 1e3) / 1e9 / hbm,

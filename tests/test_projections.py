@@ -41,9 +41,10 @@ def _run(c, T, rows=None, ws_bytes=0):
     _close(out[sel], oracle.out_proj(c.y[sel], c.W_out))
 
 
-@pytest.mark.parametrize("T,ws", [(300, 0), (64, 4 << 20), (1, 0)])
+@pytest.mark.parametrize("T,ws", [(300, 0), (64, 4 << 20), (48, 0), (17, 1 << 20), (1, 0)])
 def test_projections_35b_dims(T, ws):
-    """Hidden 2048, 16/32 heads: a ragged prefill, the B=64 decode batch, a single token."""
+    """Hidden 2048, 16/32 heads: a ragged prefill, the B=64 decode batch, 48 and 17 rows, and a
+    single token, with and without a workspace."""
     c = gdn_inputs.make_proj_case(T=T, H=2048, Hk=16, Hv=32, seed=200 + T)
     _run(c, T, ws_bytes=ws)
 
