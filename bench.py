@@ -590,7 +590,9 @@ def _barrier(world):
 def _max_over_ranks(v, world):
     if world <= 1:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    # NCCL reduces device tensors; the CPU (gloo) process group used by the tests reduces host ones
+    on_gpu = torch.distributed.get_backend() == "nccl"
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if on_gpu else "cpu")
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 
