@@ -19,6 +19,9 @@ sheet (Qwen 3.6, ggml-org GGUF)", "Gated DeltaNet layer" paragraph:
 speculative verification (the page's "Drafting" section: verify-walk rollback
 from per-position state snapshots; the NEXTN.md page's "GDN rollback").
 
+``in_proj`` / ``out_proj`` are the projections either side of the mixer
+(attn_qkv, attn_gate, ssm_alpha, ssm_beta; ssm_out) as fp64 matmuls.
+
 Parity status of each function is stated in its docstring; every one is pinned
 by ``tests/test_oracle_*.py`` against closed forms, invariants, library
 routines or brute force (none is "parity unpinned").
