@@ -34,6 +34,7 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_CHECK_FINITE = 1
 GDN_FLAG_PREFILL_FP32 = 2
 GDN_FLAG_STATE_BF16 = 4
+GDN_FLAG_TEST_STALL = 1 << 30
 PREFILL_STATIC_SCRATCH_BYTES = 128 * 1024 * 1024   # GDN_PREFILL_STATIC_SCRATCH_BYTES
 
 EXPORTED_SYMBOLS = (
@@ -129,12 +130,15 @@ def _dt(t: torch.dtype) -> int:
 
 
 def make_dims(Hk: int, Hv: int, act_dtype=torch.bfloat16, out_dtype=torch.float32, eps: float = 1e-6,
-              check_finite: bool = False, prefill_fp32: bool = False, state_dtype=torch.float32) -> GdnDims:
-    """state_dtype torch.bfloat16 selects GDN_FLAG_STATE_BF16 (bf16 activations only)."""
+              check_finite: bool = False, prefill_fp32: bool = False, state_dtype=torch.float32,
+              test_stall: bool = False) -> GdnDims:
+    """state_dtype torch.bfloat16 selects GDN_FLAG_STATE_BF16 (bf16 activations only);
+    test_stall selects GDN_FLAG_TEST_STALL (the give-up path of the kernels' waits)."""
     if state_dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("state_dtype must be torch.float32 or torch.bfloat16")
     flags = (GDN_FLAG_CHECK_FINITE if check_finite else 0) | (GDN_FLAG_PREFILL_FP32 if prefill_fp32 else 0)
     flags |= GDN_FLAG_STATE_BF16 if state_dtype == torch.bfloat16 else 0
+    flags |= GDN_FLAG_TEST_STALL if test_stall else 0
     return GdnDims(Hk, Hv, eps, _dt(act_dtype), _dt(out_dtype), flags)
 
 

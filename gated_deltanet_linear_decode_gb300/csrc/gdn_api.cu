@@ -1,6 +1,7 @@
 // gdn_api.cu -- the C ABI of libgdn.so (include/gdn.h): argument validation,
 // launch configuration and dispatch.  Host code only; every step of the
-// layer runs in the kernels of gdn_recurrent.cu and gdn_prefill.cu.
+// layer runs in the kernels of gdn_recurrent.cu, gdn_recurrent_stream.cu and
+// the gdn_prefill_*.cu files.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -52,7 +53,8 @@ gdn_status check_dims(const gdn_dims* d) {
     if ((d->act_dtype != GDN_F32 && d->act_dtype != GDN_BF16) ||
         (d->out_dtype != GDN_F32 && d->out_dtype != GDN_BF16))
         return GDN_E_INVALID_ARG;
-    if (d->flags & ~(GDN_FLAG_CHECK_FINITE | GDN_FLAG_PREFILL_FP32 | GDN_FLAG_STATE_BF16)) return GDN_E_INVALID_ARG;
+    if (d->flags & ~(GDN_FLAG_CHECK_FINITE | GDN_FLAG_PREFILL_FP32 | GDN_FLAG_STATE_BF16 | GDN_FLAG_TEST_STALL))
+        return GDN_E_INVALID_ARG;
     if (d->H_v / d->H_k > 16) return GDN_E_UNSUPPORTED;
     if ((d->flags & GDN_FLAG_STATE_BF16) && d->act_dtype != GDN_BF16) return GDN_E_UNSUPPORTED;
     return GDN_OK;
@@ -78,10 +80,6 @@ gdn_status check_ptrs(std::initializer_list<const void*> required, std::initiali
 // Rows of one v-head owned by one CTA of the recurrent kernel, chosen so a
 // (sequence, q/k-head group) cluster has at most 8 CTAs where possible.
 int rows_per_cta(int r) {
-#ifdef GDN_REC_ROWS
-    if (GDN_REC_ROWS * r <= 16 * 128 / 8 && 128 % GDN_REC_ROWS == 0 && r * (128 / GDN_REC_ROWS) <= 16)
-        return GDN_REC_ROWS;
-#endif
     if (r <= 2) return 32;
     if (r <= 4) return 64;
     return 128;

@@ -11,6 +11,7 @@ namespace gdn {
 constexpr uint32_t kFlagCheckFinite = 1u;
 constexpr uint32_t kFlagForceSimt = 2u;   // GDN_FLAG_PREFILL_FP32
 constexpr uint32_t kFlagStateBf16 = 4u;   // GDN_FLAG_STATE_BF16: states stored as bf16
+constexpr uint32_t kFlagTestStall = 1u << 30;   // GDN_FLAG_TEST_STALL: exercise the give-up path of the waits
 
 // Recurrent walk (decode step when K == 1 and the outputs alias the states;
 // speculative verify when the outputs are the checkpoint planes).

@@ -371,6 +371,7 @@ cudaError_t launch_tensor_core_prefill(const PrefillParams& p, int out_dtype, cu
     }
     cudaEvent_t ev[3] = {};
     for (int k = 0; k <= nseg && e == cudaSuccess; ++k) e = cudaEventCreateWithFlags(&ev[k], cudaEventDisableTiming);
+    bool side_used = false;   // work (or a wait) is queued on the side stream
     for (int k = 0; k < nseg && e == cudaSuccess; ++k) {
         PrefillParams q = p;
         q.chunk_lo = static_cast<int>(static_cast<long long>(nc) * k / nseg);
@@ -378,10 +379,21 @@ cudaError_t launch_tensor_core_prefill(const PrefillParams& p, int out_dtype, cu
         if ((e = launch_chunk_prep(q, stream)) != cudaSuccess) break;
         if ((e = cudaEventRecord(ev[k], stream)) != cudaSuccess) break;
         if ((e = cudaStreamWaitEvent(side, ev[k], 0)) != cudaSuccess) break;
+        side_used = true;
         e = launch_state_pass(q, out_dtype, side);
     }
-    if (e == cudaSuccess) e = cudaEventRecord(ev[nseg], side);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[nseg], 0);   // the caller's stream sees every segment
+    // Once anything is queued on the side stream, the caller's stream waits for
+    // it, on the error path too: a later call on the caller's stream must not
+    // overwrite records that a queued state pass still reads.  The first error
+    // is the one returned.
+    if (side_used) {
+        cudaError_t j = cudaEventRecord(ev[nseg], side);
+        if (j == cudaSuccess) j = cudaStreamWaitEvent(stream, ev[nseg], 0);
+        if (j != cudaSuccess) {
+            cudaStreamSynchronize(side);   // no event to order by: drain the side stream instead
+            if (e == cudaSuccess) e = j;
+        }
+    }
     for (int k = 0; k <= nseg; ++k)
         if (ev[k]) cudaEventDestroy(ev[k]);   // released once the recorded work completes
     return e;
@@ -402,6 +414,8 @@ cudaError_t launch_prefill(const PrefillParams& p, int act_dtype, int out_dtype,
         e = launch_prefill_simt(p, act_dtype, out_dtype, stream);
     }
     if (e != cudaSuccess) return e;
+    // the test hook leaves every state of the tensor-core path as it was
+    if ((p.flags & kFlagTestStall) && use_tensor_cores(act_dtype, p.flags)) return cudaSuccess;
     if (act_dtype == 1)
         conv_state_finalize_kernel<__nv_bfloat16><<<dim3((p.C + 255) / 256, p.n_seq), 256, 0, stream>>>(p);
     else

@@ -61,6 +61,7 @@ enum : int {
     kEpi0, kEpi1,                      // epilogue done with the O buffer of even / odd chunks (128 arrivals)
     kESync,                            // the epilogue warps' own barrier (128 arrivals, once per use)
     kDrain,                            // error path: every MMA issued so far retired
+    kNever,                            // test stall: nothing arrives
     kNumBars
 };
 
@@ -161,6 +162,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
         }
         tc::tmem_wait_st();
     }
+    // test hook: a wait that nothing ends, so every role takes its give-up path at once
+    if (tid == 0 && (p.flags & kFlagTestStall) && !tc::mbar_wait(bars + kNever, 0, 1 << 12)) *err_s = 1;
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();

@@ -5,8 +5,6 @@
 // to gdn_prefill_chunked as the workspace; nothing else differs.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "gdn.h"
 
 namespace {
@@ -18,24 +16,15 @@ constexpr size_t kScratchBytes = GDN_PREFILL_STATIC_SCRATCH_BYTES;
 // device address; the kernels get the address looked up below.
 static __device__ __align__(256) unsigned char g_prefill_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_lock;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the area on the current device, looked up once per device.
+// Device address of the area on the current device.  Looked up on every call
+// (a host-side query): a cached address would go stale if the device's
+// context were destroyed and created again (cudaDeviceReset, or the primary
+// context released), which loads the module anew, possibly elsewhere.
 cudaError_t scratch_address(void** addr) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_prefill_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> guard(g_lock);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_prefill_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
-    }
-    *addr = g_scratch_addr[dev];
+    *addr = p;
     return cudaSuccess;
 }
 

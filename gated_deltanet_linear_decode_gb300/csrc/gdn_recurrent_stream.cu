@@ -38,6 +38,30 @@ constexpr int kStages = 2;
 
 // Barrier among the compute warps only (the producer warp never joins it).
 __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSThreads) : "memory"); }
+// The same barrier, returning whether any compute thread passed a nonzero v
+// (one decision for all of them).
+__device__ __forceinline__ bool compute_sync_any(int v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v), "n"(kSThreads)
+        : "memory");
+    return r != 0;
+}
+constexpr int kWaitLimit = 1 << 22;   // polls of one stage wait before it gives up
+constexpr int kStallLimit = 1 << 12;  // polls of the test stall (a barrier nothing arrives on)
+
+// Bounded wait on phase `parity` of `mbar` that also gives up as soon as
+// *abort is set (another warp gave up).
+__device__ __forceinline__ bool stage_wait(uint64_t* mbar, uint32_t parity, volatile int* abort) {
+    for (int it = 0; it < kWaitLimit; it += 16) {
+        if (tc::mbar_wait(mbar, parity, 16)) return true;
+        if (*abort) return false;
+    }
+    return false;
+}
 
 __device__ __forceinline__ float conv4(float4 w, float x0, float x1, float x2, float cur) {
     return fmaf(w.w, cur, fmaf(w.z, x2, fmaf(w.y, x1, w.x * x0)));
@@ -87,12 +111,17 @@ recurrent_stream_kernel(const RecParams p) {
     float* nw_s = gates + 2 * kMaxK;                                              // [128]
     uint64_t* full = reinterpret_cast<uint64_t*>(nw_s + 128);                     // [kStages] stage landed
     uint64_t* empty = full + kStages;                                              // [kStages] stage copied out
+    uint64_t* never = empty + kStages;                                             // test stall: no arrivals
+    volatile int* abort_s = reinterpret_cast<volatile int*>(never + 1);           // a wait gave up
 
-    if (tid == 0)
+    if (tid == 0) {
         for (int st = 0; st < kStages; ++st) {
             tc::mbar_init(&full[st], 1);
             tc::mbar_init(&empty[st], 1);
         }
+        tc::mbar_init(never, 1);
+        *abort_s = 0;
+    }
     if (tid < kD) nw_s[tid] = p.norm_w[tid];
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
@@ -128,17 +157,37 @@ recurrent_stream_kernel(const RecParams p) {
         for (int t = 0; t < K; ++t) bulk_g2s(base + L.zr + t * seg, zin + static_cast<size_t>(t) * HvD, seg, mb);
     };
 
+    // Bit 4 of dev_status marks every (sequence, v-head) of item i and later
+    // items of this CTA: a wait gave up, so their states and outputs were not
+    // (fully) written.
+    auto report_from = [&](int i0, int idx, int cnt) {
+        if (!p.dev_status) return;
+        for (int i = i0 + idx; i < n_items; i += cnt) {
+            const int g = item_group(i);
+            atomicOr(p.dev_status + (g / p.Hk) * p.Hv + g % p.Hk + (i % r) * p.Hk, 16);
+        }
+    };
+
     if (warp == kProducerWarp) {
-        // ================= producer: item i into stage i % kStages once item i - kStages has left it
-        if (lane == 0)
-            for (int i = 0; i < n_items; ++i) {
+        // ================= producer: item i into stage i % kStages once item i - kStages has left it.
+        // On a wait that gives up it issues nothing more, and it returns only once
+        // every copy it issued has landed (none may land in a released CTA).
+        if (lane == 0) {
+            int issued = 0;
+            bool ok = true;
+            if (p.flags & kFlagTestStall) ok = tc::mbar_wait(never, 0, kStallLimit);   // never completes
+            for (int i = 0; i < n_items && ok; ++i) {
                 const int st = i % kStages;
-                if (i >= kStages && !tc::mbar_wait(&empty[st], ((i / kStages) - 1) & 1, 1 << 22)) {
-                    const int g = item_group(i);
-                    if (p.dev_status) atomicOr(p.dev_status + (g / p.Hk) * p.Hv + g % p.Hk, 16);
-                }
+                if (i >= kStages && !(ok = stage_wait(&empty[st], ((i / kStages) - 1) & 1, abort_s))) break;
                 issue(i);
+                issued = i + 1;
             }
+            if (!ok) {
+                *abort_s = 1;
+                for (int i = max(0, issued - kStages); i < issued; ++i)
+                    tc::mbar_wait(&full[i % kStages], (i / kStages) & 1, kWaitLimit);
+            }
+        }
         return;
     }
 
@@ -155,9 +204,7 @@ recurrent_stream_kernel(const RecParams p) {
             b_raw = ld_act(static_cast<const Tact*>(p.b_raw) + gi);
         }
         const float a_dt = p.dt_bias[h], a_ssm = p.ssm_a[h];
-        if (!tc::mbar_wait(&full[i % kStages], (i / kStages) & 1, 1 << 22)) {
-            if (tid == 0 && p.dev_status) atomicOr(p.dev_status + b * p.Hv + h, 16);
-        }
+        const bool landed = stage_wait(&full[i % kStages], (i / kStages) & 1, abort_s);
         // state rows -> registers; small inputs -> private area
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr)
@@ -168,7 +215,13 @@ recurrent_stream_kernel(const RecParams p) {
             gates[2 * tid] = sigmoidf_(b_raw);
             gates[2 * tid + 1] = a_ssm * softplusf_(a_raw + a_dt);
         }
-        compute_sync();
+        // one decision for all compute warps, before anything is written: stop at the
+        // first item whose stage did not land (what was read from it is discarded)
+        if (compute_sync_any(!landed)) {
+            *abort_s = 1;
+            report_from(i, tid, kSThreads);
+            break;
+        }
         if (tid == 0) tc::mbar_arrive(&empty[i % kStages]);   // the stage may be refilled
 
         const float4* cw = reinterpret_cast<const float4*>(cur);                      // [384] taps
@@ -288,7 +341,7 @@ size_t recurrent_stream_smem(int K, int act_dtype, bool state_bf16) {
     const int es = act_dtype == 1 ? 2 : 4;
     const StageLayout L(K, es, state_bf16 ? 2 : 4);
     const size_t cur = ((L.bytes - L.cw + 15) & ~static_cast<size_t>(15));
-    const size_t misc = (static_cast<size_t>(K) * 384 + 128 + 16 + 8 + 2 * kMaxK + 128) * 4 + 2 * kStages * 8;
+    const size_t misc = (static_cast<size_t>(K) * 384 + 128 + 16 + 8 + 2 * kMaxK + 128) * 4 + 2 * kStages * 8 + 16;
     return kStages * static_cast<size_t>(L.bytes) + cur + misc;
 }
 

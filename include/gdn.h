@@ -55,9 +55,12 @@
  *   - dev_status (optional, may be NULL) is int32 [N*H_v].  When
  *     GDN_FLAG_CHECK_FINITE is set, the kernels OR bit 0 into
  *     dev_status[n*H_v + h] if the updated state of (n, h) holds a non-finite
- *     value and bit 1 if its output does.  The caller zeroes it and reads it
- *     after synchronising (the production failure mode the home-server page
- *     records: non-finite GDN state that persists in cached state).
+ *     value and bit 1 if its output does.  Bit 4, whatever the flags, means
+ *     that a bounded wait inside a kernel gave up and the state and outputs of
+ *     (n, h) were not (fully) written (see GDN_FLAG_TEST_STALL).  The caller
+ *     zeroes it and reads it after synchronising (the production failure mode
+ *     the home-server page records: non-finite GDN state that persists in
+ *     cached state).
  */
 #ifndef GDN_H
 #define GDN_H
@@ -101,6 +104,19 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
  * Halves the state bytes of the recurrent calls.  Requires act_dtype = GDN_BF16 (else
  * GDN_E_UNSUPPORTED). */
 #define GDN_FLAG_STATE_BF16 4u
+/* Test hook for the failure path of the kernels' bounded waits (no use in
+ * production).  Every wait inside a kernel has an iteration limit; when one
+ * gives up, the kernel stops issuing work, lets the asynchronous copies and
+ * MMAs it already issued complete, writes nothing more, ORs bit 4 into
+ * dev_status for every (sequence, v-head) it did not finish, and returns, so
+ * the CUDA context stays usable.  With this flag the kernels that carry the
+ * hook -- the streaming recurrent kernel that gdn_decode_step / gdn_verify_k
+ * use when B*H_k is at least twice the SM count, and the state pass of the
+ * bf16 gdn_prefill_chunked -- first wait on a barrier that nothing arrives
+ * on, so that wait gives up after a few microseconds and the path above runs
+ * with none of the call's work done: every (sequence, v-head) they own
+ * reports bit 4 and S, conv_state and out keep their previous contents. */
+#define GDN_FLAG_TEST_STALL (1u << 30)
 
 typedef struct {
     int32_t H_k;        /* q/k heads (16 in both model sizes on the page)       */
@@ -303,9 +319,11 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, int32
  * up to 1,280 tokens fits).  Calls that need no workspace (fp32 activations,
  * or GDN_FLAG_PREFILL_FP32) do not touch the area.
  *
- * Set-up: the first call on a device that needs the area looks up its device
- * address (cudaGetSymbolAddress with that device current), which can
- * initialise the CUDA context; make that first call before any stream
+ * Set-up: every call that needs the area looks up its device address on the
+ * current device (cudaGetSymbolAddress, a host-side query; nothing is cached,
+ * so the address stays right if the device's context is destroyed and created
+ * again).  The first such call on a device can initialise the CUDA context
+ * and load the library's device code; make that first call before any stream
  * capture.  A failed look-up returns GDN_E_CUDA.
  *
  * Sharing: every call uses the same area, which keeps the previous call's

@@ -2,7 +2,8 @@
 gdn_decode_step_ring): over several speculative rounds the ring path gives
 bit for bit the outputs, checkpoints and live state of the copying
 verify + commit path, reads only the live slot and writes only the slots
-after it.  The copying path itself is held to the oracle elsewhere."""
+after it; and over several rounds it matches the fp64 oracle's verify walk
+and commits directly."""
 import pytest
 import torch
 
@@ -98,3 +99,51 @@ def test_decode_step_ring_equals_decode_step(B, Hk, Hv, act):
                 if j != k:                  # the other slots are not touched
                     assert torch.equal(S_ring[bb, j].isnan(), ring0[bb, j].isnan())
     assert torch.equal(cur.cpu(), torch.arange(B, dtype=torch.int32) % R)
+
+
+@pytest.mark.parametrize("B,Hk,Hv,K,R,act", [
+    (64, 16, 32, 3, 4, torch.bfloat16),     # the streaming kernel (the verify workload's shape)
+    (3, 2, 4, 4, 6, torch.float32),         # the cluster kernel, R > K + 1
+])
+def test_ring_rounds_match_oracle(B, Hk, Hv, K, R, act):
+    """Three speculative rounds on the state ring against the fp64 oracle's
+    verify walk (checkpoint p = the state after draft position p; accept n
+    makes checkpoint n - 1 the live state), the oracle carrying its own
+    committed states from round to round: outputs, every checkpoint slot, the
+    live slot after each commit (tolerances of tests/gpu_util.py) and the conv
+    checkpoints and conv state (bit for bit)."""
+    import numpy as np
+    import oracle
+    rounds = 3
+    c = gdn_inputs.make_case("ring_oracle", Hk=Hk, Hv=Hv, B=B, K=rounds * K, act_dtype=act, seed=310 + B)
+    d, w = G.dims(c), G.weights(c)
+    gen = torch.Generator().manual_seed(11)
+    conv_r = G.dev(c.conv0)
+    S_ring = torch.full((B, R, c.Hv, 128, 128), float("nan"), device="cuda")
+    S_ring[:, 0] = G.dev(c.S0)
+    cur = torch.zeros(B, dtype=torch.int32, device="cuda")
+    ck_conv = torch.empty(B, K, 3, c.C, device="cuda", dtype=act)
+    out = torch.empty(B * K, c.Hv * 128, device="cuda")
+    conv_ref, S_ref = c.conv0.float().numpy(), c.S0.double().numpy()
+    rows = lambda t, r: t.view(B, rounds * K, *t.shape[1:])[:, r * K:(r + 1) * K].reshape(B * K, *t.shape[1:])
+    for r in range(rounds):
+        x, z, a, b = (rows(t, r).contiguous() for t in (c.x, c.z, c.a_raw, c.b_raw))
+        acc = torch.randint(1, K + 1, (B,), generator=gen, dtype=torch.int32)
+        cur0 = cur.cpu().numpy().copy()
+        gdn.gdn_verify_k_ring(d, w, K, G.dev(x), G.dev(z), G.dev(a), G.dev(b), conv_r, S_ring, cur, ck_conv, out)
+        gdn.gdn_commit_ring(d, K, R, acc.cuda(), ck_conv, conv_r, cur)
+        torch.cuda.synchronize()
+        o_ref, _, S_ck, c_ck = oracle.verify_checkpoints(Hk, Hv, x, z, a, b, c.conv_w, c.dt_bias, c.ssm_a,
+                                                         c.norm_w, conv_ref, S_ref, K)
+        G.assert_out_close(out, o_ref, act)
+        assert G.conv_bits_equal(ck_conv, c_ck, act)
+        ring = S_ring.cpu()
+        for p in range(K):
+            slots = torch.from_numpy((cur0 + 1 + p) % R)
+            G.assert_state_close(ring[torch.arange(B), slots], S_ck[:, p], act)
+        n = acc.numpy()
+        S_ref = S_ck[np.arange(B), n - 1]
+        conv_ref = c_ck[np.arange(B), n - 1]
+        assert np.array_equal(cur.cpu().numpy(), (cur0 + n) % R)
+        G.assert_state_close(ring[torch.arange(B), cur.cpu().long()], S_ref, act)
+        assert G.conv_bits_equal(conv_r, conv_ref, act)
