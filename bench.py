@@ -84,8 +84,8 @@ def prefill_flops(T, Hv):
 # The sources that decide each part's kernels, launch shapes and memory traffic.
 _COMMON_SOURCES = ("gdn_api.cu", "gdn_common.cuh", "gdn_internal.h", "gdn_tc.cuh")
 PART_SOURCES = {
-    "prefill": _COMMON_SOURCES + ("gdn_prefill_prep.cu", "gdn_prefill_state.cu", "gdn_prefill_simt.cu",
-                                  "gdn_prefill_tc.cuh"),
+    "prefill": _COMMON_SOURCES + ("gdn_prefill_tc.cu", "gdn_prefill_prep.cuh", "gdn_prefill_chain.cuh",
+                                  "gdn_prefill_simt.cu", "gdn_prefill_tc.cuh"),
     "decode": _COMMON_SOURCES + ("gdn_recurrent.cu", "gdn_recurrent_stream.cu"),
 }
 

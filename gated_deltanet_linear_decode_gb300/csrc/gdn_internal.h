@@ -105,6 +105,7 @@ struct PrefillParams {
     int chunk_lo, chunk_hi;  // global chunk range of this launch of the two kernels
     int* chunk_base;         // device [n_seq+1]
     uint8_t* ws_v;           // v-head records, [n_chunks][Hv]
+    int* ready;              // [n_chunks][Hk] ready flags of the records (zeroed per call)
 };
 
 // Workspace bytes of gdn_prefill_chunked for the path that act_dtype / flags select.

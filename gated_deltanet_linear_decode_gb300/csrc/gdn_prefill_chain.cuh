@@ -1,11 +1,12 @@
-// gdn_prefill_state.cu -- second kernel of the tensor-core prefill: the
-// chunk-to-chunk state recurrence and the layer output (xwen CLAUDE.md page,
+// gdn_prefill_chain.cuh -- the chain role of the tensor-core prefill kernel:
+// the chunk-to-chunk state recurrence and the layer output (xwen CLAUDE.md page,
 // "Ground truth": chunk = 64 form; "Architecture cheat sheet", "Gated DeltaNet
 // layer": o = S q / sqrt(128), gated RMSNorm y = o / sqrt(mean(o^2) + eps)
 // * norm_w * silu(z)).  Every state-independent quantity of a chunk comes from
-// the records of the preparation kernel.
+// the records of the preparation role, each read once its ready flag is set
+// (and dropped from L2 once consumed).
 //
-// One CTA per (sequence, v-head); the fp32 state lives in tensor memory
+// One CTA runs one (sequence, v-head) chain at a time; the fp32 state lives in tensor memory
 // (lane j = v-row j), and so do its fp16 hi/lo parts and those of D, which the
 // MMAs read as their A operand straight from tensor memory (only W^T, Q', K'
 // and P come from shared memory, whose bandwidth bounds these MMAs).  Per chunk,
@@ -25,13 +26,15 @@
 //   warp 12     control: one lane issues the MMAs
 //   warp 13     copies: one lane issues the bulk copies of the records, each as
 //               soon as the MMAs that read its buffer have retired
-// Every wait has an iteration limit; a timeout sets dev_status bit 4.
+// Every wait has an iteration (or, for the ready flags, a time) limit; a
+// timeout sets dev_status bit 4.
+#pragma once
+
 #include "gdn_internal.h"
 #include "gdn_prefill_tc.cuh"
 
 namespace gdn {
-
-namespace {
+namespace chain {
 
 constexpr int kConvWarps = 8, kEpiWarps = 4;
 constexpr int kCtrlWarp = kConvWarps + kEpiWarps;   // MMA issue
@@ -49,12 +52,14 @@ constexpr uint32_t kOst = 98304;      // the chunk's O, fp32 [128 j][kOStride], 
 constexpr uint32_t kRs = kOst + 128 * kOStride * 4;   // per-token partial sums of O^2 [2][64] fp32
 constexpr uint32_t kNw = kRs + 512;   // norm_w [128] fp32
 constexpr uint32_t kBar = kNw + 512;  // mbarriers, then the TMEM base and the error flag
-constexpr uint32_t kStateSmem = kBar + 176;
+constexpr uint32_t kUs = (kBar + 176 + 127) / 128 * 128;   // the chunk's U, e^Gam, e^{Gam_last-Gam} (record tail)
+constexpr uint32_t kUBytes = pf::kVRec - pf::kRecU;          // 33280
+constexpr uint32_t kStateSmem = kUs + kUBytes;
 static_assert(kStateSmem <= 232448, "shared memory of the state pass exceeds 227 KB");
 
 // mbarrier slots
 enum : int {
-    kLdW = 0, kLdQ, kLdK, kLdP,        // record copies landed (transaction count)
+    kLdW = 0, kLdQ, kLdK, kLdP, kLdU,  // record copies landed (transaction count)
     kMmaD, kMmaO1, kMmaS,              // Dacc / first O group / state update retired (tcgen05.commit)
     kODone0, kODone1,                  // O of even / odd chunks complete
     kSReady, kDReady,                  // converters wrote the S / D operands (256 arrivals)
@@ -70,11 +75,14 @@ enum : int {
 constexpr uint32_t kColS = 0, kColShi = 128, kColSlo = 192, kColD = 256, kColDhi = 320, kColDlo = 352, kColO = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kWaitLimit = 1 << 24;
+constexpr uint64_t kReadyTimeoutNs = 2000000000ull;   // 2 s for a record to appear
 
+// One chain: sequence s, v-head h, on the CTA's kStateThreads threads, with
+// the CTA's tensor memory (kTmemCols columns at tmem).  Returns with every
+// MMA retired, every copy landed and every thread past a CTA-wide barrier, so
+// the next chain may reuse the barriers, shared and tensor memory.
 template <typename Tout>
-__global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const PrefillParams p) {
-    extern __shared__ __align__(1024) uint8_t sm[];
-    const int s = blockIdx.x / p.Hv, h = blockIdx.x % p.Hv;
+__device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t tmem) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hv = p.Hv, HvD = Hv * kD;
     // this launch's chunks of sequence s: [cb, ce) of its own; the state comes in and goes out
@@ -98,16 +106,17 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBar);
     static_assert(8 * kNumBars + 8 <= 176, "mbarrier area");
-    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sm + kBar + 8 * kNumBars);
     volatile int* err_s = reinterpret_cast<volatile int*>(sm + kBar + 8 * kNumBars + 4);
     const uint32_t sb = tc::smem_u32(sm);
+    const int kh = h % p.Hk;
 
-    if (warp == 0) tc::tmem_alloc(tmem_base_s, kTmemCols);
+    __syncthreads();   // the previous chain of this CTA is done with every barrier
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t cnt = 1;
             if (i == kSReady || i == kDReady) cnt = kConvThreads;
             if (i == kEpi0 || i == kEpi1 || i == kESync) cnt = kEpiThreads;
+            asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bars + i)) : "memory");
             tc::mbar_init(bars + i, cnt);
         }
         *err_s = 0;
@@ -116,7 +125,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = *tmem_base_s;
 
     // Bounded wait that also gives up as soon as another role has timed out.
     // Converter and epilogue warps back off with short sleeps so that waiting
@@ -140,6 +148,25 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
 
     const uint8_t* vrec0 = p.ws_v + (static_cast<size_t>(cbase) * Hv + h) * pf::kVRec;
     auto vrec = [&](int c) { return vrec0 + static_cast<size_t>(c) * Hv * pf::kVRec; };
+    // Acquire the ready flag of chunk c's records (set by the preparation role once
+    // they are written); bounded in time, and given up as soon as another role has.
+    const int* ready = p.ready + static_cast<size_t>(cbase) * p.Hk + kh;
+    auto wait_ready = [&](int c) -> bool {
+        const int* f = ready + static_cast<size_t>(c) * p.Hk;
+        if (pf::ld_acquire(f)) return true;
+        const uint64_t t0 = pf::global_ns();
+        uint32_t ns = 64;
+        for (;;) {
+            if (pf::ld_acquire(f)) return true;
+            if (*err_s) return false;
+            if (pf::global_ns() - t0 > kReadyTimeoutNs) {
+                *err_s = 1;
+                return false;
+            }
+            __nanosleep(ns);
+            ns = min(ns * 2, 2048u);
+        }
+    };
 
     // ---- initial state into tensor memory (converter warps; lane j = row j)
     const int quarter = warp & 3;
@@ -224,38 +251,58 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
             }
         }
     } else if (warp == kCopyWarp) {
-        // ================= copies: the records of chunk c + 1 as soon as chunk c's MMAs free the buffers
+        // ================= copies: the records of chunk c + 1 as soon as its ready flag is
+        // set and chunk c's MMAs have freed the buffers; lane 0 issues, the whole warp drops
+        // each consumed record from L2.  Lane 0 decides; the warp follows through shuffles.
+        auto discard = [&](int c) {   // whole warp: record c is consumed
+            const uint8_t* r = vrec(c);
+            for (uint32_t o = 128u * lane; o < pf::kVRec; o += 128u * 32) pf::discard_l2(r + o);
+        };
+        int req_w = 0, req_q = 0, req_k = 0, req_p = 0, req_u = 0;   // chunks requested per barrier (an error path drains them)
+        auto load = [&](int bar, uint32_t dst, int c, uint32_t off, uint32_t bytes, int& req) {
+            tc::mbar_expect_tx(bars + bar, bytes);
+            tc::bulk_g2s(sm + dst, vrec(c) + off, bytes, bars + bar);
+            req = c + 1;
+        };
+        bool ok = true;
         if (lane == 0 && nch > 0) {
-            int req_w = 0, req_q = 0, req_k = 0, req_p = 0;   // chunks requested per barrier (an error path drains them)
-            auto load = [&](int bar, uint32_t dst, int c, uint32_t off, uint32_t bytes, int& req) {
-                tc::mbar_expect_tx(bars + bar, bytes);
-                tc::bulk_g2s(sm + dst, vrec(c) + off, bytes, bars + bar);
-                req = c + 1;
-            };
-            load(kLdW, kWs, 0, pf::kRecW, 16384, req_w);
-            load(kLdQ, kQs, 0, pf::kRecQhi, 32768, req_q);
-            load(kLdK, kKs, 0, pf::kRecKhi, 32768, req_k);
-            load(kLdP, kPs, 0, pf::kRecPhi, 16384, req_p);
-            for (int c = 1; c < 3 && c < nch; ++c) tc::bulk_prefetch_l2(vrec(c), pf::kRecU);   // toward L2
-            bool ok = true;
-            for (int c = 0; c + 1 < nch && ok; ++c) {
+            if ((ok = wait_ready(0))) {
+                pf::fence_proxy_async_global();
+                load(kLdW, kWs, 0, pf::kRecW, 16384, req_w);
+                load(kLdQ, kQs, 0, pf::kRecQhi, 32768, req_q);
+                load(kLdK, kKs, 0, pf::kRecKhi, 32768, req_k);
+                load(kLdP, kPs, 0, pf::kRecPhi, 16384, req_p);
+                load(kLdU, kUs, 0, pf::kRecU, kUBytes, req_u);
+            }
+        }
+        for (int c = 0; c + 1 < nch; ++c) {
+            if (lane == 0 && ok) {
                 const uint32_t pc = c & 1, b = c & 1, pb = (c >> 1) & 1;
-                if (c + 3 < nch) tc::bulk_prefetch_l2(vrec(c + 3), pf::kRecU);
-                if (!(ok = wait(kMmaD, pc))) break;         // W^T read by Dacc
-                load(kLdW, kWs, c + 1, pf::kRecW, 16384, req_w);
-                if (!(ok = wait(kMmaO1, pc))) break;        // Q' read by the first O group
-                load(kLdQ, kQs, c + 1, pf::kRecQhi, 32768, req_q);
-                if (!(ok = wait(kMmaS, pc))) break;         // K' read by the state update
-                load(kLdK, kKs, c + 1, pf::kRecKhi, 32768, req_k);
-                if (!(ok = wait(kODone0 + b, pb))) break;   // P read by the O update
-                load(kLdP, kPs, c + 1, pf::kRecPhi, 16384, req_p);
+                do {
+                    if (!(ok = wait_ready(c + 1))) break;
+                    pf::fence_proxy_async_global();
+                    if (!(ok = wait(kMmaD, pc))) break;         // W^T read by Dacc; U read by the converters
+                    load(kLdW, kWs, c + 1, pf::kRecW, 16384, req_w);
+                    load(kLdU, kUs, c + 1, pf::kRecU, kUBytes, req_u);
+                    if (!(ok = wait(kMmaO1, pc))) break;        // Q' read by the first O group
+                    load(kLdQ, kQs, c + 1, pf::kRecQhi, 32768, req_q);
+                    if (!(ok = wait(kMmaS, pc))) break;         // K' read by the state update (U by then too)
+                    load(kLdK, kKs, c + 1, pf::kRecKhi, 32768, req_k);
+                    if (!(ok = wait(kODone0 + b, pb))) break;   // P read by the O update
+                    load(kLdP, kPs, c + 1, pf::kRecPhi, 16384, req_p);
+                } while (false);
             }
-            if (!ok) {   // error path: let every issued copy land before the CTA releases its memory
-                if (req_w) tc::mbar_wait(bars + kLdW, (req_w - 1) & 1, kWaitLimit);
-                if (req_q) tc::mbar_wait(bars + kLdQ, (req_q - 1) & 1, kWaitLimit);
-                if (req_k) tc::mbar_wait(bars + kLdK, (req_k - 1) & 1, kWaitLimit);
-                if (req_p) tc::mbar_wait(bars + kLdP, (req_p - 1) & 1, kWaitLimit);
-            }
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            discard(c);
+        }
+        if (lane == 0 && ok && nch > 0) ok = wait(kODone0 + ((nch - 1) & 1), ((nch - 1) >> 1) & 1);
+        if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && nch > 0) discard(nch - 1);
+        if (lane == 0 && !ok) {   // error path: let every issued copy land before the CTA moves on
+            if (req_w) tc::mbar_wait(bars + kLdW, (req_w - 1) & 1, kWaitLimit);
+            if (req_q) tc::mbar_wait(bars + kLdQ, (req_q - 1) & 1, kWaitLimit);
+            if (req_k) tc::mbar_wait(bars + kLdK, (req_k - 1) & 1, kWaitLimit);
+            if (req_p) tc::mbar_wait(bars + kLdP, (req_p - 1) & 1, kWaitLimit);
+            if (req_u) tc::mbar_wait(bars + kLdU, (req_u - 1) & 1, kWaitLimit);
         }
     } else if (warp < kConvWarps) {
         // ================= converters: thread = v-row j (lane quarter) x column half
@@ -263,15 +310,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
         bool ok = true;
         for (int c = 0; c < nch && ok; ++c) {
             const uint32_t pc = c & 1;
-            const uint8_t* vr = vrec(c);
-            // this chunk's U^T entries (used after the S conversion)
+            // this chunk's U^T entries (used after the S conversion) and e^{Gam_last}, copied
+            // into shared memory with the chunk's tiles (the buffer is refilled once every
+            // converter has passed the S conversion, i.e. after Dacc is issued)
+            if (!(ok = wait(kLdU, pc))) break;
             float4 u4[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                u4[q] = __ldg(reinterpret_cast<const float4*>(vr + pf::kRecU) + (8 * chalf + q) * kD + row);
-            const float eg_last = __ldg(reinterpret_cast<const float*>(vr + pf::kRecEgam) + 63);
-            if (c + 1 < nch && tid == 0)   // the next chunk's U and decay vectors toward L2 (one bulk request)
-                tc::bulk_prefetch_l2(vrec(c + 1) + pf::kRecU, pf::kVRec - pf::kRecU);
+            for (int q = 0; q < 8; ++q) u4[q] = reinterpret_cast<const float4*>(sm + kUs)[(8 * chalf + q) * kD + row];
+            const float eg_last = reinterpret_cast<const float*>(sm + kUs + (pf::kRecEgam - pf::kRecU))[63];
             if (c > 0 && !(ok = wait(kMmaS, (c - 1) & 1))) break;
             tc::fence_after_sync();
             // S -> fp16 hi/lo pairs in tensor memory; S <- e^{Gam_last} S   (this thread: row j, 64 columns)
@@ -429,22 +475,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_pass_kernel(const Pref
         if (lane == 0 && st) atomicOr(p.dev_status + s * Hv + h, st);
     }
     tc::fence_after_sync();
-    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
-}  // namespace
-
-template <typename Tout>
-cudaError_t launch_state_pass_t(const PrefillParams& p, cudaStream_t stream) {
-    auto k = state_pass_kernel<Tout>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kStateSmem));
-    if (e != cudaSuccess) return e;
-    k<<<static_cast<unsigned>(p.n_seq) * p.Hv, kStateThreads, kStateSmem, stream>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_state_pass(const PrefillParams& p, int out_dtype, cudaStream_t stream) {
-    return out_dtype == 1 ? launch_state_pass_t<__nv_bfloat16>(p, stream) : launch_state_pass_t<float>(p, stream);
-}
-
+}  // namespace chain
 }  // namespace gdn

@@ -1,10 +1,11 @@
-// gdn_prefill_prep.cu -- first kernel of the tensor-core prefill: the work of
-// a chunk that does not depend on the state, for every chunk of every
-// sequence at once (xwen CLAUDE.md page, "Ground truth": chunk = 64 form;
+// gdn_prefill_prep.cuh -- the preparation role of the tensor-core prefill
+// kernel: the work of one chunk that does not depend on the state, for every
+// chunk of every sequence (xwen CLAUDE.md page, "Ground truth": chunk = 64 form;
 // "Architecture cheat sheet", "Gated DeltaNet layer": conv1d k=4 without bias,
 // SiLU, clamp L2 norm, tiled heads, beta = sigmoid(b), g = ssm_a softplus(a + dt_bias)).
 //
-// One CTA of 8 warps per (chunk, q/k head kh).  While the chunk's raw rows and
+// One item = (chunk, q/k head kh), worked by 8 warps of a CTA (they meet at
+// named barrier 1, never at the CTA-wide barrier).  While the chunk's raw rows and
 // conv taps land it computes the gates of every v-head h with h mod H_k = kh
 // (tiled heads): beta, g, Gam (fp64 scan), e^Gam, e^{Gam_last-Gam}.  It computes
 // q_hat and k_hat of the chunk once -- and from them, while they are in
@@ -16,13 +17,15 @@
 //   T = (I + A)^{-1} on the CUDA cores (fp32);
 //   U^T = V^T (T diag beta)^T, W^T = K^T (T diag(beta e^Gam))^T on the tensor
 //   cores (fp16 hi/lo split, three MMAs per product) -> record.
-// The records (layouts in gdn_prefill_tc.cuh) feed the state pass.
+// The records (layouts in gdn_prefill_tc.cuh) feed the chain role
+// (gdn_prefill_chain.cuh), which finds each one through its ready flag.
+#pragma once
+
 #include "gdn_internal.h"
 #include "gdn_prefill_tc.cuh"
 
 namespace gdn {
-
-namespace {
+namespace prep {
 
 constexpr int kPrepThreads = 256;
 
@@ -45,7 +48,7 @@ constexpr uint32_t kGates = 201280;    // per v-head of the group: 6 x [64] fp32
 constexpr uint32_t kGateBytes = 6 * 256;
 // then the conv taps of the current v-head, float4 [128]
 __host__ __device__ inline uint32_t taps_v_off(int G) { return kGates + static_cast<uint32_t>(G) * kGateBytes; }
-inline uint32_t prep_smem(int G) { return taps_v_off(G) + 128 * 16; }
+__host__ __device__ inline uint32_t prep_smem(int G) { return taps_v_off(G) + 128 * 16; }
 static_assert(kXqk + 32 * kXrows * 16 <= kDm, "q/k staging overlaps the decay matrix");
 static_assert(kDm + 64 * 65 * 4 <= kXv, "decay matrix overlaps the v staging");
 static_assert(kXv + 16 * kXrows * 16 <= kMisc, "v staging overlaps the barriers");
@@ -54,10 +57,18 @@ static_assert(kAf + 64 * pf::kTS * 4 <= kTf && kTf + 64 * pf::kTS * 4 <= kDm, "A
 constexpr uint32_t kColQK = 0, kColU = 64, kColW = 128, kPrepTmemCols = 256;
 constexpr int kWaitLimit = 1 << 22;
 
-__global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const PrefillParams p) {
-    extern __shared__ __align__(1024) uint8_t sm[];
+// Per-CTA state of the preparation role, kept across items: the tensor-memory
+// base (kPrepTmemCols columns), the MMA-completion mbarrier and its phase, and
+// a sticky error flag (a wait gave up).
+struct Ctx {
+    uint32_t tmem;
+    uint64_t* mbar;
+    uint32_t phase;
+    int* err_s;
+};
+
+__device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& cx) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int gc = p.chunk_lo + static_cast<int>(blockIdx.x), kh = blockIdx.y;
     const int Hk = p.Hk, Hv = p.Hv, C = p.C;
 
     // sequence of this chunk: the last s with chunk_base[s] <= gc (a non-empty one)
@@ -82,31 +93,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
     const int G = Hv / Hk;
     const float4* taps_qk = reinterpret_cast<const float4*>(sm + kTb);
     const float4* taps_v = reinterpret_cast<const float4*>(sm + taps_v_off(G));
-    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sm + kMisc);
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + kMisc + 8);
-    int* err_s = reinterpret_cast<int*>(sm + kMisc + 16);
+    uint64_t* mbar = cx.mbar;
+    int* err_s = cx.err_s;
     const uint32_t sb = tc::smem_u32(sm);
-
-    if (warp == 0) tc::tmem_alloc(tmem_base_s, kPrepTmemCols);
-    if (tid == 0) {
-        tc::mbar_init(mbar, 1);
-        *err_s = 0;
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *tmem_base_s;
+    const uint32_t tmem = cx.tmem;
     const int quarter = warp & 3, chalf = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float* ghi_s = nullptr;
     const float* glo_s = nullptr;
     auto dgam = [&](int t, int r) { return (ghi_s[t] - ghi_s[r]) + (glo_s[t] - glo_s[r]); };
-    uint32_t phase = 0;
     auto wait_mma = [&]() {
-        const bool ok = tc::mbar_wait(mbar, phase, kWaitLimit);
-        phase ^= 1u;
+        const bool ok = tc::mbar_wait(mbar, cx.phase, kWaitLimit);
+        cx.phase ^= 1u;
         if (!ok) atomicExch(err_s, 1);
         tc::fence_after_sync();
     };
@@ -159,7 +158,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
             graw[e] = gt;
             gate(g, kEg)[t] = __expf(gt);
         }
-        __syncthreads();
+        pf::prep_sync();
         for (int g = warp; g < G; g += kPrepThreads / 32) {
             // inclusive scan in fp64: lane l owns tokens 2l, 2l+1
             const double g0 = static_cast<double>(graw[64 * g + 2 * lane]), g1 = static_cast<double>(graw[64 * g + 2 * lane + 1]);
@@ -183,7 +182,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         }
     }
     tc::cp_async_drain();
-    __syncthreads();
+    pf::prep_sync();
 
     // ---- q_hat, k_hat: conv, SiLU, clamp L2 -> [Q;K] hi/lo in shared memory.
     // Warp w owns staged channel groups 4w .. 4w+3 (q for w < 4, k for w >= 4;
@@ -218,7 +217,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         }
         ssq[warp * 64 + lane] = ss[0];
         ssq[warp * 64 + 32 + lane] = ss[1];
-        __syncthreads();
+        pf::prep_sync();
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             const int t = 32 * hf + lane;
@@ -254,7 +253,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         }
     }
     tc::fence_proxy_async();
-    __syncthreads();
+    pf::prep_sync();
     // [Q;K] K^T (3 passes, K = 128): rows t < 64 give Q K^T, rows 64 + t give K K^T
     if (tid == 0) {
         tc::fence_after_sync();
@@ -305,7 +304,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
                 *reinterpret_cast<uint4*>(sm + kVs + 16384 + ov) = vl;
             }
         }
-        __syncthreads();
+        pf::prep_sync();
         // decay matrix e^{Gam_t - Gam_r} (r <= t, else 0): one exponential at the right end
         // of the thread's 16 columns, then leftwards e^{Gam_t - Gam_{r-1}} = e^{Gam_t - Gam_r} e^{g_r};
         // e^Gam and e^{Gam_last - Gam_t} -> record
@@ -324,7 +323,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
                 reinterpret_cast<float*>(vrec + pf::kRecElast)[tid] = elast_s[tid];
             }
         }
-        __syncthreads();
+        pf::prep_sync();
         if (g == 0) wait_mma();   // the [Q;K] K^T products
         else tc::fence_after_sync();
         // P (rows t < 64 of the product) -> record; A (rows 64 + t) -> shared fp32
@@ -361,7 +360,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
             }
         }
         tc::fence_before_sync();
-        __syncthreads();
+        pf::prep_sync();
         // the next v-head's raw rows start loading while the diagonal blocks are solved
         pf::unit_lower_inverse<kPrepThreads>(Af, reinterpret_cast<float*>(sm + kTf), reinterpret_cast<float*>(sm + kDm),
                                              [&](int i) {
@@ -399,7 +398,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
             }
         }
         tc::fence_proxy_async();
-        __syncthreads();
+        pf::prep_sync();
         // U^T = V^T (T diag beta)^T ;  W^T = K^T (T diag(beta e^Gam))^T   (3 passes each, K = 64)
         if (tid == 0) {
             tc::fence_after_sync();
@@ -435,66 +434,18 @@ __global__ void __launch_bounds__(kPrepThreads, 1) chunk_prep_kernel(const Prefi
         tc::cp_async_drain();
         tc::fence_before_sync();
     }
-    __syncthreads();
-    if (p.dev_status && tid == 0 && *err_s) atomicOr(p.dev_status + s * Hv + kh, 16);
-    if (warp == 0) tc::tmem_dealloc(tmem, kPrepTmemCols);
-}
-
-// Exclusive prefix of the per-sequence chunk counts: chunk_base[s] is the
-// global index of sequence s's first chunk, chunk_base[n_seq] the total.
-__global__ void chunk_table_kernel(const int* cu_seqlens, int n_seq, int* chunk_base) {
-    __shared__ int carry_s;
-    __shared__ int warp_s[32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-    if (tid == 0) carry_s = 0;
-    __syncthreads();
-    for (int base = 0; base < n_seq; base += blockDim.x) {
-        const int i = base + tid;
-        const int cnt = i < n_seq ? (cu_seqlens[i + 1] - cu_seqlens[i] + kChunk - 1) / kChunk : 0;
-        int v = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int up = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += up;
-        }
-        if (lane == 31) warp_s[warp] = v;
-        __syncthreads();
-        if (warp == 0) {
-            int w = lane < nw ? warp_s[lane] : 0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int up = __shfl_up_sync(0xffffffffu, w, o);
-                if (lane >= o) w += up;
-            }
-            if (lane < nw) warp_s[lane] = w;   // inclusive over warps
-        }
-        __syncthreads();
-        const int carry = carry_s;
-        const int incl = v + (warp > 0 ? warp_s[warp - 1] : 0) + carry;
-        if (i < n_seq) chunk_base[i] = incl - cnt;
-        __syncthreads();
-        if (tid == blockDim.x - 1) carry_s = incl;
-        __syncthreads();
+    // publish: every record write of this item is visible at GPU scope before the
+    // ready flag is (the chain role acquires the flag before reading the records)
+    __threadfence();
+    pf::prep_sync();
+    if (tid == 0) {
+        if (p.dev_status && *err_s) atomicOr(p.dev_status + s * Hv + kh, 16);
+        pf::st_release(p.ready + static_cast<size_t>(gc) * Hk + kh, 1);
     }
-    if (tid == 0) chunk_base[n_seq] = carry_s;
 }
 
-}  // namespace
+// Shared-memory bytes of the role for H_v / H_k = G.
+__host__ __device__ inline uint32_t smem_bytes(int G) { return prep_smem(G); }
 
-cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t stream) {
-    chunk_table_kernel<<<1, 256, 0, stream>>>(p.cu_seqlens, p.n_seq, p.chunk_base);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_chunk_prep(const PrefillParams& p, cudaStream_t stream) {
-    if (p.chunk_hi <= p.chunk_lo) return cudaSuccess;
-    const uint32_t smem = prep_smem(p.Hv / p.Hk);
-    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    chunk_prep_kernel<<<dim3(static_cast<unsigned>(p.chunk_hi - p.chunk_lo), static_cast<unsigned>(p.Hk)), kPrepThreads, smem,
-                        stream>>>(p);
-    return cudaGetLastError();
-}
-
+}  // namespace prep
 }  // namespace gdn

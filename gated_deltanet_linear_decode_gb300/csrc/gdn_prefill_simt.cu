@@ -19,7 +19,6 @@
 // column walks free of bank conflicts).
 #include "gdn_common.cuh"
 #include <algorithm>
-#include <mutex>
 
 #include "gdn_internal.h"
 #include "gdn_prefill_tc.cuh"
@@ -300,110 +299,25 @@ cudaError_t launch_prefill_simt(const PrefillParams& p, int act_dtype, int out_d
                           : launch_prefill_simt_t<float, float>(p, stream);
 }
 
-cudaError_t launch_chunk_table(const PrefillParams& p, cudaStream_t stream);
-cudaError_t launch_chunk_prep(const PrefillParams& p, cudaStream_t stream);
-cudaError_t launch_state_pass(const PrefillParams& p, int out_dtype, cudaStream_t stream);
+cudaError_t launch_tensor_core_prefill(const PrefillParams& p, int out_dtype, cudaStream_t stream);
+size_t tc_prefill_workspace_bytes(int Hk, int Hv, int n_seq, long long T);
+void tc_prefill_bind_workspace(PrefillParams& p);
 
 namespace {
 bool use_tensor_cores(int act_dtype, uint32_t flags) { return act_dtype == 1 && !(flags & kFlagForceSimt); }
 }  // namespace
 
-// The tensor-core path keeps, per chunk, the record of every v-head; a sequence
-// of L tokens has ceil(L/64) <= L/64 + 1 chunks, so T/64 + n_seq chunks bound
-// every packing of T tokens.
-size_t prefill_workspace_bytes(int, int Hv, int n_seq, long long T, int act_dtype, uint32_t flags) {
+size_t prefill_workspace_bytes(int Hk, int Hv, int n_seq, long long T, int act_dtype, uint32_t flags) {
     if (!use_tensor_cores(act_dtype, flags)) return 0;
-    const size_t nc = static_cast<size_t>((T + kChunk - 1) / kChunk) + static_cast<size_t>(n_seq);
-    return pf::table_bytes(n_seq) + nc * static_cast<size_t>(Hv) * pf::kVRec;
+    return tc_prefill_workspace_bytes(Hk, Hv, n_seq, T);
 }
 
 void prefill_bind_workspace(PrefillParams& p, int act_dtype) {
-    if (!use_tensor_cores(act_dtype, p.flags)) return;
-    uint8_t* base = static_cast<uint8_t*>(p.workspace);
-    p.chunk_base = reinterpret_cast<int*>(base);
-    p.ws_v = base + pf::table_bytes(p.n_seq);
+    if (use_tensor_cores(act_dtype, p.flags)) tc_prefill_bind_workspace(p);
 }
 
-namespace {
-
-// One stream per device, of the highest priority, for the state passes that
-// run beside the preparation kernel: created on first use and kept for the
-// life of the process (a stream created per call would put its creation on the
-// caller's timeline).
-cudaStream_t side_stream() {
-    static std::mutex mu;
-    static cudaStream_t streams[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!streams[dev]) {
-        int least = 0, greatest = 0;
-        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
-        cudaStream_t st = nullptr;
-        if (cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest) != cudaSuccess) return nullptr;
-        streams[dev] = st;
-    }
-    return streams[dev];
-}
-
-// From 64 chunks on, the chunk range is cut into two segments: the preparation
-// of the second runs on the caller's stream while the state pass of the first
-// runs on the side stream (the state pass is a serial chain on H_v SMs per
-// sequence, the preparation fills the others), and the state of each
-// (sequence, v-head) passes from one segment to the next through S.  Measured
-// at T = 8192 (128 chunks, 48 v-heads): one segment 0.95 ms, two 0.87 ms, four
-// 0.91 ms, eight 0.97 ms -- each further cut adds a pipeline ramp and a
-// partial wave to both kernels.
-cudaError_t launch_tensor_core_prefill(const PrefillParams& p, int out_dtype, cudaStream_t stream) {
-    cudaError_t e = launch_chunk_table(p, stream);
-    if (e != cudaSuccess) return e;
-    const int nc = p.n_chunks;
-    // a bf16 state is rounded once, at the end: no segment boundary that would store it mid-sequence
-    int nseg = nc >= 64 && !(p.flags & kFlagStateBf16) ? 2 : 1;
-    cudaStream_t side = nseg > 1 ? side_stream() : nullptr;
-    if (!side) nseg = 1;
-    if (nseg == 1) {
-        PrefillParams q = p;
-        q.chunk_lo = 0;
-        q.chunk_hi = nc;
-        if ((e = launch_chunk_prep(q, stream)) != cudaSuccess) return e;
-        return launch_state_pass(q, out_dtype, stream);
-    }
-    cudaEvent_t ev[3] = {};
-    for (int k = 0; k <= nseg && e == cudaSuccess; ++k) e = cudaEventCreateWithFlags(&ev[k], cudaEventDisableTiming);
-    bool side_used = false;   // work (or a wait) is queued on the side stream
-    for (int k = 0; k < nseg && e == cudaSuccess; ++k) {
-        PrefillParams q = p;
-        q.chunk_lo = static_cast<int>(static_cast<long long>(nc) * k / nseg);
-        q.chunk_hi = static_cast<int>(static_cast<long long>(nc) * (k + 1) / nseg);
-        if ((e = launch_chunk_prep(q, stream)) != cudaSuccess) break;
-        if ((e = cudaEventRecord(ev[k], stream)) != cudaSuccess) break;
-        if ((e = cudaStreamWaitEvent(side, ev[k], 0)) != cudaSuccess) break;
-        side_used = true;
-        e = launch_state_pass(q, out_dtype, side);
-    }
-    // Once anything is queued on the side stream, the caller's stream waits for
-    // it, on the error path too: a later call on the caller's stream must not
-    // overwrite records that a queued state pass still reads.  The first error
-    // is the one returned.
-    if (side_used) {
-        cudaError_t j = cudaEventRecord(ev[nseg], side);
-        if (j == cudaSuccess) j = cudaStreamWaitEvent(stream, ev[nseg], 0);
-        if (j != cudaSuccess) {
-            cudaStreamSynchronize(side);   // no event to order by: drain the side stream instead
-            if (e == cudaSuccess) e = j;
-        }
-    }
-    for (int k = 0; k <= nseg; ++k)
-        if (ev[k]) cudaEventDestroy(ev[k]);   // released once the recorded work completes
-    return e;
-}
-
-}  // namespace
-
-// bf16 activations take the tensor-core path (chunk table, chunk preparation,
-// state pass per (sequence, v-head), overlapped by segments as above); fp32
-// activations (whose 1e-5 tolerance needs fp32 products) take the CUDA-core
+// bf16 activations take the tensor-core path (chunk table, then one kernel
+// whose preparation and chain roles run side by side); fp32 activations (whose 1e-5 tolerance needs fp32 products) take the CUDA-core
 // kernel.  Either is followed by the conv-state update, which must run after
 // every CTA has read the old rows.
 cudaError_t launch_prefill(const PrefillParams& p, int act_dtype, int out_dtype, cudaStream_t stream) {

@@ -1,0 +1,186 @@
+// gdn_prefill_tc.cu -- the tensor-core chunked prefill (bf16 activations) as
+// one persistent kernel with two roles that run side by side:
+//   * preparation CTAs (gdn_prefill_prep.cuh) take (chunk, q/k head) items in
+//     chunk order from a global counter and write, for every v-head of the
+//     q/k head's group, the chunk's state-independent record (W^T, U, Q', K',
+//     P, decay vectors), then set the item's ready flag;
+//   * chain CTAs (gdn_prefill_chain.cuh) each walk the chunks of one
+//     (sequence, v-head) at a time, the state on chip, reading every record as
+//     soon as its flag is set -- while it is still in L2 -- and dropping it from
+//     L2 once consumed, so that records need not reach HBM.
+// Method: xwen CLAUDE.md page, "Ground truth" (chunk = 64 form of the delta
+// rule), "Architecture cheat sheet", "Gated DeltaNet layer".
+//
+// Chain CTAs wait on preparation CTAs (never the reverse), so the kernel is
+// launched cooperatively: every CTA is resident at once (one per SM at most,
+// by its shared memory), and every wait is bounded.
+#include "gdn_internal.h"
+#include "gdn_prefill_chain.cuh"
+#include "gdn_prefill_prep.cuh"
+
+namespace gdn {
+
+namespace {
+
+// Exclusive prefix of the per-sequence chunk counts: chunk_base[s] is the
+// global index of sequence s's first chunk, chunk_base[n_seq] the total.  Also
+// clears the ready flags [n_flags] and the item counter of this call.
+__global__ void chunk_table_kernel(const int* cu_seqlens, int n_seq, int* chunk_base, int* ready, int n_flags,
+                                   int* counter) {
+    __shared__ int carry_s;
+    __shared__ int warp_s[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    for (int i = tid; i < n_flags; i += blockDim.x) ready[i] = 0;
+    if (tid == 0) {
+        carry_s = 0;
+        *counter = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < n_seq; base += blockDim.x) {
+        const int i = base + tid;
+        const int cnt = i < n_seq ? (cu_seqlens[i + 1] - cu_seqlens[i] + kChunk - 1) / kChunk : 0;
+        int v = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int up = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += up;
+        }
+        if (lane == 31) warp_s[warp] = v;
+        __syncthreads();
+        if (warp == 0) {
+            int w = lane < nw ? warp_s[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int up = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += up;
+            }
+            if (lane < nw) warp_s[lane] = w;   // inclusive over warps
+        }
+        __syncthreads();
+        const int carry = carry_s;
+        const int incl = v + (warp > 0 ? warp_s[warp - 1] : 0) + carry;
+        if (i < n_seq) chunk_base[i] = incl - cnt;
+        __syncthreads();
+        if (tid == blockDim.x - 1) carry_s = incl;
+        __syncthreads();
+    }
+    if (tid == 0) chunk_base[n_seq] = carry_s;
+}
+
+constexpr int kThreads = chain::kStateThreads;
+static_assert(kThreads >= prep::kPrepThreads, "the preparation role needs 8 warps");
+
+__host__ __device__ inline uint32_t fused_smem(int G) {
+    return prep::smem_bytes(G) > chain::kStateSmem ? prep::smem_bytes(G) : chain::kStateSmem;
+}
+
+// CTAs [0, n_chain) run chains j = blockIdx.x, blockIdx.x + n_chain, ... of the
+// n_seq * H_v (sequence-major); the others take preparation items.
+template <typename Tout>
+__global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const PrefillParams p, int n_chain, int* counter) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    __shared__ int item_s;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    if (static_cast<int>(blockIdx.x) < n_chain) {
+        uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + chain::kBar + 8 * chain::kNumBars);
+        if (warp == 0) tc::tmem_alloc(tslot, chain::kTmemCols);
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        const uint32_t tmem = *tslot;
+        const int n_chains = p.n_seq * p.Hv;
+        for (int j = blockIdx.x; j < n_chains; j += n_chain) chain::run<Tout>(p, j / p.Hv, j % p.Hv, sm, tmem);
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (warp == 0) tc::tmem_dealloc(tmem, chain::kTmemCols);
+        return;
+    }
+    if (warp >= prep::kPrepThreads / 32) return;   // the preparation role runs on warps 0-7
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + prep::kMisc);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + prep::kMisc + 8);
+    int* err_s = reinterpret_cast<int*>(sm + prep::kMisc + 16);
+    if (warp == 0) tc::tmem_alloc(tslot, prep::kPrepTmemCols);
+    if (tid == 0) {
+        tc::mbar_init(mbar, 1);
+        *err_s = 0;
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tc::fence_before_sync();
+    pf::prep_sync();
+    tc::fence_after_sync();
+    prep::Ctx cx{*tslot, mbar, 0u, err_s};
+    const int n_items = p.n_chunks * p.Hk;
+    for (;;) {
+        // items in chunk order: every chain finds its next chunk among the earliest
+        if (tid == 0) item_s = atomicAdd(counter, 1);
+        pf::prep_sync();
+        const int it = item_s;   // read by all before thread 0 can write the next one (the item syncs first)
+        if (it >= n_items) break;
+        prep::item(p, it / p.Hk, it % p.Hk, sm, cx);
+    }
+    tc::fence_before_sync();
+    pf::prep_sync();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(cx.tmem, prep::kPrepTmemCols);
+}
+
+// Workspace layout: chunk table, ready flags, item counter, records.
+size_t flags_bytes(size_t n_chunks_bound, int Hk) { return (n_chunks_bound * Hk * 4 + 255) / 256 * 256; }
+
+}  // namespace
+
+// A sequence of L tokens has ceil(L/64) <= L/64 + 1 chunks, so T/64 + n_seq
+// chunks bound every packing of T tokens.
+size_t tc_prefill_workspace_bytes(int Hk, int Hv, int n_seq, long long T) {
+    const size_t nc = static_cast<size_t>((T + kChunk - 1) / kChunk) + static_cast<size_t>(n_seq);
+    return pf::table_bytes(n_seq) + flags_bytes(nc, Hk) + 256 + nc * static_cast<size_t>(Hv) * pf::kVRec;
+}
+
+void tc_prefill_bind_workspace(PrefillParams& p) {
+    const size_t nc = static_cast<size_t>((p.T + kChunk - 1) / kChunk) + static_cast<size_t>(p.n_seq);
+    uint8_t* base = static_cast<uint8_t*>(p.workspace);
+    p.chunk_base = reinterpret_cast<int*>(base);
+    base += pf::table_bytes(p.n_seq);
+    p.ready = reinterpret_cast<int*>(base);
+    base += flags_bytes(nc, p.Hk);
+    p.ws_v = base + 256;   // the item counter sits in the 256 bytes before the records
+}
+
+cudaError_t launch_tensor_core_prefill(const PrefillParams& p0, int out_dtype, cudaStream_t stream) {
+    PrefillParams p = p0;
+    p.chunk_lo = 0;
+    p.chunk_hi = p.n_chunks;
+    int* counter = reinterpret_cast<int*>(p.ws_v - 256);
+    chunk_table_kernel<<<1, 256, 0, stream>>>(p.cu_seqlens, p.n_seq, p.chunk_base, p.ready, p.n_chunks * p.Hk, counter);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int n_chains = p.n_seq * p.Hv;
+    const int n_items = p.n_chunks * p.Hk;
+    // One chain per CTA while the chains take at most half the SMs; beyond that, one
+    // v-head per chain CTA (every CTA then walks every sequence once), or a third of
+    // the SMs.  The preparation role takes the rest, and at least one SM.
+    int n_chain = n_chains <= sms / 2 ? n_chains : (p.Hv <= sms / 2 ? p.Hv : sms / 3);
+    n_chain = n_chain < 1 ? 1 : n_chain;
+    int n_prep = sms - n_chain;
+    if (n_prep > n_items) n_prep = n_items;
+    if (n_prep < 1) n_prep = 1;
+    const int grid = n_chain + n_prep;
+    const uint32_t smem = fused_smem(p.Hv / p.Hk);
+
+    auto go = [&](auto kernel) -> cudaError_t {
+        cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (r != cudaSuccess) return r;
+        int nc = n_chain;
+        void* args[] = {const_cast<PrefillParams*>(&p), &nc, &counter};
+        return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(kThreads), args, smem,
+                                           stream);
+    };
+    return out_dtype == 1 ? go(prefill_fused_kernel<__nv_bfloat16>) : go(prefill_fused_kernel<float>);
+}
+
+}  // namespace gdn

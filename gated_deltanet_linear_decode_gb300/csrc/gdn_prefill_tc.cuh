@@ -41,6 +41,37 @@ __host__ __device__ inline size_t table_bytes(int n_seq) {
     return (static_cast<size_t>(n_seq + 1) * 4 + 255) / 256 * 256;
 }
 
+// ---------------------------------------------------------------- role synchronisation
+// The preparation role runs on warps 0-7 of its CTA and meets at named barrier
+// 1 (the CTA's other warps have left), never at the CTA-wide barrier 0.
+__device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Ready flags: a release store by the producer after its records are written,
+// an acquire load by the consumer before it reads them.
+__device__ __forceinline__ void st_release(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Order this thread's generic-proxy accesses to global memory (the flag just
+// acquired) before its later async-proxy accesses (bulk copies of the records).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Drop one 128-byte line of a consumed record from L2 without writing it back.
+__device__ __forceinline__ void discard_l2(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+// Global timer (ns) for the long, time-bounded waits on ready flags.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
 // ---------------------------------------------------------------- small math
 __device__ __forceinline__ float conv4(float4 w, float x0, float x1, float x2, float cur) {
     return fmaf(w.w, cur, fmaf(w.z, x2, fmaf(w.y, x1, w.x * x0)));
@@ -125,7 +156,7 @@ __device__ __forceinline__ void mac16x2x4(const float* a0, const float* a1, cons
 // them as zero).  Hf is fp32 scratch for nine 16 x 16 blocks of row stride 20
 // (11520 bytes).  While threads 0-63 solve the diagonal blocks, threads
 // 64 .. kThreads-1 run side(i) with i = tid - 64 (work of the caller's that
-// needs no barrier of its own).  Ends with a block barrier.
+// needs no barrier of its own).  Ends with a barrier of the 256 threads.
 constexpr int kTS = 68;
 template <int kThreads, typename Side>
 __device__ void unit_lower_inverse(const float* Af, float* Tf, float* Hf, Side&& side) {
@@ -154,7 +185,7 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* Hf, Side&&
     } else {
         side(tid - 64);
     }
-    __syncthreads();
+    prep_sync();
     // scratch blocks: Ahat (1,0) (2,0) (2,1) (3,0) (3,1) (3,2) at 0..5; Q20, Q31, Q30 / R30 at 6..8
     auto hb = [&](int k) { return Hf + k * 16 * kHS; };
     auto ah = [](int i, int j) { return i * (i - 1) / 2 + j; };
@@ -183,7 +214,7 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* Hf, Side&&
         mac(tblk(i, i), kTS, Af + (16 * i) * kTS + 16 * j, kTS, acc);
         store(hb(k), kHS, acc, 1.f);
     }
-    __syncthreads();
+    prep_sync();
     // 3a. T10, T21, T32 and Q20, Q31, Q30
     if (tid < 6 * 32) {
         // Ahat block (i, j) times D_j: (1,0) (2,1) (3,2) give T blocks, (2,0) (3,1) (3,0) the Q sums
@@ -193,7 +224,7 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* Hf, Side&&
         if (k < 3) store(tblk(i, j), kTS, acc, -1.f);
         else store(hb(3 + k), kHS, acc, 1.f);
     }
-    __syncthreads();
+    prep_sync();
     // 3b. T20 = -(Q20 + Ahat21 T10), T31 = -(Q31 + Ahat32 T21), R30 = Q30 + Ahat31 T10
     if (tid < 3 * 32) {
         const int k = tid >> 5, i = k ? 3 : 2, kk = k == 1 ? 2 : 1, j = k == 1 ? 1 : 0;
@@ -203,7 +234,7 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* Hf, Side&&
         if (k < 2) store(tblk(i, j), kTS, acc, -1.f);
         else store(hb(8), kHS, acc, 1.f);
     }
-    __syncthreads();
+    prep_sync();
     // 3c. T30 = -(R30 + Ahat32 T20)
     if (tid < 32) {
         float acc[2][4];
@@ -211,7 +242,7 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* Hf, Side&&
         mac(hb(ah(3, 2)), kHS, tblk(2, 0), kTS, acc);
         store(tblk(3, 0), kTS, acc, -1.f);
     }
-    __syncthreads();
+    prep_sync();
 }
 
 }  // namespace pf
