@@ -30,6 +30,8 @@
 // timeout sets dev_status bit 4.
 #pragma once
 
+#include <type_traits>
+
 #include "gdn_internal.h"
 #include "gdn_prefill_tc.cuh"
 
@@ -48,9 +50,11 @@ constexpr uint32_t kKs = 32768;       // K' hi +0, lo +16384       (64 t x 128 i
 constexpr uint32_t kWs = 65536;       // W^T hi                   (128 i x 64 t, canonical 128 rows)
 constexpr uint32_t kPs = 81920;       // P hi +0, lo +8192         (64 t x 64 r, canonical 64 rows)
 constexpr int kOStride = 68;          // floats per v-row of the staged O (64 tokens + 4: no bank conflicts)
-constexpr uint32_t kOst = 98304;      // the chunk's O, fp32 [128 j][kOStride], for the token-major epilogue
-constexpr uint32_t kRs = kOst + 128 * kOStride * 4;   // per-token partial sums of O^2 [2][64] fp32
-constexpr uint32_t kNw = kRs + 512;   // norm_w [128] fp32
+constexpr uint32_t kOstBytes = 128 * kOStride * 4;
+constexpr uint32_t kOst = 98304;      // O of chunks c & 1 = 0, 1: fp32 [2][128 j][kOStride], staged for the outputs
+constexpr uint32_t kRs = kOst + 2 * kOstBytes;   // per-token partial sums of O^2 [2][64] fp32
+constexpr uint32_t kRS = kRs + 512;   // per-token norm factor of chunks c & 1 = 0, 1: [2][64] fp32
+constexpr uint32_t kNw = kRS + 512;   // norm_w [128] fp32
 constexpr uint32_t kBar = kNw + 512;  // mbarriers, then the TMEM base and the error flag
 constexpr uint32_t kUs = (kBar + 176 + 127) / 128 * 128;   // the chunk's U, e^Gam, e^{Gam_last-Gam} (record tail)
 constexpr uint32_t kUBytes = pf::kVRec - pf::kRecU;          // 33280
@@ -64,7 +68,8 @@ enum : int {
     kODone0, kODone1,                  // O of even / odd chunks complete
     kSReady, kDReady,                  // converters wrote the S / D operands (256 arrivals)
     kEpi0, kEpi1,                      // epilogue done with the O buffer of even / odd chunks (128 arrivals)
-    kESync,                            // the epilogue warps' own barrier (128 arrivals, once per use)
+    kOutRdy0, kOutRdy1,                // staged O and norm factors of even / odd chunks ready (128 arrivals)
+    kOutFree0, kOutFree1,              // converters done with the staged O of even / odd chunks (256 arrivals)
     kDrain,                            // error path: every MMA issued so far retired
     kNever,                            // test stall: nothing arrives
     kNumBars
@@ -115,7 +120,8 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t cnt = 1;
             if (i == kSReady || i == kDReady) cnt = kConvThreads;
-            if (i == kEpi0 || i == kEpi1 || i == kESync) cnt = kEpiThreads;
+            if (i == kEpi0 || i == kEpi1 || i == kOutRdy0 || i == kOutRdy1) cnt = kEpiThreads;
+            if (i == kOutFree0 || i == kOutFree1) cnt = kConvThreads;
             asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bars + i)) : "memory");
             tc::mbar_init(bars + i, cnt);
         }
@@ -127,11 +133,11 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
     tc::fence_after_sync();
 
     // Bounded wait that also gives up as soon as another role has timed out.
-    // Converter and epilogue warps back off with short sleeps so that waiting
-    // warps leave the issue slots to the working ones (the converters, on the
-    // state chain, sleep at most 64 ns); the control and copy lanes poll.
+    // Converter and epilogue warps back off with short sleeps (at most 64 ns) so
+    // that waiting warps leave the issue slots to the working ones; the control
+    // and copy lanes poll.
     const bool sleepy = warp != kCtrlWarp && warp != kCopyWarp;
-    const uint32_t sleep_cap = warp < kConvWarps ? 64u : 256u;
+    const uint32_t sleep_cap = 64u;
     auto wait = [&](int bar, uint32_t parity) -> bool {
         uint32_t ns = 32;
         for (int it = 0; it < kWaitLimit; it += 8) {
@@ -154,12 +160,12 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
     auto wait_ready = [&](int c) -> bool {
         const int* f = ready + static_cast<size_t>(c) * p.Hk;
         if (pf::ld_acquire(f)) return true;
-        const uint64_t t0 = pf::global_ns();
+        const uint64_t tstart = pf::global_ns();
         uint32_t ns = 64;
         for (;;) {
             if (pf::ld_acquire(f)) return true;
             if (*err_s) return false;
-            if (pf::global_ns() - t0 > kReadyTimeoutNs) {
+            if (pf::global_ns() - tstart > kReadyTimeoutNs) {
                 *err_s = 1;
                 return false;
             }
@@ -167,6 +173,50 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
             ns = min(ns * 2, 2048u);
         }
     };
+
+    // Gated RMSNorm outputs of chunk cc for token tt_ and v-rows v0 .. v0 + 8 NG - 1, from
+    // the chunk's staged O and norm factor (buffers cc & 1).  zq holds the matching z (16
+    // bytes per group of 8, from load_z).  The epilogue warps write v-rows 0-63 of every
+    // chunk, the converter warps v-rows 64-127 (one chunk later, in their idle time).
+    const float* nw_s = reinterpret_cast<const float*>(sm + kNw);
+    const __nv_bfloat16* zbase = static_cast<const __nv_bfloat16*>(p.z) + h * kD;
+    auto load_z = [&](int cc, int tt_, int v0, auto ngc, uint4* zq) {
+        constexpr int NG = decltype(ngc)::value;
+        const bool valid = cc < nch && cc * kChunk + tt_ < L;
+        const uint4* src = reinterpret_cast<const uint4*>(zbase + static_cast<size_t>(t0 + cc * kChunk + tt_) * HvD + v0);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) zq[g] = valid ? __ldg(src + g) : make_uint4(0, 0, 0, 0);
+    };
+    auto outputs = [&](int cc, int tt_, int v0, auto ngc, const uint4* zq, bool& bad_out) {
+        constexpr int NG = decltype(ngc)::value;
+        if (cc * kChunk + tt_ >= L) return;
+        const size_t rowt = static_cast<size_t>(t0 + cc * kChunk + tt_);
+        const float rs = reinterpret_cast<const float*>(sm + kRS)[(cc & 1) * 64 + tt_];
+        const float* oc = reinterpret_cast<const float*>(sm + kOst + (cc & 1) * kOstBytes) + tt_;
+        Tout* op = static_cast<Tout*>(p.out) + rowt * HvD + h * kD + v0;
+        float* pp = p.prenorm ? p.prenorm + rowt * HvD + h * kD + v0 : nullptr;
+        const bool check = (p.flags & kFlagCheckFinite) != 0;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            float zf[8], o[8], y[8];
+            pf::bf16x8_to_f32(zq[g], zf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                o[i] = oc[(v0 + 8 * g + i) * kOStride];
+                y[i] = o[i] * rs * nw_s[v0 + 8 * g + i] * pf::silu_fast(zf[i]);
+                if (check) bad_out |= nonfinite_bits(y[i]);
+            }
+            pf::st_out8(op + 8 * g, y);
+            if (pp)
+#pragma unroll
+                for (int i = 0; i < 8; i += 4)
+                    *reinterpret_cast<float4*>(pp + 8 * g + i) = make_float4(
+                        o[i] * kInvSqrtD, o[i + 1] * kInvSqrtD, o[i + 2] * kInvSqrtD, o[i + 3] * kInvSqrtD);
+        }
+    };
+    using G2 = std::integral_constant<int, 2>;
+    using G4 = std::integral_constant<int, 4>;
+    bool bad_out = false;   // a non-finite output (GDN_FLAG_CHECK_FINITE)
 
     // ---- initial state into tensor memory (converter warps; lane j = row j)
     const int quarter = warp & 3;
@@ -305,11 +355,24 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
             if (req_u) tc::mbar_wait(bars + kLdU, (req_u - 1) & 1, kWaitLimit);
         }
     } else if (warp < kConvWarps) {
-        // ================= converters: thread = v-row j (lane quarter) x column half
+        // ================= converters: thread = v-row j (lane quarter) x column half; after
+        // each D conversion, the outputs of the previous chunk's v-rows 64-127 (thread =
+        // token tid % 64, v-rows 64 + 16 (tid / 64) ..)
         const int chalf = warp >> 2;
+        const int ot = tid & 63, ov = 64 + 16 * (tid >> 6);
+        uint4 zq[2];
+        // outputs of chunk cc (its O and norm factors staged by the epilogue warps), then the
+        // staged O buffer is handed back
+        auto outputs_prev = [&](int cc) -> bool {
+            if (!wait(kOutRdy0 + (cc & 1), (cc >> 1) & 1)) return false;
+            outputs(cc, ot, ov, G2{}, zq, bad_out);
+            tc::mbar_arrive(bars + kOutFree0 + (cc & 1));
+            return true;
+        };
         bool ok = true;
         for (int c = 0; c < nch && ok; ++c) {
             const uint32_t pc = c & 1;
+            if (c > 0) load_z(c - 1, ot, ov, G2{}, zq);   // used after this chunk's D conversion
             // this chunk's U^T entries (used after the S conversion) and e^{Gam_last}, copied
             // into shared memory with the chunk's tiles (the buffer is refilled once every
             // converter has passed the S conversion, i.e. after Dacc is issued)
@@ -361,6 +424,11 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
             tc::tmem_wait_st();
             tc::fence_before_sync();
             tc::mbar_arrive(bars + kDReady);
+            if (c > 0 && !(ok = outputs_prev(c - 1))) break;
+        }
+        if (ok && nch > 0) {   // the last chunk's outputs
+            load_z(nch - 1, ot, ov, G2{}, zq);
+            ok = outputs_prev(nch - 1);
         }
         // final state out (after the last update)
         if (ok && nch > 0) ok = wait(kMmaS, (nch - 1) & 1);
@@ -386,37 +454,43 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
             }
         }
     } else {   // warps kConvWarps .. kConvWarps + kEpiWarps - 1
-        // ================= epilogue
+        // ================= epilogue: per chunk, O row j -> staged O (shared memory, buffer
+        // c & 1; the tensor-memory O buffer is then free), the per-token norm factors, and
+        // the outputs of v-rows 0-63 (thread = token tt, v-rows 32 jh ..); the converters
+        // write v-rows 64-127 from the same staged O
         const int eq = warp - kConvWarps;   // lane quarter
         const int j = eq * 32 + lane, e = tid - kConvThreads;
-        const int tt = e & 63, jh = e >> 6;   // token-major part: token tt, v-rows 64 jh ..
+        const int tt = e & 63, jh = e >> 6;
         const uint32_t te = tmem + (static_cast<uint32_t>(eq * 32) << 16);
-        float* Ost = reinterpret_cast<float*>(sm + kOst);
         float* Rs = reinterpret_cast<float*>(sm + kRs);
-        float* nw = reinterpret_cast<float*>(sm + kNw);
-        nw[e] = p.norm_w[e];
-        const __nv_bfloat16* zh = static_cast<const __nv_bfloat16*>(p.z) + h * kD + 64 * jh;
-        const bool check = (p.flags & kFlagCheckFinite) != 0;
-        uint32_t es_phase = 0;
-        auto epi_sync = [&]() -> bool {   // bounded barrier of the 128 epilogue threads
-            tc::mbar_arrive(bars + kESync);
-            const bool r = wait(kESync, es_phase);
-            es_phase ^= 1u;
-            return r;
+        float* RS = reinterpret_cast<float*>(sm + kRS);
+        reinterpret_cast<float*>(sm + kNw)[e] = p.norm_w[e];
+        // The 128 epilogue threads meet at named barrier 2 (no sleeping waits on the
+        // output path).  The waits that can give up are followed by a vote at that
+        // barrier, so every epilogue thread takes the same decision and none is left
+        // waiting at a later barrier.
+        auto epi_sync = [&]() { asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory"); };
+        auto epi_all = [&](bool good) -> bool {   // barrier + "every thread passed good"
+            uint32_t any_bad;
+            asm volatile(
+                "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\tbar.red.or.pred q, 2, %2, p;\n\t"
+                "selp.u32 %0, 1, 0, q;\n\t}"
+                : "=r"(any_bad)
+                : "r"(good ? 1u : 0u), "n"(kEpiThreads)
+                : "memory");
+            return any_bad == 0;
         };
-        bool ok = epi_sync();   // norm_w staged
+        epi_sync();   // norm_w staged
+        bool ok = true;
+        uint4 zq[4];
         for (int c = 0; c < nch && ok; ++c) {
-            const uint32_t b = c & 1;   // O buffer
-            const int c0 = c * kChunk, n = min(kChunk, L - c0);
-            const bool valid = tt < n;
-            const size_t rowt = static_cast<size_t>(t0 + c0 + tt);
-            // this thread's z (token tt, v-rows 64 jh ..): 128 bytes, loaded ahead of the wait
-            uint4 zq[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                zq[k] = valid ? __ldg(reinterpret_cast<const uint4*>(zh + rowt * HvD) + k) : make_uint4(0, 0, 0, 0);
-            if (!(ok = wait(kODone0 + b, (c >> 1) & 1))) break;
+            const uint32_t b = c & 1;   // O buffers (tensor memory and staged)
+            load_z(c, tt, 32 * jh, G4{}, zq);
+            // O of chunk c complete, and the converters done with the staged O of chunk c - 2
+            const bool got = wait(kODone0 + b, (c >> 1) & 1) && (c < 2 || wait(kOutFree0 + b, ((c - 2) >> 1) & 1));
+            if (!(ok = epi_all(got))) break;
             tc::fence_after_sync();
+            float* Ost = reinterpret_cast<float*>(sm + kOst + b * kOstBytes);
             {   // O row j (64 tokens) -> registers -> shared memory; the O buffer is then free
                 float v[32];
 #pragma unroll
@@ -430,39 +504,20 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
             }
             tc::fence_before_sync();
             tc::mbar_arrive(bars + kEpi0 + b);
-            if (!(ok = epi_sync())) break;   // O staged
+            epi_sync();   // O staged
             // token-major: partial sum of O^2 over v-rows 64 jh .. of token tt
             const float* oc = Ost + 64 * jh * kOStride + tt;
             float ss = 0.f;
 #pragma unroll 16
             for (int r = 0; r < 64; ++r) ss = fmaf(oc[r * kOStride], oc[r * kOStride], ss);
             Rs[jh * 64 + tt] = ss;
-            if (!(ok = epi_sync())) break;   // partial sums written
-            // o = O / sqrt(128); y = o / sqrt(mean(o^2) + eps) * norm_w * silu(z)
-            const float rs =
-                rsqrtf((Rs[tt] + Rs[64 + tt]) * (kInvSqrtD * kInvSqrtD / kD) + p.eps) * kInvSqrtD;
-            if (valid) {
-                Tout* op = static_cast<Tout*>(p.out) + rowt * HvD + h * kD + 64 * jh;
-                float* pp = p.prenorm ? p.prenorm + rowt * HvD + h * kD + 64 * jh : nullptr;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    float zf[8], o[8], y[8];
-                    pf::bf16x8_to_f32(zq[k], zf);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        o[i] = oc[(8 * k + i) * kOStride];
-                        y[i] = o[i] * rs * nw[64 * jh + 8 * k + i] * pf::silu_fast(zf[i]);
-                        if (check) bad |= nonfinite_bits(y[i]);
-                    }
-                    pf::st_out8(op + 8 * k, y);
-                    if (pp)
-#pragma unroll
-                        for (int i = 0; i < 8; i += 4)
-                            *reinterpret_cast<float4*>(pp + 8 * k + i) = make_float4(
-                                o[i] * kInvSqrtD, o[i + 1] * kInvSqrtD, o[i + 2] * kInvSqrtD, o[i + 3] * kInvSqrtD);
-                }
-            }
-            if (!(ok = epi_sync())) break;   // every thread is done with the staged O and the partial sums
+            epi_sync();   // partial sums written
+            // o = O / sqrt(128); y = o / sqrt(mean(o^2) + eps) * norm_w * silu(z): the factor
+            // 1 / sqrt(mean(o^2) + eps) / sqrt(128) of token tt, for both output halves
+            if (jh == 0) RS[b * 64 + tt] = rsqrtf((Rs[tt] + Rs[64 + tt]) * (kInvSqrtD * kInvSqrtD / kD) + p.eps) * kInvSqrtD;
+            epi_sync();   // norm factors written; Rs may be reused by the next chunk
+            tc::mbar_arrive(bars + kOutRdy0 + b);   // the converters may read the staged O and RS
+            outputs(c, tt, 32 * jh, G4{}, zq, bad_out);
         }
     }
 
@@ -470,7 +525,8 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
     __syncthreads();
     if (p.dev_status) {
         int st = 0;
-        if (p.flags & kFlagCheckFinite) st = __any_sync(0xffffffffu, bad) ? (warp < kConvWarps ? 1 : 2) : 0;
+        if (p.flags & kFlagCheckFinite)
+            st = (__any_sync(0xffffffffu, bad) ? 1 : 0) | (__any_sync(0xffffffffu, bad_out) ? 2 : 0);
         if (tid == 0 && *err_s) st |= 16;
         if (lane == 0 && st) atomicOr(p.dev_status + s * Hv + h, st);
     }
