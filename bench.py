@@ -7,8 +7,9 @@ A step is one pass of the whole hot path over one batch of synthetic input:
   * decode: B=64 sequences, one token each, H_k=16 / H_v=32, bf16, fp32 state
     updated in place (gdn_decode_step);
   * speculative verify: the same B=64 sequences, K=3 tokens each, with
-    per-position checkpoints (gdn_verify_k), then gdn_commit of a seeded
-    accept length in {1,2,3}.
+    per-position checkpoints on a state ring (gdn_verify_k_ring), then
+    gdn_commit_ring of a seeded accept length in {1,2,3} (the accepted
+    checkpoint becomes the live state where it lies; only conv rows move).
 value = tokens processed per second over the step (8192 + 64 + 192 tokens);
 the per-part figures (tokens/s, ms, roofline) are under "parts".
 
@@ -49,8 +50,9 @@ import gdn_inputs  # noqa: E402
 
 METRIC = "GDN layer tokens/s: prefill T=8192 & decode B=64; % of roofline"
 WORKLOAD = ("prefill T=8192 H_k=16 H_v=48 bf16 (chunk 64) + decode B=64 H_k=16 H_v=32 bf16 "
-            "+ verify B=64 K=3 + commit")
+            "+ verify B=64 K=3 + commit (state ring)")
 L2_FLUSH_BYTES = 256 << 20
+TOKENS_PER_STEP = 8192 + 64 + 64 * 3   # prefill T + decode B + verify B * K
 
 
 # ------------------------------------------------------------------ algorithmic work
@@ -245,10 +247,8 @@ class Workload:
         g, i = self.gdn, self.p_in
         g.gdn_prefill_chunked(self.p_dims, self.p_w, self.cu_h, self.cu_d, i["x"], i["z"], i["a_raw"], i["b_raw"],
                               self.p_conv, self.p_S, self.p_out, zero_init=True, workspace=self.p_ws)
-        # chunk table + (preparation + state pass) per segment + conv-state update; the library cuts
-        # n chunks into two segments from n = 64 on
-        n = int(((self.cu_h[1:] - self.cu_h[:-1] + 63) // 64).sum())
-        return 2 + 2 * (2 if n >= 64 else 1)
+        # chunk table, the prefill kernel (preparation and chain roles side by side), conv-state update
+        return 3
 
     def decode(self):
         g, i = self.gdn, self.d_in
@@ -256,12 +256,23 @@ class Workload:
                           self.d_out)
         return 1
 
-    def verify(self):
+    def verify_copy(self):
+        """Verify + commit on plain states (the accepted checkpoint is copied back)."""
         g, i = self.gdn, self.v_in
         g.gdn_verify_k(self.d_dims, self.d_w, self.vc.K, i["x"], i["z"], i["a_raw"], i["b_raw"], self.d_conv,
                        self.d_S, self.v_ckc, self.v_ckS, self.v_out)
         g.gdn_commit(self.d_dims, self.vc.K, self.acc, self.v_ckc, self.v_ckS, self.d_conv, self.d_S)
         return 2
+
+    def verify_only(self):
+        g, i = self.gdn, self.v_in
+        g.gdn_verify_k(self.d_dims, self.d_w, self.vc.K, i["x"], i["z"], i["a_raw"], i["b_raw"], self.d_conv,
+                       self.d_S, self.v_ckc, self.v_ckS, self.v_out)
+        return 1
+
+    def verify(self):
+        """The step's verify: verify walk + commit on the state ring (the commit moves no state)."""
+        return self.verify_ring()
 
     def verify_ring(self):
         g, i = self.gdn, self.v_in
@@ -343,23 +354,29 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
 
-    # outside the step: the verify + commit pair on a state ring, where the commit moves no state
-    ring_ms = []
-    for it in range(args.warmup + max(1, args.steps)):
-        wl.flush_l2()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        wl.verify_ring()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if it >= args.warmup:
-            ring_ms.append(e0.elapsed_time(e1))
+    # outside the step: the verify walk alone, and verify + commit on plain states (the commit copies the
+    # accepted checkpoint back)
+    def timed_alone(fn):
+        ms = []
+        for it in range(args.warmup + max(1, args.steps)):
+            wl.flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= args.warmup:
+                ms.append(e0.elapsed_time(e1))
+        return statistics.mean(ms)
+    only_ms = timed_alone(wl.verify_only)
+    copy_ms = timed_alone(wl.verify_copy)
 
     tot_ms = sum(step_ms)
     tot_ms = _max_over_ranks(tot_ms, world)
     e2e_tot = _max_over_ranks(sum(e2e_ms), world)
     pc, dc, vc = wl.pc, wl.dc, wl.vc
     tok_step = pc.T + dc.N + vc.N * vc.K
+    assert tok_step == TOKENS_PER_STEP
     value = world * tok_step * args.steps / (tot_ms / 1e3)
     hbm, tf, peak_src = peaks()
     pm = statistics.mean(parts["prefill"])
@@ -377,12 +394,15 @@ def run_gpu(args, rank, world):
               "frac": db / (dm / 1e3) / 1e9 / hbm, "traffic": traffic.get("decode"), "algorithmic_bytes": db,
               "peak_source": peak_src}
     v_roof = {"bound": "hbm", "achieved": vb / (vm / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
-              "frac": vb / (vm / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes_verify_only": vb,
-              "note": "time includes the commit copy"}
-    rm = statistics.mean(ring_ms)
-    r_roof = {"bound": "hbm", "achieved": vb / (rm / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
-              "frac": vb / (rm / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes": vb,
-              "note": "ring commit: conv rows and slot index only; timed outside the step"}
+              "frac": vb / (vm / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes": vb,
+              "note": "verify walk + commit on the state ring (conv rows and slot index only)"}
+    o_roof = {"bound": "hbm", "achieved": vb / (only_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+              "frac": vb / (only_ms / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes": vb,
+              "note": "verify walk alone, timed outside the step"}
+    c_roof = {"bound": "hbm", "achieved": vb / (copy_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+              "frac": vb / (copy_ms / 1e3) / 1e9 / hbm, "traffic": None, "algorithmic_bytes_verify_only": vb,
+              "note": "verify + commit on plain states (the commit copies the accepted checkpoint); "
+                      "timed outside the step"}
     dominant = max((pm, "prefill", p_roof), (dm, "decode", d_roof), (vm, "verify", v_roof))[1:]
     h2d, d2h = wl.io_bytes()
     line = {
@@ -390,14 +410,15 @@ def run_gpu(args, rank, world):
         "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 (bf16 activations in/out, fp32 state)",
         "data": "synthetic (seeded; no weights or dataset)",
-        "config": {"workload": WORKLOAD, "tokens_per_step": tok_step, "l2": "flushed (256 MiB write) before each "
-                   "timed step; inputs also exceed L2", "parallelism": f"replicas x{world}"},
+        "config": step_config(world),
         "roofline": {**dominant[1], "kernel": dominant[0]},
         "parts": {
             "prefill_T8192": {"tokens_per_s": pc.T / (pm / 1e3), "ms": pm, "roofline": p_roof},
             "decode_B64": {"tokens_per_s": dc.N / (dm / 1e3), "ms": dm, "roofline": d_roof},
-            "verify_B64_K3_commit": {"tokens_per_s": vc.N * vc.K / (vm / 1e3), "ms": vm, "roofline": v_roof},
-            "verify_B64_K3_commit_ring": {"tokens_per_s": vc.N * vc.K / (rm / 1e3), "ms": rm, "roofline": r_roof},
+            "verify_B64_K3_commit_ring": {"tokens_per_s": vc.N * vc.K / (vm / 1e3), "ms": vm, "roofline": v_roof},
+            "verify_B64_K3_alone": {"tokens_per_s": vc.N * vc.K / (only_ms / 1e3), "ms": only_ms, "roofline": o_roof},
+            "verify_B64_K3_commit_copy": {"tokens_per_s": vc.N * vc.K / (copy_ms / 1e3), "ms": copy_ms,
+                                          "roofline": c_roof},
         },
         "e2e": {"value": world * tok_step * len(e2e_ms) / (e2e_tot / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -598,69 +619,96 @@ def _max_over_ranks(v, world):
 
 
 # ------------------------------------------------------------------ the oracle (CPU)
-def oracle_step(cases, prefill_tokens=None):
+def oracle_step(cases, prefill_tokens=None, n_threads=0):
     """One step of the workload through the CPU oracle (fp64, OpenMP): the
-    prefill (all 48 heads; its first `prefill_tokens` tokens when given), the
-    B=64 decode step and the B=64 K=3 verify walk with checkpoints.
-    Returns (seconds used, seconds extrapolated to the whole step)."""
+    prefill (all 48 heads; only its first `prefill_tokens` tokens when given),
+    the B=64 decode step and the B=64 K=3 verify walk with checkpoints.
+    Returns the seconds of (prefill, decode, verify)."""
     import oracle
     pc, dc, vc = cases
     n = pc.T if prefill_tokens is None else prefill_tokens
     t0 = time.perf_counter()
     oracle.forward(pc.Hk, pc.Hv, pc.x[:n], pc.z[:n], pc.a_raw[:n], pc.b_raw[:n], pc.conv_w, pc.dt_bias, pc.ssm_a,
-                   pc.norm_w, pc.conv0, pc.S0, cu_seqlens=[0, n])
+                   pc.norm_w, pc.conv0, pc.S0, cu_seqlens=[0, n], n_threads=n_threads)
     t1 = time.perf_counter()
     oracle.forward(dc.Hk, dc.Hv, dc.x, dc.z, dc.a_raw, dc.b_raw, dc.conv_w, dc.dt_bias, dc.ssm_a, dc.norm_w,
-                   dc.conv0, dc.S0, cu_seqlens=np.arange(dc.N + 1))
+                   dc.conv0, dc.S0, cu_seqlens=np.arange(dc.N + 1), n_threads=n_threads)
     t2 = time.perf_counter()
     oracle.verify_checkpoints(vc.Hk, vc.Hv, vc.x, vc.z, vc.a_raw, vc.b_raw, vc.conv_w, vc.dt_bias, vc.ssm_a,
-                              vc.norm_w, vc.conv0, vc.S0, vc.K)
+                              vc.norm_w, vc.conv0, vc.S0, vc.K, n_threads=n_threads)
     t3 = time.perf_counter()
-    return t3 - t0, (t1 - t0) * pc.T / n + (t2 - t1) + (t3 - t2)
+    return t1 - t0, t2 - t1, t3 - t2
+
+
+def host_cores():
+    """CPU cores this process may run on, and the oracle's OpenMP thread count."""
+    import oracle
+    return len(os.sched_getaffinity(0)), oracle.max_threads()
+
+
+def single_thread_rates(cases, prefill_tokens=256):
+    """The oracle on one thread, per part of the step: the B=64 decode and the
+    B=64 K=3 verify whole, the prefill on its first `prefill_tokens` tokens."""
+    pc, dc, vc = cases
+    tp, td, tv = oracle_step(cases, prefill_tokens, n_threads=1)
+    return {"prefill_tokens_per_s": prefill_tokens / tp, "decode_tokens_per_s": dc.N / td,
+            "verify_tokens_per_s": vc.N * vc.K / tv,
+            "sample": f"one thread: prefill tokens 0..{prefill_tokens - 1} of T=8192 (48 heads), the whole B=64 "
+                      f"decode, the whole B=64 K=3 verify"}
 
 
 def cpu_baseline(min_seconds=10.0):
     """The oracle, as it stands, on the host cores: whole steps of the workload,
-    repeated until at least `min_seconds` of CPU work."""
+    repeated until at least `min_seconds` of CPU work; and its single-thread
+    rates on a bounded sample."""
     import oracle
     oracle.build()
     cases = (gdn_inputs.prefill_t8192(), gdn_inputs.decode_b64(), gdn_inputs.verify_b64_k3())
     tok = cases[0].T + cases[1].N + cases[2].N * cases[2].K
     reps, used = 0, 0.0
     while used < min_seconds or reps == 0:
-        u, _ = oracle_step(cases)
-        used += u
+        used += sum(oracle_step(cases))
         reps += 1
-    return {"value": tok * reps / used, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+    cores, omp = host_cores()
+    return {"value": tok * reps / used, "unit": "tokens/s", "cores": omp, "cores_available": cores,
+            "kind": "oracle",
             "sample": f"fp64 C oracle, whole steps of the workload (prefill T=8192 all 48 heads + B=64 decode + "
-                      f"B=64 K=3 verify) x{reps}, {used:.1f} s of CPU work", "seconds": used}
+                      f"B=64 K=3 verify) x{reps}, {used:.1f} s of CPU work, {omp} OpenMP threads on {cores} cores",
+            "seconds": used, "single_thread": single_thread_rates(cases)}
+
+
+def step_config(world):
+    """The workload description both arms print."""
+    return {"workload": WORKLOAD, "tokens_per_step": TOKENS_PER_STEP,
+            "l2": "flushed (256 MiB write) before each timed step; inputs also exceed L2",
+            "parallelism": f"replicas x{world}"}
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle as it stands on the host cores, timing
+    whole steps of the workload (no extrapolation)."""
     if rank != 0:
         return None
     import oracle
     oracle.build()
     cases = (gdn_inputs.prefill_t8192(), gdn_inputs.decode_b64(), gdn_inputs.verify_b64_k3())
     tok = cases[0].T + cases[1].N + cases[2].N * cases[2].K
-    n = 512
     for _ in range(args.warmup):
-        oracle_step(cases, n)
-    fulls, used = [], 0.0
-    for _ in range(args.steps):
-        u, f = oracle_step(cases, n)
-        fulls.append(f)
-        used += u
-    tot = sum(fulls)
-    value = tok * len(fulls) / tot
+        oracle_step(cases)
+    times = [sum(oracle_step(cases)) for _ in range(args.steps)]
+    tot = sum(times)
+    value = tok * len(times) / tot
+    cores, omp = host_cores()
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(fulls),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "tokens_per_step": tok},
-        "cpu_baseline": {"kind": "oracle", "cores": oracle.max_threads(), "value": value, "unit": "tokens/s",
-                         "sample": f"each step: prefill tokens 0..{n - 1} of T=8192 scaled by 8192/{n}, full B=64 "
-                                   f"decode, full B=64 K=3 verify ({used:.1f} s of CPU work in total)"},
+        "data": "synthetic (seeded; no weights or dataset)", "config": step_config(world),
+        "cpu_baseline": {"kind": "oracle", "cores": omp, "cores_available": cores, "value": value,
+                         "unit": "tokens/s",
+                         "sample": f"whole steps of the workload (prefill T=8192 all 48 heads + B=64 decode + B=64 K=3 "
+                                   f"verify), {args.steps} timed after {args.warmup} untimed, {omp} OpenMP threads on "
+                                   f"{cores} cores"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
