@@ -195,11 +195,14 @@ class ClockSampler:
 class Workload:
     """Device-resident inputs/outputs of one step, plus pinned host copies for e2e."""
 
-    def __init__(self, device):
+    def __init__(self, device, prefill_tokens=8192):
         import gated_deltanet_linear_decode_gb300 as gdn
         self.gdn = gdn
         dev = device
-        self.pc = gdn_inputs.prefill_t8192()
+        # the prefill workload (a shorter sequence of the same shape only for profiling runs)
+        self.pc = (gdn_inputs.prefill_t8192() if prefill_tokens == 8192 else
+                   gdn_inputs.make_case(f"prefill T={prefill_tokens} Hk=16 Hv=48 bf16", Hk=16, Hv=48,
+                                        lengths=[prefill_tokens], S0="zero", conv0="zero", seed=1002))
         self.dc = gdn_inputs.decode_b64()
         self.vc = gdn_inputs.verify_b64_k3()
         pc, dc, vc = self.pc, self.dc, self.vc
@@ -594,7 +597,7 @@ def run_part(args):
     """Warm-up then timed launches of one part only (profiling aid)."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    wl = Workload(dev)
+    wl = Workload(dev, args.prefill_tokens)
     fn = {"prefill": wl.prefill, "decode": wl.decode, "verify": wl.verify}[args.only]
     for _ in range(args.warmup + args.steps):
         wl.flush_l2()
@@ -722,6 +725,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the batch-1 graph decode and the varlen T=65536 prefill (timed outside the step)")
+    ap.add_argument("--prefill-tokens", type=int, default=8192,
+                    help="with --only prefill: the sequence length (a smaller case for profiling)")
     ap.add_argument("--only", choices=["prefill", "decode", "verify"], default=None,
                     help="run only one part of the step (for profiling); no JSON line")
     args = ap.parse_args()

@@ -106,6 +106,9 @@ struct PrefillParams {
     int* chunk_base;         // device [n_seq+1]
     uint8_t* ws_v;           // v-head records, [n_chunks][Hv]
     int* ready;              // [n_chunks][Hk] ready flags of the records (zeroed per call)
+    int* consumed;           // [n_chunks][Hk] chains of the group done with the chunk's records (zeroed per call)
+    int ahead;               // the preparation role writes chunk c once chunk c - ahead is consumed
+    int* abort_flag;         // set by a chain that gave up: the preparation role stops waiting on chains
 };
 
 // Workspace bytes of gdn_prefill_chunked for the path that act_dtype / flags select.

@@ -344,9 +344,13 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
             }
             if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
             discard(c);
+            if (lane == 0) pf::red_release_add(p.consumed + static_cast<size_t>(cbase + c) * p.Hk + kh, 1);   // done with chunk c
         }
         if (lane == 0 && ok && nch > 0) ok = wait(kODone0 + ((nch - 1) & 1), ((nch - 1) >> 1) & 1);
-        if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && nch > 0) discard(nch - 1);
+        if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && nch > 0) {
+            discard(nch - 1);
+            if (lane == 0) pf::red_release_add(p.consumed + static_cast<size_t>(cbase + nch - 1) * p.Hk + kh, 1);
+        }
         if (lane == 0 && !ok) {   // error path: let every issued copy land before the CTA moves on
             if (req_w) tc::mbar_wait(bars + kLdW, (req_w - 1) & 1, kWaitLimit);
             if (req_q) tc::mbar_wait(bars + kLdQ, (req_q - 1) & 1, kWaitLimit);
@@ -523,6 +527,7 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
 
     tc::fence_before_sync();
     __syncthreads();
+    if (tid == 0 && *err_s) atomicExch(p.abort_flag, 1);   // no preparation CTA waits on this chain any more
     if (p.dev_status) {
         int st = 0;
         if (p.flags & kFlagCheckFinite)

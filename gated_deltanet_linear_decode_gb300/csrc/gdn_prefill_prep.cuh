@@ -56,6 +56,7 @@ static_assert(kAf + 64 * pf::kTS * 4 <= kTf && kTf + 64 * pf::kTS * 4 <= kDm, "A
 
 constexpr uint32_t kColQK = 0, kColU = 64, kColW = 128, kPrepTmemCols = 256;
 constexpr int kWaitLimit = 1 << 22;
+constexpr uint64_t kFlowTimeoutNs = 2000000000ull;
 
 // Per-CTA state of the preparation role, kept across items: the tensor-memory
 // base (kPrepTmemCols columns), the MMA-completion mbarrier and its phase, and
@@ -65,11 +66,35 @@ struct Ctx {
     uint64_t* mbar;
     uint32_t phase;
     int* err_s;
+    bool no_flow;   // thread 0: the flow-control wait gave up once, so it is skipped from then on
 };
 
 __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& cx) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hk = p.Hk, Hv = p.Hv, C = p.C;
+
+    // Flow control: the records of (chunk gc, q/k head kh) are written once the H_v / H_k
+    // chains of the group are done with chunk gc - ahead, so that the records in flight stay
+    // in L2.  Thread 0 waits (bounded in time; it stops waiting for good once a chain has
+    // given up), the others start staging, and the first barrier of the item holds every
+    // record write until it is through.
+    if (tid == 0 && gc >= p.ahead && !cx.no_flow) {
+        const int* f = p.consumed + static_cast<size_t>(gc - p.ahead) * Hk + kh;
+        const volatile int* abort_flag = p.abort_flag;
+        const int need = Hv / Hk;
+        if (pf::ld_acquire(f) < need) {
+            const uint64_t tstart = pf::global_ns();
+            uint32_t ns = 128;
+            while (pf::ld_acquire(f) < need) {
+                if (*abort_flag || pf::global_ns() - tstart > kFlowTimeoutNs) {
+                    cx.no_flow = true;
+                    break;
+                }
+                __nanosleep(ns);
+                ns = min(ns * 2, 2048u);
+            }
+        }
+    }
 
     // sequence of this chunk: the last s with chunk_base[s] <= gc (a non-empty one)
     const int* tab = p.chunk_base;

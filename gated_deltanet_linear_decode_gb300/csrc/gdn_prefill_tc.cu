@@ -24,16 +24,19 @@ namespace {
 
 // Exclusive prefix of the per-sequence chunk counts: chunk_base[s] is the
 // global index of sequence s's first chunk, chunk_base[n_seq] the total.  Also
-// clears the ready flags [n_flags] and the item counter of this call.
+// clears the ready flags [n_flags], the consumed counters [n_consumed] and
+// the item counter and abort flag of this call.
 __global__ void chunk_table_kernel(const int* cu_seqlens, int n_seq, int* chunk_base, int* ready, int n_flags,
-                                   int* counter) {
+                                   int* consumed, int n_consumed, int* counter) {
     __shared__ int carry_s;
     __shared__ int warp_s[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     for (int i = tid; i < n_flags; i += blockDim.x) ready[i] = 0;
+    for (int i = tid; i < n_consumed; i += blockDim.x) consumed[i] = 0;
     if (tid == 0) {
         carry_s = 0;
-        *counter = 0;
+        counter[0] = 0;   // item counter
+        counter[1] = 0;   // abort flag
     }
     __syncthreads();
     for (int base = 0; base < n_seq; base += blockDim.x) {
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const Prefil
     if (warp == 0) tc::tmem_dealloc(cx.tmem, prep::kPrepTmemCols);
 }
 
-// Workspace layout: chunk table, ready flags, item counter, records.
+// Workspace layout: chunk table, ready flags, consumed counters, item counter, records.
 size_t flags_bytes(size_t n_chunks_bound, int Hk) { return (n_chunks_bound * Hk * 4 + 255) / 256 * 256; }
 
 }  // namespace
@@ -134,7 +137,8 @@ size_t flags_bytes(size_t n_chunks_bound, int Hk) { return (n_chunks_bound * Hk 
 // chunks bound every packing of T tokens.
 size_t tc_prefill_workspace_bytes(int Hk, int Hv, int n_seq, long long T) {
     const size_t nc = static_cast<size_t>((T + kChunk - 1) / kChunk) + static_cast<size_t>(n_seq);
-    return pf::table_bytes(n_seq) + flags_bytes(nc, Hk) + 256 + nc * static_cast<size_t>(Hv) * pf::kVRec;
+    return pf::table_bytes(n_seq) + 2 * flags_bytes(nc, Hk) + 256 +
+           nc * static_cast<size_t>(Hv) * pf::kVRec;
 }
 
 void tc_prefill_bind_workspace(PrefillParams& p) {
@@ -144,7 +148,10 @@ void tc_prefill_bind_workspace(PrefillParams& p) {
     base += pf::table_bytes(p.n_seq);
     p.ready = reinterpret_cast<int*>(base);
     base += flags_bytes(nc, p.Hk);
-    p.ws_v = base + 256;   // the item counter sits in the 256 bytes before the records
+    p.consumed = reinterpret_cast<int*>(base);
+    base += flags_bytes(nc, p.Hk);
+    p.ws_v = base + 256;   // the item counter and the abort flag sit in the 256 bytes before the records
+    p.abort_flag = reinterpret_cast<int*>(p.ws_v - 256) + 1;
 }
 
 cudaError_t launch_tensor_core_prefill(const PrefillParams& p0, int out_dtype, cudaStream_t stream) {
@@ -152,13 +159,11 @@ cudaError_t launch_tensor_core_prefill(const PrefillParams& p0, int out_dtype, c
     p.chunk_lo = 0;
     p.chunk_hi = p.n_chunks;
     int* counter = reinterpret_cast<int*>(p.ws_v - 256);
-    chunk_table_kernel<<<1, 256, 0, stream>>>(p.cu_seqlens, p.n_seq, p.chunk_base, p.ready, p.n_chunks * p.Hk, counter);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-
-    int dev = 0, sms = 0;
+    int dev = 0, sms = 0, l2 = 0;
+    cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess) return e;
     const int n_chains = p.n_seq * p.Hv;
     const int n_items = p.n_chunks * p.Hk;
     // One chain per CTA while the chains take at most half the SMs; beyond that, one
@@ -171,6 +176,23 @@ cudaError_t launch_tensor_core_prefill(const PrefillParams& p0, int out_dtype, c
     if (n_prep < 1) n_prep = 1;
     const int grid = n_chain + n_prep;
     const uint32_t smem = fused_smem(p.Hv / p.Hk);
+
+    // Records of at most `ahead` chunks in flight, about 9/16 of L2, so that they stay in L2
+    // between the preparation CTA that writes them and the chain that reads them (the rest
+    // of L2 holds the activations and outputs streaming past).  Measured at T = 8192 on
+    // 48 v-heads: DRAM traffic 1.07 GB unthrottled, 0.44 GB at 9/16, time within 3 %.
+    // The gate needs every v-head of a sequence walked at once (each chain CTA then
+    // meets the chunks in global order); with fewer chain CTAs than v-heads a chain may
+    // start only after another has finished its sequence, so there is no gate.
+    if (n_chain >= p.Hv) {
+        p.ahead = static_cast<int>(static_cast<size_t>(l2) / 16 * 9 / (static_cast<size_t>(p.Hv) * pf::kVRec));
+        if (p.ahead < 4) p.ahead = 4;
+    } else {
+        p.ahead = p.n_chunks;   // gc < n_chunks: never gated
+    }
+    chunk_table_kernel<<<1, 256, 0, stream>>>(p.cu_seqlens, p.n_seq, p.chunk_base, p.ready, p.n_chunks * p.Hk,
+                                              p.consumed, p.n_chunks * p.Hk, counter);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     auto go = [&](auto kernel) -> cudaError_t {
         cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -56,6 +56,9 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 // Order this thread's generic-proxy accesses to global memory (the flag just
 // acquired) before its later async-proxy accesses (bulk copies of the records).
 __device__ __forceinline__ void fence_proxy_async_global() {

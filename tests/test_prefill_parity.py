@@ -132,10 +132,12 @@ def test_varlen_t65536_sampled_sequences():
 
 
 @pytest.mark.parametrize("Hk,Hv,lengths", [(1, 1, [64]), (1, 3, [1]), (4, 8, [127, 65]), (2, 32, [300]),
-                                            (3, 3, [5, 200, 64, 63])])
+                                            (3, 3, [5, 200, 64, 63]), (8, 96, [200, 70])])
 def test_tensor_core_prefill_shapes(Hk, Hv, lengths):
     """Tensor-core prefill across head ratios 1..16, one-token and
-    whole-chunk sequences, against the oracle."""
+    whole-chunk sequences, against the oracle.  96 v-heads over two sequences
+    is more chains than the kernel gives chain CTAs (each CTA then walks
+    several (sequence, v-head) chains, without the records-in-flight gate)."""
     c = gdn_inputs.make_case("tcs", Hk=Hk, Hv=Hv, lengths=lengths, seed=Hk * 31 + Hv + sum(lengths))
     out, pre, conv, S, _ = run_prefill(c)
     ref = oracle_run(c)
