@@ -25,8 +25,8 @@ slowest rank's time is used.
 the step: decode at batch 1 as 1000 in-place steps captured in one CUDA graph,
 and the packed varlen prefill (8 sequences, T=65536, nonzero initial state).
 
---impl reference times the CPU oracle (fp64, OpenMP) on the host cores on a
-bounded sample of the same step.
+--impl reference times the CPU oracle (fp64, OpenMP) on the host cores over
+whole steps of the same workload (about a second each), nothing extrapolated.
 """
 from __future__ import annotations
 

@@ -17,17 +17,23 @@
 //   S    = e^{Gam_last} S + D^T K'   (K' = diag(e^{Gam_last - Gam}) K; three passes)
 //   O   += D^T P^T      (three passes)
 //   o_t  = O[:, t] / sqrt(128)  -> gated RMSNorm -> out
-// Warp roles, meeting only at mbarriers:
-//   warps 0-7   convert: S -> fp16 hi/lo (and the decay of S), Dacc -> D hi/lo
-//   warps 8-11  epilogue: O -> shared memory (row j per thread), then token-major:
-//               o -> gated RMSNorm -> out, a thread owning one token and 64 v-rows
-//               (z and out move in 16-byte pieces); up to two chunks behind
-//               (O is double-buffered in tensor memory; z is staged by cp.async)
+// Warp roles, meeting at mbarriers (the epilogue warps among themselves at a
+// named barrier):
+//   warps 0-7   convert: S -> fp16 hi/lo (and the decay of S), Dacc -> D hi/lo;
+//               after each D conversion, the outputs of v-rows 64-127 of the
+//               previous chunk from the staged O
+//   warps 8-11  epilogue: O -> shared memory (row j per thread; double-buffered),
+//               the per-token RMS factors, then token-major o -> gated RMSNorm ->
+//               out for v-rows 0-63, a thread owning one token (z and out move in
+//               16-byte pieces); up to two chunks behind (O is double-buffered in
+//               tensor memory; z is staged by cp.async)
 //   warp 12     control: one lane issues the MMAs
-//   warp 13     copies: one lane issues the bulk copies of the records, each as
-//               soon as the MMAs that read its buffer have retired
+//   warp 13     copies: one lane waits for each record's ready flag and issues its
+//               bulk copies as soon as the MMAs that read the buffer have retired,
+//               then drops the consumed record from L2 and counts the chunk consumed
 // Every wait has an iteration (or, for the ready flags, a time) limit; a
-// timeout sets dev_status bit 4.
+// timeout sets dev_status bit 4 and the abort flag that releases the
+// preparation role's records-in-flight gate.
 #pragma once
 
 #include <type_traits>
@@ -59,7 +65,7 @@ constexpr uint32_t kBar = kNw + 512;  // mbarriers, then the TMEM base and the e
 constexpr uint32_t kUs = (kBar + 176 + 127) / 128 * 128;   // the chunk's U, e^Gam, e^{Gam_last-Gam} (record tail)
 constexpr uint32_t kUBytes = pf::kVRec - pf::kRecU;          // 33280
 constexpr uint32_t kStateSmem = kUs + kUBytes;
-static_assert(kStateSmem <= 232448, "shared memory of the state pass exceeds 227 KB");
+static_assert(kStateSmem <= 232448, "shared memory of the chain role exceeds 227 KB");
 
 // mbarrier slots
 enum : int {

@@ -1,6 +1,6 @@
-// gdn_prefill_tc.cuh -- pieces shared by the two kernels of the tensor-core
-// prefill: the chunk-preparation kernel (everything of a chunk that does not
-// depend on the state) and the state pass (the chunk-to-chunk recurrence and
+// gdn_prefill_tc.cuh -- pieces shared by the two roles of the tensor-core
+// prefill kernel: the preparation role (everything of a chunk that does not
+// depend on the state) and the chain role (the chunk-to-chunk recurrence and
 // the outputs), plus the layout of the records the first hands to the second.
 //
 // Method: xwen CLAUDE.md page, "Ground truth" (chunk = 64 form of the delta

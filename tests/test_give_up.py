@@ -6,7 +6,7 @@ pairs it did not finish and returns (the home-server page's lesson on GDN
 state faults: report the failure, never leave it silent).
 
 GDN_FLAG_TEST_STALL makes the streaming recurrent kernel and the prefill's
-state pass first wait on a barrier that nothing arrives on; that wait gives
+chain role (the chunk-to-chunk recurrence) first wait on a barrier that nothing arrives on; that wait gives
 up after a few microseconds.  The tests check the report, that no state or
 output byte changed, and that the same context then runs a normal call that
 matches the oracle (the context stayed usable)."""

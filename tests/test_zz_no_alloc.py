@@ -63,8 +63,7 @@ def test_static_prefill_matches_workspace_entry_point_on_two_calls():
     through gdn_prefill_chunked with a torch-allocated workspace: two ragged
     multi-sequence problems with the model's head counts (16/48, bf16 in, fp32
     out) and one long single sequence with few heads (2/4, 4,100 tokens, 65
-    chunks: the chunk range is cut into segments whose kernels run on two
-    streams).  Both entry points run the same deterministic kernels on the same
+    chunks, each v-head's chain walking them all).  Both entry points run the same deterministic kernels on the same
     inputs, so outputs, pre-norm outputs, states and conv states must agree
     bit for bit -- a stale byte read from the shared area (left by the call
     before) would show as a difference."""
