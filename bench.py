@@ -517,24 +517,50 @@ def run_extras(dev, warmup, reps):
                                                  "algorithmic_bytes": bb}}
     del S, conv
 
-    # the projections either side of the mixer (cuBLASLt GEMMs): 27B dims over the T=8192 prefill
-    # (tensor-bound) and 35B dims over the B=64 decode batch (bound by reading the weights)
-    ws = torch.empty(32 << 20, device=dev, dtype=torch.uint8)
+    # decode B=64 with ssm_alpha / ssm_beta folded into the kernel (hidden 2048 -> a_raw, b_raw)
+    c = gdn_inputs.decode_b64()
+    pc = gdn_inputs.make_proj_case(T=c.N, H=2048, Hk=c.Hk, Hv=c.Hv, seed=11)
+    d = gdn.make_dims(c.Hk, c.Hv, torch.bfloat16, torch.bfloat16)
+    w = gdn.make_weights(c.conv_w, c.dt_bias, c.ssm_a, c.norm_w, device=dev)
+    i = {k: getattr(c, k).to(dev) for k in ("x", "z")}
+    hid, Wa, Wb = pc.hidden.to(dev), pc.W_a.to(dev), pc.W_b.to(dev)
+    conv, S = c.conv0.to(dev), c.S0.to(dev)
+    o = torch.empty(c.N, c.Hv * 128, device=dev, dtype=torch.bfloat16)
+    am = timed_graph(lambda: gdn.gdn_decode_step_ab(d, w, i["x"], i["z"], hid, Wa, Wb, conv, S, o))
+    ab = decode_bytes(c.N, c.Hk, c.Hv) + 2 * (c.N * 2048 + 2 * c.Hv * 2048) - 2 * 2 * c.N * c.Hv
+    out["decode_B64_fold_ab_H2048"] = {"tokens_per_s": c.N / (am / 1e3), "us": 1e3 * am,
+                                       "roofline": {"bound": "hbm", "achieved": ab / (am / 1e3) / 1e9, "peak": hbm,
+                                                    "unit": "GB/s", "frac": ab / (am / 1e3) / 1e9 / hbm,
+                                                    "algorithmic_bytes": ab}}
+    del S, conv
+
+    # the projections either side of the mixer: 27B dims over the T=8192 prefill (tensor-bound,
+    # cuBLASLt) and, bound by reading the weights, the library's weight-streaming kernel at the
+    # B=64 decode batch (35B and 27B dims) and the B=64 K=3 verify batch (35B dims)
     for name, T, H, Hk, Hv in (("proj_in_out_T8192_H5120", 8192, 5120, 16, 48),
-                               ("proj_in_out_B64_H2048", 64, 2048, 16, 32)):
+                               ("proj_in_out_B64_H2048", 64, 2048, 16, 32),
+                               ("proj_in_out_B64_H5120", 64, 5120, 16, 48),
+                               ("proj_in_out_T192_H2048", 192, 2048, 16, 32)):
         c = gdn_inputs.make_proj_case(T=T, H=H, Hk=Hk, Hv=Hv, seed=7)
         d = gdn.make_dims(Hk, Hv, torch.bfloat16, torch.bfloat16)
         C, HvD = 128 * (2 * Hk + Hv), 128 * Hv
+        ws = torch.empty(max(32 << 20, gdn.gdn_proj_workspace_bytes(d, T, H)), device=dev, dtype=torch.uint8)
         t = {k: getattr(c, k).to(dev) for k in ("hidden", "W_qkv", "W_z", "W_a", "W_b", "y", "W_out")}
         bf = dict(device=dev, dtype=torch.bfloat16)
         x, z = torch.empty(T, C, **bf), torch.empty(T, HvD, **bf)
         a, b, po = torch.empty(T, Hv, **bf), torch.empty(T, Hv, **bf), torch.empty(T, H, **bf)
 
-        def proj():
+        def proj_in():
             gdn.gdn_in_proj(d, t["hidden"], t["W_qkv"], t["W_z"], t["W_a"], t["W_b"], x, z, a, b, workspace=ws)
+
+        def proj_out():
             gdn.gdn_out_proj(d, t["y"], t["W_out"], po, workspace=ws)
 
-        pm = timed_graph(proj)
+        def proj():
+            proj_in()
+            proj_out()
+
+        pm, pin, pout = timed_graph(proj), timed_graph(proj_in), timed_graph(proj_out)
 
         def torch_linear():   # the same five GEMMs through torch (cuBLAS), for comparison only
             for W, o in ((t["W_qkv"], x), (t["W_z"], z), (t["W_a"], a), (t["W_b"], b)):
@@ -545,13 +571,14 @@ def run_extras(dev, warmup, reps):
         flops = 2.0 * T * H * (C + HvD + 2 * Hv) + 2.0 * T * HvD * H
         wbytes = 2 * H * (C + HvD + 2 * Hv) + 2 * H * HvD
         abytes = 2 * T * (H + C + HvD + 2 * Hv) + 2 * T * (HvD + H)
-        out[name] = {"ms": pm, "torch_cublas_ms": cm, "tflops": flops / (pm / 1e3) / 1e12,
+        out[name] = {"ms": pm, "in_ms": pin, "out_ms": pout, "torch_cublas_ms": cm,
+                     "kernel": "weight-streaming (TMA + tcgen05)" if T <= 256 else "cuBLASLt",
+                     "tflops": flops / (pm / 1e3) / 1e12,
                      "frac_of_bf16_peak": flops / (pm / 1e3) / 1e12 / tf,
                      "GBps": (wbytes + abytes) / (pm / 1e3) / 1e9,
                      "frac_of_hbm_peak": (wbytes + abytes) / (pm / 1e3) / 1e9 / hbm,
                      "flops": flops, "bytes": wbytes + abytes}
-        del t, x, z, a, b, po
-    del ws
+        del t, x, z, a, b, po, ws
 
     # packed varlen prefill, 8 sequences, T=65536
     c = gdn_inputs.varlen_t65536()

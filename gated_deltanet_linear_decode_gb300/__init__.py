@@ -22,11 +22,11 @@ from . import _build
 
 __all__ = [
     "GdnError", "GdnDims", "GdnWeights", "make_dims", "make_weights", "library",
-    "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step",
+    "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step", "gdn_decode_step_ab",
     "gdn_verify_k", "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked",
     "gdn_prefill_chunked_static", "gdn_verify_k_ring", "gdn_commit_ring", "gdn_decode_step_ring",
     "gdn_state_faults", "gdn_state_reset", "GdnInProjWeights", "gdn_in_proj", "gdn_out_proj",
-    "PREFILL_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "HEAD_DIM",
+    "gdn_proj_workspace_bytes", "PREFILL_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "HEAD_DIM",
 ]
 
 HEAD_DIM = 128
@@ -38,10 +38,10 @@ GDN_FLAG_TEST_STALL = 1 << 30
 PREFILL_STATIC_SCRATCH_BYTES = 128 * 1024 * 1024   # GDN_PREFILL_STATIC_SCRATCH_BYTES
 
 EXPORTED_SYMBOLS = (
-    "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step",
+    "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step", "gdn_decode_step_ab",
     "gdn_verify_k", "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked",
     "gdn_prefill_chunked_static", "gdn_verify_k_ring", "gdn_commit_ring", "gdn_decode_step_ring",
-    "gdn_state_faults", "gdn_state_reset", "gdn_in_proj", "gdn_out_proj",
+    "gdn_state_faults", "gdn_state_reset", "gdn_in_proj", "gdn_out_proj", "gdn_proj_workspace_bytes",
 )
 
 
@@ -87,6 +87,7 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         "gdn_version": (I32, []),
         "gdn_conv_state_init": (ctypes.c_int, [D, I32, P, P, P]),
         "gdn_decode_step": (ctypes.c_int, [D, W, I32, P, P, P, P, P, P, P, P, P, P]),
+        "gdn_decode_step_ab": (ctypes.c_int, [D, W, I32, I32, P, P, P, P, P, P, P, P, P, P, P]),
         "gdn_verify_k": (ctypes.c_int, [D, W, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P]),
         "gdn_commit": (ctypes.c_int, [D, I32, I32, P, P, P, P, P, P]),
         "gdn_prefill_workspace_bytes": (SZ, [D, I32, ctypes.c_int64]),
@@ -97,8 +98,9 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         "gdn_decode_step_ring": (ctypes.c_int, [D, W, I32, I32, P, P, P, P, P, P, P, P, P, P, P]),
         "gdn_state_faults": (ctypes.c_int, [D, I32, P, I32, P, P]),
         "gdn_state_reset": (ctypes.c_int, [D, I32, I32, P, P, P, P, P]),
-        "gdn_in_proj": (ctypes.c_int, [D, I32, I32, P, ctypes.POINTER(GdnInProjWeights), P, P, P, P, P, SZ, P]),
-        "gdn_out_proj": (ctypes.c_int, [D, I32, I32, P, P, P, P, SZ, P]),
+        "gdn_in_proj": (ctypes.c_int, [D, I32, I32, P, ctypes.POINTER(GdnInProjWeights), P, P, P, P, P, SZ, P, P]),
+        "gdn_out_proj": (ctypes.c_int, [D, I32, I32, P, P, P, P, SZ, P, P]),
+        "gdn_proj_workspace_bytes": (SZ, [D, I32, I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -224,6 +226,23 @@ def gdn_decode_step(dims: GdnDims, w: Weights, x, z, a_raw, b_raw, conv_state, S
         _ptr(conv_state), _ptr(S), _ptr(out), _ptr(prenorm_out), _ptr(dev_status), _stream(stream)))
 
 
+def gdn_decode_step_ab(dims: GdnDims, w: Weights, x, z, hidden, W_a, W_b, conv_state, S, out,
+                       prenorm_out=None, dev_status=None, stream=None) -> None:
+    """gdn_decode_step with ssm_alpha / ssm_beta folded in: a_raw, b_raw formed in the kernel from
+    hidden [B][H] and W_a, W_b [H_v][H] (bf16)."""
+    B, H = hidden.shape
+    C, HvD = HEAD_DIM * (2 * dims.H_k + dims.H_v), dims.H_v * HEAD_DIM
+    a, bf = _act(dims), torch.bfloat16
+    _need(x, a, (B, C)); _need(z, a, (B, HvD)); _need(hidden, bf, (B, H))
+    _need(W_a, bf, (dims.H_v, H)); _need(W_b, bf, (dims.H_v, H))
+    _need(conv_state, a, (B, 3, C)); _need(S, _st(dims), (B, dims.H_v, HEAD_DIM, HEAD_DIM))
+    _need(out, _out(dims), (B, HvD)); _need(prenorm_out, torch.float32, (B, HvD), optional=True)
+    _need(dev_status, torch.int32, (B * dims.H_v,), optional=True)
+    _check("gdn_decode_step_ab", library().gdn_decode_step_ab(
+        ctypes.byref(dims), ctypes.byref(w.struct()), B, H, _ptr(x), _ptr(z), _ptr(hidden), _ptr(W_a), _ptr(W_b),
+        _ptr(conv_state), _ptr(S), _ptr(out), _ptr(prenorm_out), _ptr(dev_status), _stream(stream)))
+
+
 def gdn_verify_k(dims: GdnDims, w: Weights, K: int, x, z, a_raw, b_raw, conv_state, S, conv_ckpt, S_ckpt,
                  out, prenorm_out=None, dev_status=None, stream=None) -> None:
     """Verify walk over K tokens per sequence (x [B*K][C]); writes per-position checkpoints."""
@@ -331,33 +350,39 @@ def gdn_state_reset(dims: GdnDims, S, dev_status, conv_state=None, ring_cur=None
 
 
 def gdn_in_proj(dims: GdnDims, hidden, W_qkv, W_z, W_a, W_b, x, z, a_raw, b_raw, workspace=None,
-                stream=None) -> None:
+                dev_status=None, stream=None) -> None:
     """attn_qkv / attn_gate / ssm_alpha / ssm_beta: hidden [T][H] bf16 -> x, z, a_raw, b_raw (bf16);
-    weights in the [out][in] layout (cuBLASLt GEMMs, fp32 accumulation)."""
+    weights in the [out][in] layout (fp32 accumulation; the library's weight-streaming kernel for
+    T <= 256, cuBLASLt above)."""
     T, H = hidden.shape
     C, HvD = HEAD_DIM * (2 * dims.H_k + dims.H_v), dims.H_v * HEAD_DIM
     bf = torch.bfloat16
     _need(hidden, bf, (T, H)); _need(W_qkv, bf, (C, H)); _need(W_z, bf, (HvD, H))
     _need(W_a, bf, (dims.H_v, H)); _need(W_b, bf, (dims.H_v, H))
     _need(x, bf, (T, C)); _need(z, bf, (T, HvD)); _need(a_raw, bf, (T, dims.H_v)); _need(b_raw, bf, (T, dims.H_v))
-    _need(workspace, None, None, optional=True)
+    _need(workspace, None, None, optional=True); _need(dev_status, torch.int32, (1,), optional=True)
     w = GdnInProjWeights(_ptr(W_qkv), _ptr(W_z), _ptr(W_a), _ptr(W_b))
     nws = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("gdn_in_proj", library().gdn_in_proj(ctypes.byref(dims), T, H, _ptr(hidden), ctypes.byref(w), _ptr(x),
                                                 _ptr(z), _ptr(a_raw), _ptr(b_raw), _ptr(workspace), nws,
-                                                _stream(stream)))
+                                                _ptr(dev_status), _stream(stream)))
 
 
-def gdn_out_proj(dims: GdnDims, y, W_out, out, workspace=None, stream=None) -> None:
+def gdn_proj_workspace_bytes(dims: GdnDims, T: int, H: int) -> int:
+    """Workspace that lets the projections at T <= 256 rows spread over every SM."""
+    return int(library().gdn_proj_workspace_bytes(ctypes.byref(dims), T, H))
+
+
+def gdn_out_proj(dims: GdnDims, y, W_out, out, workspace=None, dev_status=None, stream=None) -> None:
     """ssm_out: y [T][H_v*128] bf16 -> out [T][H] bf16, W_out [H][H_v*128]."""
     T, HvD = y.shape
     H = out.shape[1]
     bf = torch.bfloat16
     _need(y, bf, (T, dims.H_v * HEAD_DIM)); _need(W_out, bf, (H, HvD)); _need(out, bf, (T, H))
-    _need(workspace, None, None, optional=True)
+    _need(workspace, None, None, optional=True); _need(dev_status, torch.int32, (1,), optional=True)
     nws = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("gdn_out_proj", library().gdn_out_proj(ctypes.byref(dims), T, H, _ptr(y), _ptr(W_out), _ptr(out),
-                                                  _ptr(workspace), nws, _stream(stream)))
+                                                  _ptr(workspace), nws, _ptr(dev_status), _stream(stream)))
 
 
 def gdn_prefill_workspace_bytes(dims: GdnDims, n_seq: int, T_total: int) -> int:

@@ -90,15 +90,15 @@ gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_E
 // Streaming (persistent, one CTA per SM) recurrent kernel when there are at
 // least two (sequence, q/k-group) items per SM and its stages fit in shared
 // memory; the cluster kernel otherwise.  The choice depends on B, H_k and K
-// only, never on the data.
-bool use_stream_kernel(int B, int Hk, int K, int act_dtype, bool state_bf16, int* grid) {
+// only (and, with ssm_alpha / ssm_beta folded in, the hidden size), never on the data.
+bool use_stream_kernel(int B, int Hk, int K, int act_dtype, bool state_bf16, int ab_H, int* grid) {
     int dev = 0, sms = 0, smem = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
     const long long items = static_cast<long long>(B) * Hk;
     if (items < 2LL * sms) return false;
-    if (gdn::recurrent_stream_smem(K, act_dtype, state_bf16) > static_cast<size_t>(smem)) return false;
+    if (gdn::recurrent_stream_smem(K, act_dtype, state_bf16, ab_H) > static_cast<size_t>(smem)) return false;
     *grid = sms;
     return true;
 }
@@ -136,19 +136,37 @@ gdn_status gdn_conv_state_init(const gdn_dims* dims, int32_t n_seq, void* conv_s
 }
 
 // ring_cur != nullptr: S_in == S_out is a state ring [B][R][H_v][128][128] (see gdn_verify_k_ring).
+// ssm_alpha / ssm_beta folded into the recurrent kernels (gdn_decode_step_ab)
+struct AbFold {
+    int32_t H;
+    const void* hidden;
+    const void* W_a;
+    const void* W_b;
+};
+
 static gdn_status recurrent_common(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t K,
                                    const void* x, const void* z, const void* a_raw, const void* b_raw,
                                    const void* conv_in, const void* S_in, void* conv_out, void* S_out,
                                    bool verify, void* out, float* prenorm_out, int32_t* dev_status,
-                                   gdn_stream_t stream, const int32_t* ring_cur = nullptr, int32_t R = 0) {
+                                   gdn_stream_t stream, const int32_t* ring_cur = nullptr, int32_t R = 0,
+                                   const AbFold* ab = nullptr) {
     gdn_status s = check_dims(dims);
     if (s != GDN_OK) return s;
     if (B < 0 || K < 1 || K > GDN_MAX_VERIFY_K) return GDN_E_INVALID_ARG;
     if (ring_cur && (R < (verify ? K + 1 : 1) || R > GDN_MAX_VERIFY_K + 1)) return GDN_E_INVALID_ARG;
+    if (ab && (ab->H < 8 || ab->H % 8 != 0)) return GDN_E_INVALID_ARG;
+    if (ab && dims->act_dtype != GDN_BF16) return GDN_E_UNSUPPORTED;
     if (B == 0) return GDN_OK;
     if ((s = check_weights(w)) != GDN_OK) return s;
-    if ((s = check_ptrs({x, z, a_raw, b_raw, conv_in, S_in, conv_out, S_out, out}, {prenorm_out, dev_status})) != GDN_OK)
+    if (ab) {
+        // the folded projections take the place of a_raw / b_raw
+        if ((s = check_ptrs({x, z, ab->hidden, ab->W_a, ab->W_b, conv_in, S_in, conv_out, S_out, out},
+                            {prenorm_out, dev_status})) != GDN_OK)
+            return s;
+    } else if ((s = check_ptrs({x, z, a_raw, b_raw, conv_in, S_in, conv_out, S_out, out}, {prenorm_out, dev_status})) !=
+               GDN_OK) {
         return s;
+    }
     if (ring_cur && (s = check_ptrs({ring_cur}, {})) != GDN_OK) return s;
     const int Hk = dims->H_k, Hv = dims->H_v;
     const size_t C = static_cast<size_t>(kD) * (2 * Hk + Hv);
@@ -159,13 +177,16 @@ static gdn_status recurrent_common(const gdn_dims* dims, const gdn_weights* w, i
     const size_t cv_bytes = static_cast<size_t>(B) * 3 * C * ea;
     // a ring is read and written in one buffer (like the in-place decode state)
     const size_t S_out_bytes = ring_cur ? S_bytes * R : (verify ? S_bytes * K : S_bytes);
-    const Range ins[] = {{x, T * C * ea}, {z, T * HvD * ea}, {a_raw, T * Hv * ea}, {b_raw, T * Hv * ea},
-                         {w->conv_w, C * 16}, {w->dt_bias, Hv * 4u}, {w->ssm_a, Hv * 4u}, {w->norm_w, kD * 4u},
-                         {verify ? conv_in : nullptr, cv_bytes}, {verify && !ring_cur ? S_in : nullptr, S_bytes},
-                         {ring_cur, B * 4u}};
+    const size_t Hab = ab ? static_cast<size_t>(ab->H) : 0;
+    const Range ins[] = {{x, T * C * ea}, {z, T * HvD * ea}, {ab ? nullptr : a_raw, T * Hv * ea},
+                         {ab ? nullptr : b_raw, T * Hv * ea}, {w->conv_w, C * 16}, {w->dt_bias, Hv * 4u},
+                         {w->ssm_a, Hv * 4u}, {w->norm_w, kD * 4u}, {verify ? conv_in : nullptr, cv_bytes},
+                         {verify && !ring_cur ? S_in : nullptr, S_bytes}, {ring_cur, B * 4u},
+                         {ab ? ab->hidden : nullptr, T * Hab * 2}, {ab ? ab->W_a : nullptr, Hv * Hab * 2},
+                         {ab ? ab->W_b : nullptr, Hv * Hab * 2}};
     const Range outs[] = {{out, T * HvD * eo}, {prenorm_out, T * HvD * 4}, {dev_status, B * Hv * 4u},
                           {conv_out, verify ? cv_bytes * K : cv_bytes}, {S_out, S_out_bytes}};
-    if (any_overlap(outs, 5, ins, 11)) return GDN_E_INVALID_ARG;
+    if (any_overlap(outs, 5, ins, 14)) return GDN_E_INVALID_ARG;
 
     gdn::RecParams p{};
     const int r = Hv / Hk;
@@ -187,8 +208,13 @@ static gdn_status recurrent_common(const gdn_dims* dims, const gdn_weights* w, i
     }
     p.out = out; p.prenorm = prenorm_out; p.dev_status = dev_status;
     p.ring_cur = ring_cur; p.ring_R = R; p.ring_shift = verify ? 1 : 0;
+    if (ab) {
+        p.a_raw = nullptr; p.b_raw = nullptr;
+        p.ab_hidden = ab->hidden; p.W_a = ab->W_a; p.W_b = ab->W_b; p.ab_H = ab->H;
+    }
     int grid = 0;
-    if (use_stream_kernel(B, Hk, K, dims->act_dtype, (dims->flags & GDN_FLAG_STATE_BF16) != 0, &grid))
+    if (use_stream_kernel(B, Hk, K, dims->act_dtype, (dims->flags & GDN_FLAG_STATE_BF16) != 0, ab ? ab->H : 0,
+                          &grid))
         return cuda_status(gdn::launch_recurrent_stream(p, dims->act_dtype, dims->out_dtype, grid,
                                                         reinterpret_cast<cudaStream_t>(stream)));
     return cuda_status(gdn::launch_recurrent(p, dims->act_dtype, dims->out_dtype, rpc,
@@ -200,6 +226,14 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, int32_t B
                            float* prenorm_out, int32_t* dev_status, gdn_stream_t stream) {
     return recurrent_common(dims, w, B, 1, x, z, a_raw, b_raw, conv_state, S, conv_state, S, false, out,
                             prenorm_out, dev_status, stream);
+}
+
+gdn_status gdn_decode_step_ab(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t H, const void* x,
+                              const void* z, const void* hidden, const void* W_a, const void* W_b, void* conv_state,
+                              void* S, void* out, float* prenorm_out, int32_t* dev_status, gdn_stream_t stream) {
+    const AbFold ab{H, hidden, W_a, W_b};
+    return recurrent_common(dims, w, B, 1, x, z, nullptr, nullptr, conv_state, S, conv_state, S, false, out,
+                            prenorm_out, dev_status, stream, nullptr, 0, &ab);
 }
 
 gdn_status gdn_verify_k(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t K, const void* x,

@@ -39,6 +39,37 @@ __device__ __forceinline__ bool nonfinite_bits(float v) {
     return (__float_as_uint(v) & 0x7f800000u) == 0x7f800000u;
 }
 
+// ---------------------------------------------------------------- folded a/b projections
+// This thread's share of hidden . W_a and hidden . W_b (bf16 rows of H elements, H a
+// multiple of 8, 16-byte aligned): the 8-element chunks i, i + step, ...  One fixed order
+// of FMAs.  Returns (a part, b part).  kGlobal: the rows are in global memory (read
+// through the read-only path), else in shared memory.
+template <bool kGlobal>
+__device__ __forceinline__ float2 ab_dot_part(const __nv_bfloat16* hid, const __nv_bfloat16* wa,
+                                             const __nv_bfloat16* wb, int H, int i, int step) {
+    auto ld = [](const __nv_bfloat16* row, int c) {
+        const uint4* p = reinterpret_cast<const uint4*>(row) + c;
+        if constexpr (kGlobal) return __ldg(p);
+        else return *p;
+    };
+    float sa = 0.f, sb = 0.f;
+    for (int c = i; c < (H >> 3); c += step) {
+        const uint4 hv = ld(hid, c);
+        const uint4 av = ld(wa, c);
+        const uint4 bv = ld(wb, c);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hv);
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&av);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 hf = __bfloat1622float2(h2[e]), af = __bfloat1622float2(a2[e]), bf = __bfloat1622float2(b2[e]);
+            sa = fmaf(hf.y, af.y, fmaf(hf.x, af.x, sa));
+            sb = fmaf(hf.y, bf.y, fmaf(hf.x, bf.x, sb));
+        }
+    }
+    return make_float2(sa, sb);
+}
+
 // ---------------------------------------------------------------- warp reductions
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

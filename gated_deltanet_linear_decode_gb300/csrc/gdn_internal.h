@@ -42,6 +42,13 @@ struct RecParams {
     // reads slot ring_cur[b] and writes position t to slot (ring_cur[b] + ring_shift + t) % ring_R
     const int* ring_cur;
     int ring_R, ring_shift;
+    // ssm_alpha / ssm_beta folded in (ab_hidden != nullptr): a_raw and b_raw of token row r
+    // and v-head h are the fp32 dot products hidden[r] . W_a[h] and hidden[r] . W_b[h]
+    // (bf16 operands, length ab_H); a_raw / b_raw above are then unused
+    const void* ab_hidden;  // [B*K][ab_H] bf16
+    const void* W_a;        // [Hv][ab_H] bf16
+    const void* W_b;        // [Hv][ab_H] bf16
+    int ab_H;
 };
 
 #ifdef __CUDACC__
@@ -119,7 +126,7 @@ cudaError_t launch_prefill(const PrefillParams& p, int act_dtype, int out_dtype,
 
 cudaError_t launch_recurrent(const RecParams& p, int act_dtype, int out_dtype, int rows_per_cta,
                              cudaStream_t stream);
-size_t recurrent_stream_smem(int K, int act_dtype, bool state_bf16);
+size_t recurrent_stream_smem(int K, int act_dtype, bool state_bf16, int ab_H);
 cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_dtype, int grid, cudaStream_t stream);
 cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream);
 cudaError_t launch_conv_init(void* dst, const void* src, size_t bytes, cudaStream_t stream);
@@ -135,5 +142,19 @@ struct ResetParams {
     const int* dev_status;   // [N*Hv]
 };
 cudaError_t launch_state_reset(const ResetParams& p, cudaStream_t stream);
+
+// One GEMM of a projection call: out [T][rows] = in [T][K] . W [rows][K]^T (bf16).
+struct ProjGemm {
+    const void* W;
+    void* out;
+    int rows;
+};
+constexpr int kProjStreamMaxRows = 256;   // the weight-streaming kernel takes T <= this
+// Up to 4 GEMMs sharing `in`, one launch (gdn_proj_stream.cu).  With a workspace of at least
+// proj_stream_workspace_bytes() every SM streams an equal share of the weights; without,
+// one CTA per 128-row tile.  status: optional, bit 4.
+size_t proj_stream_workspace_bytes(const int* rows, int n_gemm, int T, int K);
+cudaError_t launch_proj_stream(const ProjGemm* g, int n_gemm, const void* in, int T, int K, void* workspace,
+                               size_t workspace_bytes, int* status, cudaStream_t stream);
 
 }  // namespace gdn

@@ -1,9 +1,11 @@
 // gdn_proj.cu -- the projections either side of the token mixer (include/gdn_proj.h):
 // attn_qkv, attn_gate, ssm_alpha, ssm_beta before it and ssm_out after it (xwen CLAUDE.md
-// page, "Architecture cheat sheet", "Gated DeltaNet layer").  They are plain dense GEMMs,
-// so they run on the tensor cores through cuBLASLt (bf16 operands, fp32 accumulation);
-// this file is host code only: validation, one cached cuBLASLt handle per device, and a
-// cache of the chosen algorithm per problem shape.
+// page, "Architecture cheat sheet", "Gated DeltaNet layer").  They are dense GEMMs.  At
+// decode-size batches (T <= 256) they are bound by the weight stream and run in the
+// library's own weight-streaming kernel (gdn_proj_stream.cu: TMA + tcgen05, the four
+// input GEMMs in one launch); larger T is tensor-bound and runs through cuBLASLt (bf16
+// operands, fp32 accumulation).  This file is host code only: validation, dispatch, one
+// cached cuBLASLt handle per device, and a cache of the chosen algorithm per shape.
 #include <cublasLt.h>
 #include <cuda_runtime.h>
 
@@ -13,6 +15,7 @@
 #include <tuple>
 
 #include "gdn.h"
+#include "gdn_internal.h"
 #include "gdn_proj.h"
 
 namespace {
@@ -123,9 +126,18 @@ gdn_status gemm_bf16(const void* A, const void* W, void* C, int T, int N, int K,
 
 extern "C" {
 
+size_t gdn_proj_workspace_bytes(const gdn_dims* dims, int32_t T, int32_t H) {
+    if (check_proj_dims(dims, T, H) != GDN_OK || T == 0 || T > gdn::kProjStreamMaxRows) return 0;
+    const int C = kD * (2 * dims->H_k + dims->H_v), HvD = kD * dims->H_v, Hv = dims->H_v;
+    const int in_rows[4] = {C, HvD, Hv, Hv}, out_rows[1] = {H};
+    const size_t a = gdn::proj_stream_workspace_bytes(in_rows, 4, T, H);
+    const size_t b = gdn::proj_stream_workspace_bytes(out_rows, 1, T, HvD);
+    return a > b ? a : b;
+}
+
 gdn_status gdn_in_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* hidden, const gdn_in_proj_weights* w,
                        void* x, void* z, void* a_raw, void* b_raw, void* workspace, size_t workspace_bytes,
-                       gdn_stream_t stream) {
+                       int32_t* dev_status, gdn_stream_t stream) {
     gdn_status s = check_proj_dims(dims, T, H);
     if (s != GDN_OK) return s;
     if (T == 0) return GDN_OK;
@@ -135,7 +147,8 @@ gdn_status gdn_in_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* h
     const void* ptrs[] = {hidden, w->W_qkv, w->W_z, w->W_a, w->W_b, x, z, a_raw, b_raw};
     for (const void* p : ptrs)
         if (!aligned16(p)) return GDN_E_ALIGNMENT;
-    if (workspace && !aligned16(workspace)) return GDN_E_ALIGNMENT;
+    if ((workspace && !aligned16(workspace)) || (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3u)))
+        return GDN_E_ALIGNMENT;
     const size_t Tz = static_cast<size_t>(T), Hz = static_cast<size_t>(H);
     const int C = kD * (2 * dims->H_k + dims->H_v), HvD = kD * dims->H_v, Hv = dims->H_v;
     const void* ins[] = {hidden, w->W_qkv, w->W_z, w->W_a, w->W_b};
@@ -148,7 +161,16 @@ gdn_status gdn_in_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* h
         for (int j = i + 1; j < 5; ++j)
             if (overlap(outs[i], out_b[i], outs[j], out_b[j])) return GDN_E_INVALID_ARG;
     }
+    if (overlap(dev_status, 4, hidden, Tz * Hz * 2)) return GDN_E_INVALID_ARG;
+    for (int i = 0; i < 5; ++i)
+        if (overlap(dev_status, 4, outs[i], out_b[i])) return GDN_E_INVALID_ARG;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (T <= gdn::kProjStreamMaxRows) {
+        const gdn::ProjGemm g[4] = {{w->W_qkv, x, C}, {w->W_z, z, HvD}, {w->W_a, a_raw, Hv}, {w->W_b, b_raw, Hv}};
+        return gdn::launch_proj_stream(g, 4, hidden, T, H, workspace, workspace_bytes, dev_status, st) == cudaSuccess
+                   ? GDN_OK
+                   : GDN_E_CUDA;
+    }
     if ((s = gemm_bf16(hidden, w->W_qkv, x, T, C, H, workspace, workspace_bytes, st)) != GDN_OK) return s;
     if ((s = gemm_bf16(hidden, w->W_z, z, T, HvD, H, workspace, workspace_bytes, st)) != GDN_OK) return s;
     if ((s = gemm_bf16(hidden, w->W_a, a_raw, T, Hv, H, workspace, workspace_bytes, st)) != GDN_OK) return s;
@@ -156,19 +178,28 @@ gdn_status gdn_in_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* h
 }
 
 gdn_status gdn_out_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* y, const void* W_out, void* out,
-                        void* workspace, size_t workspace_bytes, gdn_stream_t stream) {
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status, gdn_stream_t stream) {
     gdn_status s = check_proj_dims(dims, T, H);
     if (s != GDN_OK) return s;
     if (T == 0) return GDN_OK;
     if (!y || !W_out || !out || (workspace_bytes > 0 && !workspace)) return GDN_E_INVALID_ARG;
-    if (!aligned16(y) || !aligned16(W_out) || !aligned16(out) || (workspace && !aligned16(workspace)))
+    if (!aligned16(y) || !aligned16(W_out) || !aligned16(out) || (workspace && !aligned16(workspace)) ||
+        (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3u)))
         return GDN_E_ALIGNMENT;
     const size_t Tz = static_cast<size_t>(T), Hz = static_cast<size_t>(H);
     const int HvD = kD * dims->H_v;
     if (overlap(out, Tz * Hz * 2, y, Tz * HvD * 2) || overlap(out, Tz * Hz * 2, W_out, Hz * HvD * 2) ||
         overlap(workspace, workspace_bytes, y, Tz * HvD * 2) || overlap(workspace, workspace_bytes, W_out, Hz * HvD * 2) ||
-        overlap(workspace, workspace_bytes, out, Tz * Hz * 2))
+        overlap(workspace, workspace_bytes, out, Tz * Hz * 2) || overlap(dev_status, 4, out, Tz * Hz * 2) ||
+        overlap(dev_status, 4, y, Tz * HvD * 2))
         return GDN_E_INVALID_ARG;
+    if (T <= gdn::kProjStreamMaxRows) {
+        const gdn::ProjGemm g[1] = {{W_out, out, H}};
+        return gdn::launch_proj_stream(g, 1, y, T, HvD, workspace, workspace_bytes, dev_status,
+                                       reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+                   ? GDN_OK
+                   : GDN_E_CUDA;
+    }
     return gemm_bf16(y, W_out, out, T, H, HvD, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -66,6 +66,7 @@ recurrent_kernel(const RecParams p) {
     __shared__ float red[2][NW];
     __shared__ float part[NW];
     __shared__ float gates[2];
+    __shared__ float abp[NW][2];   // folded a/b: the warps' partial dot products
     __shared__ float rms_part[kMaxK];
 
     // ---- state rows: issue the 128-bit loads before anything else
@@ -120,10 +121,23 @@ recurrent_kernel(const RecParams p) {
             v_s[tid] = siluf_(conv4(Wv, to_f(wv[0]), to_f(wv[1]), to_f(wv[2]), to_f(xv)));
             zsil = siluf_(ld_act(static_cast<const Tact*>(p.z) + row * HvD + h * kD + j0 + tid));
         }
-        if (tid == 0) {
-            // step 6: gates
-            gates[0] = sigmoidf_(ld_act(static_cast<const Tact*>(p.b_raw) + row * p.Hv + h));
-            gates[1] = a_ssm * softplusf_(ld_act(static_cast<const Tact*>(p.a_raw) + row * p.Hv + h) + a_dt);
+        if (!p.ab_hidden) {
+            if (tid == 0) {
+                // step 6: gates
+                gates[0] = sigmoidf_(ld_act(static_cast<const Tact*>(p.b_raw) + row * p.Hv + h));
+                gates[1] = a_ssm * softplusf_(ld_act(static_cast<const Tact*>(p.a_raw) + row * p.Hv + h) + a_dt);
+            }
+        } else {
+            // ssm_alpha / ssm_beta folded in: a share of hidden[row] . W_a[h] and . W_b[h]
+            const float2 pr = ab_dot_part<true>(static_cast<const __nv_bfloat16*>(p.ab_hidden) + row * p.ab_H,
+                                          static_cast<const __nv_bfloat16*>(p.W_a) + static_cast<size_t>(h) * p.ab_H,
+                                          static_cast<const __nv_bfloat16*>(p.W_b) + static_cast<size_t>(h) * p.ab_H,
+                                          p.ab_H, tid, NT);
+            const float sa = warp_sum(pr.x), sb = warp_sum(pr.y);
+            if (lane == 0) {
+                abp[warp][0] = sa;
+                abp[warp][1] = sb;
+            }
         }
         // ---- step 4: clamp-form L2 norms of q and k (threads 0..127 = warps 0..3)
         {
@@ -131,6 +145,17 @@ recurrent_kernel(const RecParams p) {
             if (lane == 0) { red[0][warp] = sq; red[1][warp] = sk; }
         }
         __syncthreads();
+        if (p.ab_hidden && tid == 0) {
+            // step 6 with the folded projections (read before the next barrier)
+            float sa = 0.f, sb = 0.f;
+#pragma unroll
+            for (int w8 = 0; w8 < NW; ++w8) {
+                sa += abp[w8][0];
+                sb += abp[w8][1];
+            }
+            gates[0] = sigmoidf_(sb);
+            gates[1] = a_ssm * softplusf_(sa + a_dt);
+        }
         if (own_qk) {
             const float nq = sqrtf((red[0][0] + red[0][1]) + (red[0][2] + red[0][3]));
             const float nk = sqrtf((red[1][0] + red[1][1]) + (red[1][2] + red[1][3]));

@@ -80,12 +80,15 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
 // Byte layout of one stage (es = activation element size, ss = state element
 // size): the state tile first, then the small inputs.
 struct StageLayout {
-    uint32_t cw, xr, zr, bytes;   // conv taps (q|k|v), raw rows [K+3][q|k|v], z rows [K]
-    __host__ __device__ StageLayout(int K, int es, int ss) {
+    // conv taps (q|k|v), raw rows [K+3][q|k|v], z rows [K]; then, with ssm_alpha / ssm_beta
+    // folded in (H > 0), the hidden rows [K][H], W_a[h] and W_b[h] (bf16)
+    uint32_t cw, xr, zr, ab, bytes;
+    __host__ __device__ StageLayout(int K, int es, int ss, int H) {
         cw = kD * kD * ss;
         xr = cw + 384 * 16;
         zr = xr + (K + 3) * 384 * es;
-        bytes = zr + K * 128 * es;
+        ab = (zr + K * 128 * es + 15) & ~15u;
+        bytes = H > 0 ? ab + (K + 2) * H * 2 : ab;
     }
 };
 
@@ -98,10 +101,11 @@ recurrent_stream_kernel(const RecParams p) {
     const int K = p.K, C = p.C, HvD = p.Hv * kD;
     const int r = p.Hv / p.Hk;
     const int n_groups = p.B * p.Hk;
-    const StageLayout L(K, es, ss);
+    const int H = p.ab_hidden ? p.ab_H : 0;
+    const StageLayout L(K, es, ss, H);
     // private copy of the current item's small inputs, after the stages
     uint8_t* cur = sm + kStages * L.bytes;
-    const uint32_t cur_bytes = L.bytes - L.cw;
+    const uint32_t cur_bytes = L.ab - L.cw;
     float* qk_s = reinterpret_cast<float*>(cur + ((cur_bytes + 15) & ~15u));   // [K][256] q_hat | k_hat
     float* v_s = qk_s + K * 256;                                                  // [K][128]
     float* o_s = v_s + K * 128;                                                   // [128]
@@ -109,7 +113,8 @@ recurrent_stream_kernel(const RecParams p) {
     float* part = red + 16;                                                       // [8]
     float* gates = part + 8;                                                      // [K][2]
     float* nw_s = gates + 2 * kMaxK;                                              // [128]
-    uint64_t* full = reinterpret_cast<uint64_t*>(nw_s + 128);                     // [kStages] stage landed
+    float* abp = nw_s + 128;                                  // [K][8 warps][2] folded a/b partial sums
+    uint64_t* full = reinterpret_cast<uint64_t*>(abp + 16 * kMaxK);               // [kStages] stage landed
     uint64_t* empty = full + kStages;                                              // [kStages] stage copied out
     uint64_t* never = empty + kStages;                                             // test stall: no arrivals
     volatile int* abort_s = reinterpret_cast<volatile int*>(never + 1);           // a wait gave up
@@ -155,6 +160,14 @@ recurrent_stream_kernel(const RecParams p) {
         }
         const Tact* zin = static_cast<const Tact*>(p.z) + static_cast<size_t>(b) * K * HvD + h * kD;
         for (int t = 0; t < K; ++t) bulk_g2s(base + L.zr + t * seg, zin + static_cast<size_t>(t) * HvD, seg, mb);
+        if (H > 0) {   // the folded projections' operands
+            const uint32_t rb = static_cast<uint32_t>(H) * 2;
+            const __nv_bfloat16* hid = static_cast<const __nv_bfloat16*>(p.ab_hidden) + static_cast<size_t>(b) * K * H;
+            for (int t = 0; t < K; ++t) bulk_g2s(base + L.ab + t * rb, hid + static_cast<size_t>(t) * H, rb, mb);
+            bulk_g2s(base + L.ab + K * rb, static_cast<const __nv_bfloat16*>(p.W_a) + static_cast<size_t>(h) * H, rb, mb);
+            bulk_g2s(base + L.ab + (K + 1) * rb, static_cast<const __nv_bfloat16*>(p.W_b) + static_cast<size_t>(h) * H,
+                     rb, mb);
+        }
     };
 
     // Bit 4 of dev_status marks every (sequence, v-head) of item i and later
@@ -198,7 +211,7 @@ recurrent_stream_kernel(const RecParams p) {
         const uint8_t* stg = sm + (i % kStages) * L.bytes;
         // gates for the item's tokens: plain loads, issued before the wait
         float a_raw = 0.f, b_raw = 0.f;
-        if (tid < K) {
+        if (tid < K && !p.ab_hidden) {
             const size_t gi = (static_cast<size_t>(b) * K + tid) * p.Hv + h;
             a_raw = ld_act(static_cast<const Tact*>(p.a_raw) + gi);
             b_raw = ld_act(static_cast<const Tact*>(p.b_raw) + gi);
@@ -211,9 +224,22 @@ recurrent_stream_kernel(const RecParams p) {
             sreg[rr] = StateIO<Ts>::ld(stg + ((warp * 16 + rr) * kD + 4 * lane) * ss);
         for (uint32_t e = tid * 16; e < cur_bytes; e += kSThreads * 16)
             *reinterpret_cast<uint4*>(cur + e) = *reinterpret_cast<const uint4*>(stg + L.cw + e);
-        if (tid < K) {
+        if (tid < K && !H) {
             gates[2 * tid] = sigmoidf_(b_raw);
             gates[2 * tid + 1] = a_ssm * softplusf_(a_raw + a_dt);
+        }
+        if (H > 0) {
+            // ssm_alpha / ssm_beta folded in: each compute thread's share of the dot products of
+            // the token's hidden row with W_a[h], W_b[h] (all in the stage), summed over warps below
+            const __nv_bfloat16* sab = reinterpret_cast<const __nv_bfloat16*>(stg + L.ab);
+            for (int t = 0; t < K; ++t) {
+                const float2 pr = ab_dot_part<false>(sab + t * H, sab + K * H, sab + (K + 1) * H, H, tid, kSThreads);
+                const float sa = warp_sum(pr.x), sb = warp_sum(pr.y);
+                if (lane == 0) {
+                    abp[(t * 8 + warp) * 2] = sa;
+                    abp[(t * 8 + warp) * 2 + 1] = sb;
+                }
+            }
         }
         // one decision for all compute warps, before anything is written: stop at the
         // first item whose stage did not land (what was read from it is discarded)
@@ -223,6 +249,18 @@ recurrent_stream_kernel(const RecParams p) {
             break;
         }
         if (tid == 0) tc::mbar_arrive(&empty[i % kStages]);   // the stage may be refilled
+        if (H > 0 && tid < K) {
+            // the folded a_raw, b_raw: the warps' partial sums (the next barrier orders them
+            // before step 7)
+            float sa = 0.f, sb = 0.f;
+#pragma unroll
+            for (int w8 = 0; w8 < 8; ++w8) {
+                sa += abp[(tid * 8 + w8) * 2];
+                sb += abp[(tid * 8 + w8) * 2 + 1];
+            }
+            gates[2 * tid] = sigmoidf_(sb);
+            gates[2 * tid + 1] = a_ssm * softplusf_(sa + a_dt);
+        }
 
         const float4* cw = reinterpret_cast<const float4*>(cur);                      // [384] taps
         const Tact* xr = reinterpret_cast<const Tact*>(cur + (L.xr - L.cw));           // [K+3][384]
@@ -337,17 +375,18 @@ recurrent_stream_kernel(const RecParams p) {
 
 }  // namespace
 
-size_t recurrent_stream_smem(int K, int act_dtype, bool state_bf16) {
+size_t recurrent_stream_smem(int K, int act_dtype, bool state_bf16, int ab_H) {
     const int es = act_dtype == 1 ? 2 : 4;
-    const StageLayout L(K, es, state_bf16 ? 2 : 4);
-    const size_t cur = ((L.bytes - L.cw + 15) & ~static_cast<size_t>(15));
-    const size_t misc = (static_cast<size_t>(K) * 384 + 128 + 16 + 8 + 2 * kMaxK + 128) * 4 + 2 * kStages * 8 + 16;
+    const StageLayout L(K, es, state_bf16 ? 2 : 4, ab_H);
+    const size_t cur = ((L.ab - L.cw + 15) & ~static_cast<size_t>(15));
+    const size_t misc = (static_cast<size_t>(K) * 384 + 128 + 16 + 8 + 2 * kMaxK + 128 + 16 * kMaxK) * 4 +
+                        2 * kStages * 8 + 16;
     return kStages * static_cast<size_t>(L.bytes) + cur + misc;
 }
 
 cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_dtype, int grid, cudaStream_t stream) {
     const bool sbf = (p.flags & kFlagStateBf16) != 0;
-    const size_t smem = recurrent_stream_smem(p.K, act_dtype, sbf);
+    const size_t smem = recurrent_stream_smem(p.K, act_dtype, sbf, p.ab_hidden ? p.ab_H : 0);
     auto go = [&](auto kernel) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;

@@ -41,6 +41,21 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_m
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same with bf16 A and B.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return idesc_f16(M, N, 0, 0, 0) | (1u << 7) | (1u << 10);
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzle
+// layout that a TMA copy with CU_TENSOR_MAP_SWIZZLE_128B writes: rows of 64
+// 16-bit elements (128 bytes), the 16-byte chunks of row r permuted by r mod 8,
+// 8-row groups 1024 bytes apart (SBO), the tile based on a 1024-byte boundary.
+// A K step of 16 elements inside the row advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (1ull << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -102,6 +117,18 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint3
                      smem_u32(smem_dst)),
                  "l"(gsrc), "r"(bytes), "r"(smem_u32(mbar))
                  : "memory");
+}
+
+// Tiled 2-D tensor copy global -> shared (TMA) of the box at (x, y) of the
+// tensor map `map` (a __grid_constant__ kernel parameter or global memory),
+// counted on `mbar` as transaction bytes.  x * element size must be a multiple
+// of 16 bytes; out-of-range parts of the box are filled with zeros.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* map, int x, int y, uint64_t* mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(mbar))
+        : "memory");
 }
 
 // Hint: bring `bytes` (multiple of 16) at `gsrc` into L2.

@@ -166,7 +166,26 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, int32_t B
                            int32_t* dev_status, gdn_stream_t stream);
 
 /*
- * gdn_verify_k -- speculative verify: B sequences, K tokens each (1 <= K <=
+ * gdn_decode_step_ab -- gdn_decode_step with the ssm_alpha and ssm_beta
+ * projections folded in (xwen CLAUDE.md page, "Architecture cheat sheet",
+ * "Gated DeltaNet layer": a_raw = ssm_alpha(hidden), b_raw = ssm_beta(hidden)).
+ * Instead of a_raw / b_raw the kernel reads the layer input and the two
+ * weights and forms, for sequence b and v-head h,
+ *   a_raw = sum_k hidden[b][k] W_a[h][k],   b_raw = sum_k hidden[b][k] W_b[h][k]
+ * in fp32 from the bf16 operands, and uses them unrounded (gdn_in_proj rounds
+ * its a_raw / b_raw outputs to bf16; here they never leave the chip).
+ *   hidden [B][H] bf16; W_a, W_b [H_v][H] bf16 (the [out][in] layout of
+ *   gdn_in_proj); H >= 8, H % 8 == 0 (else GDN_E_INVALID_ARG)
+ * Requires act_dtype = GDN_BF16 (GDN_E_UNSUPPORTED otherwise).  Everything
+ * else, including errors and dev_status, as gdn_decode_step.
+ */
+gdn_status gdn_decode_step_ab(const gdn_dims* dims, const gdn_weights* w, int32_t B, int32_t H,
+                              const void* x, const void* z, const void* hidden, const void* W_a,
+                              const void* W_b, void* conv_state, void* S, void* out,
+                              float* prenorm_out, int32_t* dev_status, gdn_stream_t stream);
+
+/*
+ * gdn_verify_k -- speculative verify: B sequences, K tokens each (1 <=
  * GDN_MAX_VERIFY_K), token p of sequence b at row b*K + p.  Walks the
  * recurrence through the K tokens and keeps a state checkpoint after every
  * position (the page's "Drafting" section: verify-walk rollback from

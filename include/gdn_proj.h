@@ -9,15 +9,33 @@
  * the gated RMSNorm output goes through ssm_out.  Hidden sizes on that page:
  * 5120 (27B, 16/48 heads) and 2048 (35B-A3B, 16/32 heads).
  *
- * Both calls are plain bf16 GEMMs with fp32 accumulation on the tensor cores,
- * run by cuBLASLt (out = in . W^T, W in the [out][in] layout of a linear
- * layer's weight).  Conventions as in gdn.h: caller-owned, 16-byte aligned
- * device buffers, asynchronous on `stream`, errors returned, outputs must not
- * overlap inputs.  Requires act_dtype = out_dtype = GDN_BF16
- * (GDN_E_UNSUPPORTED otherwise).  The workspace is optional scratch for
- * cuBLASLt (NULL / 0 allowed; a few MiB lets it pick faster kernels); the
- * library allocates no device memory.  One cuBLASLt handle per device is
- * created on first use and kept for the life of the process.
+ * Both calls are bf16 GEMMs with fp32 accumulation on the tensor cores
+ * (out = in . W^T, W in the [out][in] layout of a linear layer's weight),
+ * each output element rounded once to bf16 from its fp32 sum.  For T <= 256
+ * (decode and speculative-verify batches: the weights are read once and used
+ * by few rows, so the time is the weight stream) they run in the library's
+ * own weight-streaming kernel: 128-row tiles of W and the input streamed by
+ * TMA into shared memory, tcgen05 MMAs into tensor memory, K split over a
+ * cluster of up to 8 CTAs whose partial sums meet in distributed shared
+ * memory; gdn_in_proj's four GEMMs share one launch.  For T > 256 they run
+ * through cuBLASLt (tensor-bound; one cuBLASLt handle per device is created
+ * on first use and kept for the life of the process).  The order in which
+ * the fp32 sums are formed differs between the two paths.
+ *
+ * Conventions as in gdn.h: caller-owned, 16-byte aligned device buffers,
+ * asynchronous on `stream`, errors returned, outputs must not overlap inputs.
+ * Requires act_dtype = out_dtype = GDN_BF16 (GDN_E_UNSUPPORTED otherwise).
+ * The workspace is optional (NULL / 0 allowed; the library allocates no
+ * device memory).  For T <= 256, one of at least gdn_proj_workspace_bytes()
+ * lets the streaming kernel give every SM an equal share of the weights (runs
+ * of a 128-row tile's K split between CTAs add fp32 partial sums through it);
+ * without it each CTA streams whole tiles, which leaves SMs idle when there
+ * are fewer tiles than SMs.  For T > 256 it is cuBLASLt's scratch (a few MiB
+ * lets it pick faster kernels).  Calls that share a workspace must not
+ * overlap on the GPU.
+ * dev_status (optional, may be NULL) is one int32: the weight-streaming kernel
+ * ORs bit 4 into it when one of its bounded waits gave up (its outputs are
+ * then not written); the caller zeroes it and reads it after synchronising.
  */
 #ifndef GDN_PROJ_H
 #define GDN_PROJ_H
@@ -40,18 +58,30 @@ typedef struct {
  *   hidden [T][H]  ->  x [T][C], z [T][H_v*128], a_raw [T][H_v], b_raw [T][H_v]
  * (four GEMMs; each output element rounded once from its fp32 sum).
  * T == 0 is a no-op.  GDN_E_INVALID_ARG for T < 0, H < 8 or H % 8 != 0, null
- * pointers or overlaps; GDN_E_CUDA if cuBLASLt fails or finds no kernel.
+ * pointers or overlaps; GDN_E_ALIGNMENT for a device pointer off 16 bytes
+ * (dev_status: 4); GDN_E_CUDA if a launch fails, or cuBLASLt fails or finds
+ * no kernel.
  */
+/*
+ * gdn_proj_workspace_bytes -- workspace that lets gdn_in_proj and gdn_out_proj
+ * with these dims, T and H spread their weight streams over every SM of the
+ * current device (the larger of the two needs); 0 for T > 256 or invalid
+ * arguments.  Host-only query.
+ */
+size_t gdn_proj_workspace_bytes(const gdn_dims* dims, int32_t T, int32_t H);
+
 gdn_status gdn_in_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* hidden,
                        const gdn_in_proj_weights* w, void* x, void* z, void* a_raw, void* b_raw,
-                       void* workspace, size_t workspace_bytes, gdn_stream_t stream);
+                       void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                       gdn_stream_t stream);
 
 /*
  * gdn_out_proj -- ssm_out: y [T][H_v*128] (the mixer's out)  ->  out [T][H],
  * W_out [H][H_v*128] bf16.  Errors as gdn_in_proj.
  */
 gdn_status gdn_out_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* y, const void* W_out,
-                        void* out, void* workspace, size_t workspace_bytes, gdn_stream_t stream);
+                        void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        gdn_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -95,12 +95,14 @@ int main(void) {
 
     /* projections */
     gdn_in_proj_weights pw = {P(1), P(2), P(3), P(4)};
-    EXPECT(gdn_in_proj(&d, 4, 2048, P(5), &pw, P(6), P(7), P(8), P(9), NULL, 0, NULL), GDN_E_UNSUPPORTED);   /* fp32 out */
+    EXPECT(gdn_in_proj(&d, 4, 2048, P(5), &pw, P(6), P(7), P(8), P(9), NULL, 0, NULL, NULL), GDN_E_UNSUPPORTED);   /* fp32 out */
     d.out_dtype = GDN_BF16;   /* the projections run bf16 in and out */
-    EXPECT(gdn_in_proj(&d, -1, 2048, P(5), &pw, P(6), P(7), P(8), P(9), NULL, 0, NULL), GDN_E_INVALID_ARG);
-    EXPECT(gdn_in_proj(&d, 4, 2044, P(5), &pw, P(6), P(7), P(8), P(9), NULL, 0, NULL), GDN_E_INVALID_ARG);
-    EXPECT(gdn_in_proj(&d, 0, 2048, P(5), &pw, P(6), P(7), P(8), P(9), NULL, 0, NULL), GDN_OK);
-    EXPECT(gdn_out_proj(&d, 4, 2048, NULL, P(6), P(7), NULL, 0, NULL), GDN_E_INVALID_ARG);
+    EXPECT(gdn_in_proj(&d, -1, 2048, P(5), &pw, P(6), P(7), P(8), P(9), NULL, 0, NULL, NULL), GDN_E_INVALID_ARG);
+    EXPECT(gdn_in_proj(&d, 4, 2044, P(5), &pw, P(6), P(7), P(8), P(9), NULL, 0, NULL, NULL), GDN_E_INVALID_ARG);
+    EXPECT(gdn_in_proj(&d, 4, 2048, P(5), &pw, P(6), P(7), P(8), P(9), NULL, 0, (int32_t*)((char*)P(10) + 2), NULL),
+           GDN_E_ALIGNMENT);
+    EXPECT(gdn_in_proj(&d, 0, 2048, P(5), &pw, P(6), P(7), P(8), P(9), NULL, 0, NULL, NULL), GDN_OK);
+    EXPECT(gdn_out_proj(&d, 4, 2048, NULL, P(6), P(7), NULL, 0, NULL, NULL), GDN_E_INVALID_ARG);
 
     printf(fails ? "%d failures\n" : "ok\n", fails);
     return fails ? 1 : 0;

@@ -108,6 +108,30 @@ def test_decode_validation():
     assert _decode(d, _w(), pre=FAKE + 0x6000000) == 1   # prenorm overlaps out
 
 
+def _decode_ab(d, w, B=4, H=2048, hidden=FAKE + 0x2000000, **kw):
+    args = dict(z=FAKE + 0x1000000, Wa=FAKE + 0x7000000, Wb=FAKE + 0x8000000, cs=FAKE + 0x4000000,
+                S=FAKE + 0x5000000, out=FAKE + 0x6000000, pre=None, st=None)
+    args.update(kw)
+    return _call("gdn_decode_step_ab", ctypes.byref(d), ctypes.byref(w) if w is not None else None, B, H, FAKE,
+                 args["z"], hidden, args["Wa"], args["Wb"], args["cs"], args["S"], args["out"], args["pre"],
+                 args["st"], None)
+
+
+def test_decode_ab_validation():
+    """The decode step with ssm_alpha / ssm_beta folded in: H, the activation type, the three
+    projection pointers and their overlaps are checked before any CUDA call."""
+    d = _dims()
+    assert _decode_ab(d, _w(), B=0) == 0              # no-op
+    assert _decode_ab(d, _w(), H=0) == 1
+    assert _decode_ab(d, _w(), H=2044) == 1           # H not a multiple of 8
+    assert _decode_ab(_dims(act=0), _w()) == 2        # fp32 activations
+    assert _decode_ab(d, _w(), hidden=None) == 1
+    assert _decode_ab(d, _w(), Wa=None) == 1
+    assert _decode_ab(d, _w(), Wb=FAKE + 0x8000000 + 8) == 3
+    assert _decode_ab(d, _w(), out=FAKE + 0x2000000) == 1   # output overlaps hidden
+    assert _decode_ab(d, _w(), S=FAKE + 0x7000000) == 1     # state overlaps W_a
+
+
 def test_verify_and_commit_validation():
     d = _dims()
     w = _w()
@@ -177,8 +201,8 @@ def test_projection_validation():
     d_bf = _dims(out=1)
     w = gdn.GdnInProjWeights(FAKE * 0x100, FAKE * 0x200, FAKE * 0x300, FAKE * 0x400)
     outs = [FAKE * 0x500, FAKE * 0x600, FAKE * 0x700, FAKE * 0x800]
-    call = lambda dims, T, H, hid, ww, o=outs, ws=None, nws=0: L.gdn_in_proj(
-        ctypes.byref(dims), T, H, hid, ctypes.byref(ww) if ww is not None else None, *o, ws, nws, None)
+    call = lambda dims, T, H, hid, ww, o=outs, ws=None, nws=0, st=None: L.gdn_in_proj(
+        ctypes.byref(dims), T, H, hid, ctypes.byref(ww) if ww is not None else None, *o, ws, nws, st, None)
     assert call(d, 4, 2048, FAKE * 0x900, w) == 2                  # fp32 output type: unsupported
     assert call(_dims(act=0, out=1), 4, 2048, FAKE * 0x900, w) == 2
     assert call(d_bf, 0, 2048, FAKE * 0x900, w) == 0                # T = 0: no-op
@@ -189,10 +213,13 @@ def test_projection_validation():
     assert call(d_bf, 4, 2048, FAKE * 0x900 + 8, w) == 3
     assert call(d_bf, 4, 2048, FAKE * 0x900, w, ws=None, nws=64) == 1   # workspace size without a workspace
     assert call(d_bf, 4, 2048, outs[0], w) == 1                     # hidden overlaps x
-    assert L.gdn_out_proj(ctypes.byref(d_bf), 4, 2048, FAKE * 0x100, FAKE * 0x200, FAKE * 0x100, None, 0, None) == 1
-    assert L.gdn_out_proj(ctypes.byref(d_bf), 4, 2048, FAKE * 0x100, FAKE * 0x200, FAKE * 0x300 + 4, None, 0,
-                          None) == 3
-    assert L.gdn_out_proj(ctypes.byref(d), 4, 2048, FAKE * 0x100, FAKE * 0x200, FAKE * 0x300, None, 0, None) == 2
+    assert call(d_bf, 4, 2048, FAKE * 0x900, w, st=FAKE * 0xa00 + 2) == 3   # status word off 4 bytes
+    assert call(d_bf, 4, 2048, FAKE * 0x900, w, st=outs[1]) == 1    # status word inside z
+    op = lambda dims, y, o, st=None: L.gdn_out_proj(ctypes.byref(dims), 4, 2048, y, FAKE * 0x200, o, None, 0, st, None)
+    assert op(d_bf, FAKE * 0x100, FAKE * 0x100) == 1
+    assert op(d_bf, FAKE * 0x100, FAKE * 0x300 + 4) == 3
+    assert op(d, FAKE * 0x100, FAKE * 0x300) == 2
+    assert op(d_bf, FAKE * 0x100, FAKE * 0x300, st=FAKE * 0x300) == 1   # status word inside out
 
 
 def test_prefill_validation():

@@ -1,7 +1,14 @@
 """GPU parity of the projections either side of the mixer (gdn_in_proj,
 gdn_out_proj) against the fp64 oracle on the same bf16 inputs.  Each output
 is one fp32 sum of exact bf16 products rounded once to bf16, so the bound is
-half a bf16 ulp of the reference plus 1e-4 for the fp32 accumulation."""
+half a bf16 ulp of the reference plus 1e-4 for the fp32 accumulation.
+
+T <= 256 runs the library's weight-streaming kernel: with a workspace of
+gdn_proj_workspace_bytes() every SM takes an equal run of k-blocks and tiles
+split between CTAs meet through fp32 partial sums; without one, a CTA per
+whole tile.  Both are run, with zero fill past the last weight row and past
+the last multiple of 64 in K.  Larger T runs cuBLASLt.  The status word of
+the streaming kernel must stay clear."""
 import numpy as np
 import pytest
 import torch
@@ -23,6 +30,9 @@ def _close(got, ref):
 
 def _run(c, T, rows=None, ws_bytes=0):
     d = gdn.make_dims(c.Hk, c.Hv, torch.bfloat16, torch.bfloat16)
+    if ws_bytes == "auto":
+        ws_bytes = gdn.gdn_proj_workspace_bytes(d, T, c.H)
+        assert ws_bytes > 0
     dv = lambda t: t.cuda().contiguous()
     C, HvD = 128 * (2 * c.Hk + c.Hv), 128 * c.Hv
     x = torch.empty(T, C, device="cuda", dtype=torch.bfloat16)
@@ -31,9 +41,12 @@ def _run(c, T, rows=None, ws_bytes=0):
     b = torch.empty(T, c.Hv, device="cuda", dtype=torch.bfloat16)
     out = torch.empty(T, c.H, device="cuda", dtype=torch.bfloat16)
     ws = torch.empty(ws_bytes, device="cuda", dtype=torch.uint8) if ws_bytes else None
-    gdn.gdn_in_proj(d, dv(c.hidden), dv(c.W_qkv), dv(c.W_z), dv(c.W_a), dv(c.W_b), x, z, a, b, workspace=ws)
-    gdn.gdn_out_proj(d, dv(c.y), dv(c.W_out), out, workspace=ws)
+    st = torch.zeros(1, device="cuda", dtype=torch.int32)
+    gdn.gdn_in_proj(d, dv(c.hidden), dv(c.W_qkv), dv(c.W_z), dv(c.W_a), dv(c.W_b), x, z, a, b, workspace=ws,
+                    dev_status=st)
+    gdn.gdn_out_proj(d, dv(c.y), dv(c.W_out), out, workspace=ws, dev_status=st)
     torch.cuda.synchronize()
+    assert int(st.item()) == 0
     sel = slice(None) if rows is None else rows
     refs = oracle.in_proj(c.hidden[sel], c.W_qkv, c.W_z, c.W_a, c.W_b)
     for got, ref in zip((x, z, a, b), refs):
@@ -41,10 +54,12 @@ def _run(c, T, rows=None, ws_bytes=0):
     _close(out[sel], oracle.out_proj(c.y[sel], c.W_out))
 
 
-@pytest.mark.parametrize("T,ws", [(300, 0), (64, 4 << 20), (48, 0), (17, 1 << 20), (1, 0)])
+@pytest.mark.parametrize("T,ws", [(300, 0), (257, 4 << 20), (256, "auto"), (192, 0), (129, "auto"), (64, "auto"),
+                                  (64, 0), (48, "auto"), (17, 1 << 20), (1, "auto"), (1, 0)])
 def test_projections_35b_dims(T, ws):
-    """Hidden 2048, 16/32 heads: a ragged prefill, the B=64 decode batch, 48 and 17 rows, and a
-    single token, with and without a workspace."""
+    """Hidden 2048, 16/32 heads: ragged prefills either side of the 256-row switch to cuBLASLt,
+    the B=64 K=3 verify batch, the B=64 decode batch, 48 and 17 rows, and a single token, with
+    and without a workspace."""
     c = gdn_inputs.make_proj_case(T=T, H=2048, Hk=16, Hv=32, seed=200 + T)
     _run(c, T, ws_bytes=ws)
 
@@ -55,3 +70,20 @@ def test_projections_27b_dims_full_size_sampled():
     c = gdn_inputs.make_proj_case(T=T, H=5120, Hk=16, Hv=48, seed=210)
     rows = torch.randperm(T, generator=torch.Generator().manual_seed(3))[:24].sort().values
     _run(c, T, rows=rows, ws_bytes=32 << 20)
+
+
+@pytest.mark.parametrize("T", [64, 192])
+def test_projections_27b_dims_decode_batches(T):
+    """Hidden 5120, 16/48 heads at the decode and verify batch sizes (the streaming kernel splits
+    K of the input GEMMs two ways and of ssm_out four ways)."""
+    c = gdn_inputs.make_proj_case(T=T, H=5120, Hk=16, Hv=48, seed=220 + T)
+    _run(c, T, ws_bytes="auto")
+
+
+@pytest.mark.parametrize("T", [5, 100])
+def test_projections_ragged_hidden(T):
+    """H = 2056: K ends 8 past a multiple of 64 (zero-filled copies), ssm_out's 2056 rows end 8
+    into their last 128-row tile, and ssm_alpha / ssm_beta are 4-row GEMMs."""
+    c = gdn_inputs.make_proj_case(T=T, H=2056, Hk=2, Hv=4, seed=230 + T)
+    _run(c, T, ws_bytes="auto")
+    _run(c, T)
