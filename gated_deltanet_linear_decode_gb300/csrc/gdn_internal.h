@@ -2,6 +2,7 @@
 // kernels of libgdn.so (not installed; the public surface is include/gdn.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -85,6 +86,7 @@ struct CommitParams {
 
 // Chunked prefill over packed sequences.
 struct PrefillParams {
+    CUtensorMap xmap;        // x [T][C] bf16, boxes of [67 positions][64 channels], 128-byte swizzle
     int n_seq;
     long long T;
     int max_len;
@@ -142,6 +144,11 @@ struct ResetParams {
     const int* dev_status;   // [N*Hv]
 };
 cudaError_t launch_state_reset(const ResetParams& p, cudaStream_t stream);
+
+// A TMA tensor map of a 2-D bf16 tensor [outer][inner] (row pitch inner * 2 bytes, 16-byte
+// aligned) with boxes of [box_outer <= 256][64] elements in the 128-byte swizzle layout;
+// false if the driver refuses it (gdn_tma.cu).
+bool make_tensor_map_bf16_sw128(CUtensorMap* m, const void* base, int inner, int outer, int box_outer);
 
 // One GEMM of a projection call: out [T][rows] = in [T][K] . W [rows][K]^T (bf16).
 struct ProjGemm {

@@ -37,21 +37,29 @@ constexpr uint32_t kTbe = 114688;      // T diag(beta e^Gam) hi +0, lo +8192 (fi
 constexpr uint32_t kAf = 131072;       // fp32 [64][pf::kTS] A
 constexpr uint32_t kTf = 148480;       // fp32 [64][pf::kTS] T
 constexpr uint32_t kDm = 167424;       // fp32 [64][65] decay matrix; then the solve's scratch (11520 bytes)
-// Raw rows are staged channel-group major: 16 bytes (8 channels) of row rr for
-// channel group cg at ((cg) * kXrows + rr) * 16, so that a warp reading one
-// channel group of 32 consecutive rows touches 512 consecutive bytes.
+// Raw rows arrive by TMA in boxes of [67 positions][64 channels] (128-byte rows, the
+// 16-byte chunks of row R permuted by R mod 8, boxes 1024-byte aligned): channel group
+// cg (8 channels) of position row R is at box (cg / 8), row R, chunk (cg % 8) ^ (R % 8),
+// so a warp reading one channel group of 32 consecutive rows hits every bank once per
+// 8 rows.
 constexpr int kXrows = 67;             // positions c0-3 .. c0+63
-constexpr uint32_t kXqk = 131072;      // raw q|k rows: groups 0-15 q, 16-31 k (consumed before kAf.. are used)
-constexpr uint32_t kXv = 184064;       // raw v rows: groups 0-15
-constexpr uint32_t kMisc = 201216;     // TMEM base, mbarrier, error flag
-constexpr uint32_t kGates = 201280;    // per v-head of the group: 6 x [64] fp32 (below)
+constexpr uint32_t kXBoxBytes = kXrows * 128;
+constexpr uint32_t kXBoxStride = 9216;  // 1024-byte aligned boxes
+constexpr uint32_t kXqk = 131072;      // raw q|k rows: boxes 0-1 q, 2-3 k (consumed before kAf.. are used)
+constexpr uint32_t kXv = 184320;       // raw v rows of one v-head: boxes 0-1
+constexpr uint32_t kMisc = 202112;     // TMEM base, mbarriers (MMA, q|k rows, v rows), error flag
+constexpr uint32_t kGates = 202176;    // per v-head of the group: 6 x [64] fp32 (below)
+__device__ __forceinline__ uint32_t xrow_off(int cg, int R) {
+    return static_cast<uint32_t>((cg >> 3) * kXBoxStride + R * 128 + (((cg & 7) ^ (R & 7)) << 4));
+}
 constexpr uint32_t kGateBytes = 6 * 256;
 // then the conv taps of the current v-head, float4 [128]
 __host__ __device__ inline uint32_t taps_v_off(int G) { return kGates + static_cast<uint32_t>(G) * kGateBytes; }
 __host__ __device__ inline uint32_t prep_smem(int G) { return taps_v_off(G) + 128 * 16; }
-static_assert(kXqk + 32 * kXrows * 16 <= kDm, "q/k staging overlaps the decay matrix");
+static_assert(kXqk % 1024 == 0 && kXv % 1024 == 0 && kXBoxStride >= kXBoxBytes, "TMA boxes of the raw rows");
+static_assert(kXqk + 3 * kXBoxStride + kXBoxBytes <= kDm, "q/k staging overlaps the decay matrix");
 static_assert(kDm + 64 * 65 * 4 <= kXv, "decay matrix overlaps the v staging");
-static_assert(kXv + 16 * kXrows * 16 <= kMisc, "v staging overlaps the barriers");
+static_assert(kXv + kXBoxStride + kXBoxBytes <= kMisc && kMisc + 40 <= kGates, "v staging overlaps the barriers");
 static_assert(kAf + 64 * pf::kTS * 4 <= kTf && kTf + 64 * pf::kTS * 4 <= kDm, "A / T tiles overlap");
 
 constexpr uint32_t kColQK = 0, kColU = 64, kColW = 128, kPrepTmemCols = 256;
@@ -67,6 +75,9 @@ struct Ctx {
     uint32_t phase;
     int* err_s;
     bool no_flow;   // thread 0: the flow-control wait gave up once, so it is skipped from then on
+    uint64_t* xbar;   // the q|k raw rows of the item landed (TMA)
+    uint64_t* vbar;   // a v-head's raw rows landed (TMA)
+    uint32_t xphase, vphase;
 };
 
 __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& cx) {
@@ -135,36 +146,53 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
         tc::fence_after_sync();
     };
 
-    // ---- stage the raw rows of positions c0-3 .. c0+n-1 (left context from the
-    // carried conv state in the first chunk of a sequence) and the conv taps
-    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x);
+    // ---- stage the raw rows of positions c0-3 .. c0+63 by TMA (one thread; positions past the
+    // tensor read as zeros, positions past the sequence are never used) and the conv taps.
+    // In the first chunk of a sequence, rows 0-2 (positions -3 .. -1) are replaced, once
+    // landed, by the carried conv state (zeros with zero_init).
     const __nv_bfloat16* cst = static_cast<const __nv_bfloat16*>(p.conv_state) + static_cast<size_t>(s) * 3 * C;
-    const int nrow = n + 3;
-    auto stage16 = [&](uint8_t* dst, int pos, int ch) {
-        if (pos >= 0)
-            tc::cp_async16(dst, x + static_cast<size_t>(t0 + pos) * C + ch);
-        else if (!p.zero_init)
-            tc::cp_async16(dst, cst + (3 + pos) * C + ch);
-        else
-            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    const int y0 = t0 + c0 - 3;
+    auto left_context = [&](uint32_t box0, int nbox, int ch0, int idx, int cnt) {
+        // rows 0-2 of boxes box0 .. box0+nbox-1 (channels ch0 + 64 * box ..), 8 channels a thread
+        for (int e = idx; e < nbox * 3 * 8; e += cnt) {
+            const int bx = e / 24, R = (e / 8) % 3, c = e & 7;
+            const uint4 v = p.zero_init ? make_uint4(0, 0, 0, 0)
+                                        : *reinterpret_cast<const uint4*>(cst + R * C + ch0 + 64 * bx + 8 * c);
+            *reinterpret_cast<uint4*>(sm + box0 + bx * kXBoxStride + R * 128 + ((c ^ R) << 4)) = v;
+        }
     };
-    for (int e = tid; e < nrow * 32; e += kPrepThreads) {
-        const int rr = e >> 5, cg = e & 31, sec = cg >> 4;
-        stage16(sm + kXqk + (cg * kXrows + rr) * 16, c0 - 3 + rr, sec * Hk * kD + kh * kD + 8 * (cg & 15));
+    auto stage_v_rows = [&](int h) {   // one thread
+        tc::fence_proxy_async();   // the generic reads of the previous v rows come first
+        tc::mbar_expect_tx(cx.vbar, 2 * kXBoxBytes);
+        for (int bx = 0; bx < 2; ++bx)
+            tc::tma_load_2d(sm + kXv + bx * kXBoxStride, &p.xmap, 2 * Hk * kD + h * kD + 64 * bx, y0, cx.vbar);
+    };
+    if (tid == 0) {
+        tc::fence_proxy_async();
+        tc::mbar_expect_tx(cx.xbar, 4 * kXBoxBytes);
+        for (int bx = 0; bx < 4; ++bx)
+            tc::tma_load_2d(sm + kXqk + bx * kXBoxStride, &p.xmap, (bx >> 1) * Hk * kD + kh * kD + 64 * (bx & 1), y0,
+                            cx.xbar);
+        stage_v_rows(kh);
     }
     static_assert(kPrepThreads == 256, "one q/k channel's taps per thread");
     tc::cp_async16(sm + kTb + 16 * tid,
                    reinterpret_cast<const float4*>(p.conv_w) + ((tid >> 7) * Hk * kD + kh * kD + (tid & 127)));
-    // v-head h's raw rows and conv taps, by threads idx = 0 .. cnt-1
-    auto stage_v = [&](int h, int idx, int cnt) {
-        for (int e = idx; e < nrow * 16; e += cnt) {
-            const int rr = e >> 4, cg = e & 15;
-            stage16(sm + kXv + (cg * kXrows + rr) * 16, c0 - 3 + rr, 2 * Hk * kD + h * kD + 8 * cg);
-        }
+    // v-head h's conv taps, by threads idx = 0 .. cnt-1
+    auto stage_v_taps = [&](int h, int idx, int cnt) {
         for (int c = idx; c < kD; c += cnt)
             tc::cp_async16(sm + taps_v_off(G) + 16 * c, reinterpret_cast<const float4*>(p.conv_w) + (2 * Hk * kD + h * kD + c));
     };
-    stage_v(kh, tid, kPrepThreads);
+    stage_v_taps(kh, tid, kPrepThreads);
+    // wait for v-head h's raw rows (all threads), then its left context in a first chunk
+    auto land_v_rows = [&](int h) {
+        if (!tc::mbar_wait(cx.vbar, cx.vphase, kWaitLimit)) atomicExch(err_s, 1);
+        cx.vphase ^= 1u;
+        if (c0 == 0) {
+            left_context(kXv, 2, 2 * Hk * kD + h * kD, tid, kPrepThreads);
+            pf::prep_sync();
+        }
+    };
 
     // ---- gates of every v-head of the group while the rows land: beta, g, e^g; then
     // warp g scans head g's g in fp64 into Gam, e^Gam and e^{Gam_last - Gam}
@@ -207,6 +235,12 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
         }
     }
     tc::cp_async_drain();
+    if (!tc::mbar_wait(cx.xbar, cx.xphase, kWaitLimit)) atomicExch(err_s, 1);
+    cx.xphase ^= 1u;
+    if (c0 == 0) {
+        left_context(kXqk, 2, kh * kD, tid, kPrepThreads);
+        left_context(kXqk + 2 * kXBoxStride, 2, Hk * kD + kh * kD, tid, kPrepThreads);
+    }
     pf::prep_sync();
 
     // ---- q_hat, k_hat: conv, SiLU, clamp L2 -> [Q;K] hi/lo in shared memory.
@@ -231,7 +265,7 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
                 float win[4][8];
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
-                    pf::bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + kXqk + (cg * kXrows + t + r) * 16), win[r]);
+                    pf::bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + kXqk + xrow_off(cg, t + r)), win[r]);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float v = pf::silu_fast(pf::conv4(w[i], win[0][i], win[1][i], win[2][i], win[3][i]));
@@ -297,6 +331,7 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
     for (int g = 0; g < G; ++g) {
         const int h = kh + g * Hk;
         uint8_t* vrec = p.ws_v + (static_cast<size_t>(gc) * Hv + h) * pf::kVRec;
+        land_v_rows(h);
         const float* beta_s = gate(g, kBeta);
         const float* eg_s = gate(g, kEg);
         const float* egam_s = gate(g, kEgam);
@@ -319,7 +354,7 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
                     float win[4][8], vv[8];
 #pragma unroll
                     for (int r = 0; r < 4; ++r)
-                        pf::bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + kXv + (cg * kXrows + t + r) * 16), win[r]);
+                        pf::bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm + kXv + xrow_off(cg, t + r)), win[r]);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) vv[i] = pf::silu_fast(pf::conv4(w[i], win[0][i], win[1][i], win[2][i], win[3][i]));
                     tc::split8(vv, vh, vl);
@@ -389,7 +424,10 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
         // the next v-head's raw rows start loading while the diagonal blocks are solved
         pf::unit_lower_inverse<kPrepThreads>(Af, reinterpret_cast<float*>(sm + kTf), reinterpret_cast<float*>(sm + kDm),
                                              [&](int i) {
-                                                 if (g + 1 < G) stage_v(h + Hk, i, kPrepThreads - 64);
+                                                 if (g + 1 < G) {
+                                                     if (i == 0) stage_v_rows(h + Hk);
+                                                     stage_v_taps(h + Hk, i, kPrepThreads - 64);
+                                                 }
                                              });
         // T diag(beta) and T diag(beta e^Gam): thread -> row tid%64, 16 columns
         {

@@ -73,14 +73,17 @@ __global__ void chunk_table_kernel(const int* cu_seqlens, int n_seq, int* chunk_
 constexpr int kThreads = chain::kStateThreads;
 static_assert(kThreads >= prep::kPrepThreads, "the preparation role needs 8 warps");
 
+// The preparation role bases its map on the next 1024-byte boundary (the 128-byte swizzle
+// of its TMA boxes repeats every 1024 bytes), hence the extra 1024 bytes.
 __host__ __device__ inline uint32_t fused_smem(int G) {
-    return prep::smem_bytes(G) > chain::kStateSmem ? prep::smem_bytes(G) : chain::kStateSmem;
+    return prep::smem_bytes(G) + 1024 > chain::kStateSmem ? prep::smem_bytes(G) + 1024 : chain::kStateSmem;
 }
 
 // CTAs [0, n_chain) run chains j = blockIdx.x, blockIdx.x + n_chain, ... of the
 // n_seq * H_v (sequence-major); the others take preparation items.
 template <typename Tout>
-__global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const PrefillParams p, int n_chain, int* counter) {
+__global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid_constant__ PrefillParams p, int n_chain,
+                                                                    int* counter) {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ int item_s;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -100,19 +103,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const Prefil
         return;
     }
     if (warp >= prep::kPrepThreads / 32) return;   // the preparation role runs on warps 0-7
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + prep::kMisc);
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + prep::kMisc + 8);
-    int* err_s = reinterpret_cast<int*>(sm + prep::kMisc + 16);
+    uint8_t* smp = sm + ((1024u - (tc::smem_u32(sm) & 1023u)) & 1023u);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smp + prep::kMisc);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(smp + prep::kMisc + 8);
+    int* err_s = reinterpret_cast<int*>(smp + prep::kMisc + 16);
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(smp + prep::kMisc + 24);
+    uint64_t* vbar = reinterpret_cast<uint64_t*>(smp + prep::kMisc + 32);
     if (warp == 0) tc::tmem_alloc(tslot, prep::kPrepTmemCols);
     if (tid == 0) {
         tc::mbar_init(mbar, 1);
+        tc::mbar_init(xbar, 1);
+        tc::mbar_init(vbar, 1);
         *err_s = 0;
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.xmap)) : "memory");
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tc::fence_before_sync();
     pf::prep_sync();
     tc::fence_after_sync();
-    prep::Ctx cx{*tslot, mbar, 0u, err_s};
+    prep::Ctx cx{*tslot, mbar, 0u, err_s, false, xbar, vbar, 0u, 0u};
     const int n_items = p.n_chunks * p.Hk;
     for (;;) {
         // items in chunk order: every chain finds its next chunk among the earliest
@@ -120,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const Prefil
         pf::prep_sync();
         const int it = item_s;   // read by all before thread 0 can write the next one (the item syncs first)
         if (it >= n_items) break;
-        prep::item(p, it / p.Hk, it % p.Hk, sm, cx);
+        prep::item(p, it / p.Hk, it % p.Hk, smp, cx);
     }
     tc::fence_before_sync();
     pf::prep_sync();
@@ -159,6 +168,8 @@ cudaError_t launch_tensor_core_prefill(const PrefillParams& p0, int out_dtype, c
     p.chunk_lo = 0;
     p.chunk_hi = p.n_chunks;
     int* counter = reinterpret_cast<int*>(p.ws_v - 256);
+    // the raw rows of a chunk (positions c0-3 .. c0+63) come in by TMA, 64 channels a box
+    if (!make_tensor_map_bf16_sw128(&p.xmap, p.x, p.C, static_cast<int>(p.T), prep::kXrows)) return cudaErrorInvalidValue;
     int dev = 0, sms = 0, l2 = 0;
     cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;

@@ -289,36 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1) proj_stream_kernel(const __grid_c
     if (warp == 5) tc::tmem_dealloc(tmem, static_cast<uint32_t>(p.tmem_cols));
 }
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled from the driver, looked up once (no link against libcuda).
-EncodeTiled encode_fn() {
-    static std::once_flag once;
-    static EncodeTiled fn = nullptr;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiled>(f);
-    });
-    return fn;
-}
-
 // 2-D bf16 tensor [outer][inner] (row pitch inner * 2 bytes), box [box_outer][64], 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, int inner, int outer, int box_outer) {
-    EncodeTiled enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_outer)};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return make_tensor_map_bf16_sw128(m, base, inner, outer, box_outer);
 }
 
 }  // namespace
