@@ -87,7 +87,7 @@ def prefill_flops(T, Hv):
 _COMMON_SOURCES = ("gdn_api.cu", "gdn_common.cuh", "gdn_internal.h", "gdn_tc.cuh")
 PART_SOURCES = {
     "prefill": _COMMON_SOURCES + ("gdn_prefill_tc.cu", "gdn_prefill_prep.cuh", "gdn_prefill_chain.cuh",
-                                  "gdn_prefill_simt.cu", "gdn_prefill_tc.cuh"),
+                                  "gdn_prefill_simt.cu", "gdn_prefill_tc.cuh", "gdn_tma.cu"),
     "decode": _COMMON_SOURCES + ("gdn_recurrent.cu", "gdn_recurrent_stream.cu"),
 }
 
@@ -620,12 +620,33 @@ def run_extras(dev, warmup, reps):
     return out
 
 
+def proj_part(dev):
+    """The input and output projections at the B=64 decode batch, 35B dims (hidden 2048,
+    16/32 heads), through the weight-streaming kernel with its workspace (profiling aid)."""
+    import gated_deltanet_linear_decode_gb300 as gdn
+    T, H, Hk, Hv = 64, 2048, 16, 32
+    c = gdn_inputs.make_proj_case(T=T, H=H, Hk=Hk, Hv=Hv, seed=7)
+    d = gdn.make_dims(Hk, Hv, torch.bfloat16, torch.bfloat16)
+    t = {k: getattr(c, k).to(dev) for k in ("hidden", "W_qkv", "W_z", "W_a", "W_b", "y", "W_out")}
+    bf = dict(device=dev, dtype=torch.bfloat16)
+    x, z = torch.empty(T, 128 * (2 * Hk + Hv), **bf), torch.empty(T, 128 * Hv, **bf)
+    a, b, po = torch.empty(T, Hv, **bf), torch.empty(T, Hv, **bf), torch.empty(T, H, **bf)
+    ws = torch.empty(gdn.gdn_proj_workspace_bytes(d, T, H), device=dev, dtype=torch.uint8)
+
+    def run():
+        gdn.gdn_in_proj(d, t["hidden"], t["W_qkv"], t["W_z"], t["W_a"], t["W_b"], x, z, a, b, workspace=ws)
+        gdn.gdn_out_proj(d, t["y"], t["W_out"], po, workspace=ws)
+    return run
+
+
 def run_part(args):
     """Warm-up then timed launches of one part only (profiling aid)."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     wl = Workload(dev, args.prefill_tokens)
-    fn = {"prefill": wl.prefill, "decode": wl.decode, "verify": wl.verify}[args.only]
+    fn = {"prefill": wl.prefill, "decode": wl.decode, "verify": wl.verify}.get(args.only)
+    if args.only == "proj":
+        fn = proj_part(dev)
     for _ in range(args.warmup + args.steps):
         wl.flush_l2()
         fn()
@@ -754,7 +775,7 @@ def main():
                     help="skip the batch-1 graph decode and the varlen T=65536 prefill (timed outside the step)")
     ap.add_argument("--prefill-tokens", type=int, default=8192,
                     help="with --only prefill: the sequence length (a smaller case for profiling)")
-    ap.add_argument("--only", choices=["prefill", "decode", "verify"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "verify", "proj"], default=None,
                     help="run only one part of the step (for profiling); no JSON line")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
