@@ -17,7 +17,12 @@ Timing: CUDA events on the launching stream, W >= 3 warm-up steps, L2 flushed
 (a 256 MiB write) before every timed step, outside the timed region; every
 input is also larger than L2.  e2e: the same step through the C ABI with the
 step's inputs copied from pinned host memory and its outputs read back, inside
-the timed region.  Under torchrun (N > 1) each rank runs its own replica (no
+the timed region, the copies pipelined against the compute on two side streams:
+the decode and verify inputs first (those calls run while the prefill's inputs
+arrive), then the prefill's 8192 tokens through gdn_prefill_chunked in 4
+segments of 2048 (state carried on the device; the chunk grid, hence every
+result, is that of one call), segment i+1's inputs copied in while segment i
+runs and each segment's outputs copied out as soon as it is done.  Under torchrun (N > 1) each rank runs its own replica (no
 collective on the data path: the layer shards by sequence and head) and the
 slowest rank's time is used.
 
@@ -284,15 +289,73 @@ class Workload:
         g.gdn_commit_ring(self.d_dims, self.vc.K, self.vc.K + 1, self.acc, self.v_ckc, self.r_conv, self.r_cur)
         return 2
 
-    def h2d(self):
-        for src, dst in ((self.h, self.p_in), (self.hd, self.d_in), (self.hv, self.v_in)):
-            for k in src:
-                dst[k].copy_(src[k], non_blocking=True)
+    def e2e_step(self, n_seg=4, small_first=True):
+        """One step from host buffers to host buffers through the C ABI, with the transfers
+        pipelined against the compute on two side streams.  The decode and verify inputs (a few
+        MB) go first, so those two calls run while the prefill's inputs are still arriving; the
+        prefill's tokens then go through gdn_prefill_chunked in n_seg segments (the conv and
+        recurrent state carried on the device from one call to the next, the chunk grid
+        unchanged, so the results are those of one call), segment i+1's inputs copied in while
+        segment i computes and each segment's outputs copied out as soon as it is done.
+        Returns the number of library kernels launched."""
+        cur = torch.cuda.current_stream()
+        if not hasattr(self, "s_in"):
+            self.s_in, self.s_out = torch.cuda.Stream(self.p_out.device), torch.cuda.Stream(self.p_out.device)
+        T = self.pc.T
+        seg = T // n_seg
+        assert seg * n_seg == T and seg % 64 == 0
+        if getattr(self, "cu_seg_len", None) != seg:
+            self.cu_seg_h = torch.tensor([0, seg], dtype=torch.int32)
+            self.cu_seg_d = self.cu_seg_h.to(self.p_out.device)
+            self.cu_seg_len = seg
+        ev_in = [torch.cuda.Event() for _ in range(n_seg + 1)]
+        ev_done = [torch.cuda.Event() for _ in range(n_seg + 1)]
+        self.s_in.wait_stream(cur)
+        self.s_out.wait_stream(cur)
+        def small_in():
+            for src, dst in ((self.hd, self.d_in), (self.hv, self.v_in)):
+                for k in src:
+                    dst[k].copy_(src[k], non_blocking=True)
+            ev_in[n_seg].record(self.s_in)
 
-    def d2h(self):
-        self.h_pout.copy_(self.p_out, non_blocking=True)
-        self.h_dout.copy_(self.d_out, non_blocking=True)
-        self.h_vout.copy_(self.v_out, non_blocking=True)
+        with torch.cuda.stream(self.s_in):
+            if small_first:
+                small_in()
+            for i in range(n_seg):
+                for k in self.h:
+                    self.p_in[k][i * seg:(i + 1) * seg].copy_(self.h[k][i * seg:(i + 1) * seg], non_blocking=True)
+                ev_in[i].record(self.s_in)
+            if not small_first:
+                small_in()
+        n = 0
+        if small_first:
+            cur.wait_event(ev_in[n_seg])
+            n += self.decode() + self.verify()
+            ev_done[n_seg].record(cur)
+        pi = self.p_in
+        for i in range(n_seg):
+            cur.wait_event(ev_in[i])
+            sl = slice(i * seg, (i + 1) * seg)
+            self.gdn.gdn_prefill_chunked(self.p_dims, self.p_w, self.cu_seg_h, self.cu_seg_d, pi["x"][sl], pi["z"][sl],
+                                         pi["a_raw"][sl], pi["b_raw"][sl], self.p_conv, self.p_S, self.p_out[sl],
+                                         zero_init=(i == 0), workspace=self.p_ws)
+            n += 3
+            ev_done[i].record(cur)
+        if not small_first:
+            cur.wait_event(ev_in[n_seg])
+            n += self.decode() + self.verify()
+            ev_done[n_seg].record(cur)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(ev_done[n_seg])
+            self.h_dout.copy_(self.d_out, non_blocking=True)
+            self.h_vout.copy_(self.v_out, non_blocking=True)
+            for i in range(n_seg):
+                self.s_out.wait_event(ev_done[i])
+                sl = slice(i * seg, (i + 1) * seg)
+                self.h_pout[sl].copy_(self.p_out[sl], non_blocking=True)
+        cur.wait_stream(self.s_out)
+        cur.wait_stream(self.s_in)
+        return n
 
     def io_bytes(self):
         h2d = sum(t.numel() * t.element_size() for d in (self.h, self.hd, self.hv) for t in d.values())
@@ -344,15 +407,18 @@ def run_gpu(args, rank, world):
     wall = time.perf_counter() - t_wall0
     clocks = sampler.stop()
 
-    # e2e: host buffers in, results out, inside the timed region
+    # e2e: host buffers in, results out, inside the timed region (after W untimed steps that
+    # create the side streams and the segment tables)
+    for _ in range(args.warmup):
+        wl.flush_l2()
+        wl.e2e_step()
+    torch.cuda.synchronize()
     e2e_ms = []
     for _ in range(max(1, args.steps)):
         wl.flush_l2()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        wl.h2d()
-        wl.prefill(); wl.decode(); wl.verify()
-        wl.d2h()
+        wl.e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))

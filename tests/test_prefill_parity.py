@@ -114,6 +114,36 @@ def test_split_and_resume():
     assert G.conv_bits_equal(conv, ref.conv_state, c.act_dtype)
 
 
+def test_prefill_in_segments_is_bit_identical():
+    """A sequence prefilled in four calls of 256 tokens (zero initial state in the first, the
+    conv and recurrent state carried on the device through the others) gives the outputs, the
+    final state and the conv state of one call over all 1024 tokens bit for bit: the chunk
+    grid is the same (256 is a multiple of 64), so is every operation.  (The bench's end-to-end
+    leg streams its prefill this way to overlap the host copies.)"""
+    c = gdn_inputs.make_case("seg", Hk=4, Hv=12, lengths=[1024], S0="zero", conv0="zero", seed=31)
+    d, w = G.dims(c, torch.bfloat16), G.weights(c)
+    dev = lambda t: G.dev(t)
+    x, z, a, b = dev(c.x), dev(c.z), dev(c.a_raw), dev(c.b_raw)
+
+    def run(segs):
+        conv = torch.zeros(1, 3, c.C, device="cuda", dtype=torch.bfloat16)
+        S = torch.zeros(1, c.Hv, 128, 128, device="cuda")
+        out = torch.empty(c.T, c.Hv * 128, device="cuda", dtype=torch.bfloat16)
+        L = c.T // segs
+        cu_h = torch.tensor([0, L], dtype=torch.int32)
+        ws = torch.empty(gdn.gdn_prefill_workspace_bytes(d, 1, L), device="cuda", dtype=torch.uint8)
+        for i in range(segs):
+            sl = slice(i * L, (i + 1) * L)
+            gdn.gdn_prefill_chunked(d, w, cu_h, G.dev(cu_h), x[sl], z[sl], a[sl], b[sl], conv, S, out[sl],
+                                    zero_init=(i == 0), workspace=ws)
+        torch.cuda.synchronize()
+        return out, S, conv
+
+    one, four = run(1), run(4)
+    for u, v in zip(one, four):
+        assert torch.equal(u, v)
+
+
 def test_varlen_t65536_all_sequences():
     """The packed varlen workload (8 sequences, T=65536, nonzero initial
     state) at full size on the GPU, in the launch configuration the bench
