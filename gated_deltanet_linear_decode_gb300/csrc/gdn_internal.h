@@ -114,7 +114,7 @@ struct PrefillParams {
     int chunk_lo, chunk_hi;  // global chunk range of this launch of the two kernels
     int* chunk_base;         // device [n_seq+1]
     uint8_t* ws_v;           // v-head records, [n_chunks][Hv]
-    int* ready;              // [n_chunks][Hk] ready flags of the records (zeroed per call)
+    int* ready;              // [n_chunks][Hv] ready flags of the records, one per v-head (zeroed per call)
     int* consumed;           // [n_chunks][Hk] chains of the group done with the chunk's records (zeroed per call)
     int ahead;               // the preparation role writes chunk c once chunk c - ahead is consumed
     int* abort_flag;         // set by a chain that gave up: the preparation role stops waiting on chains

@@ -162,9 +162,9 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
     auto vrec = [&](int c) { return vrec0 + static_cast<size_t>(c) * Hv * pf::kVRec; };
     // Acquire the ready flag of chunk c's records (set by the preparation role once
     // they are written); bounded in time, and given up as soon as another role has.
-    const int* ready = p.ready + static_cast<size_t>(cbase) * p.Hk + kh;
+    const int* ready = p.ready + static_cast<size_t>(cbase) * Hv + h;
     auto wait_ready = [&](int c) -> bool {
-        const int* f = ready + static_cast<size_t>(c) * p.Hk;
+        const int* f = ready + static_cast<size_t>(c) * Hv;
         if (pf::ld_acquire(f)) return true;
         const uint64_t tstart = pf::global_ns();
         uint32_t ns = 64;

@@ -4,8 +4,9 @@
 // "Architecture cheat sheet", "Gated DeltaNet layer": conv1d k=4 without bias,
 // SiLU, clamp L2 norm, tiled heads, beta = sigmoid(b), g = ssm_a softplus(a + dt_bias)).
 //
-// One item = (chunk, q/k head kh), worked by 8 warps of a CTA (they meet at
-// named barrier 1, never at the CTA-wide barrier).  While the chunk's raw rows and
+// One item = (chunk, q/k head kh) and a range of the group's v-heads (all of
+// them, but one each for the call's first chunk), worked by 8 warps of a CTA
+// (they meet at named barrier 1, never at the CTA-wide barrier).  While the chunk's raw rows and
 // conv taps land it computes the gates of every v-head h with h mod H_k = kh
 // (tiled heads): beta, g, Gam (fp64 scan), e^Gam, e^{Gam_last-Gam}.  It computes
 // q_hat and k_hat of the chunk once -- and from them, while they are in
@@ -80,7 +81,10 @@ struct Ctx {
     uint32_t xphase, vphase;
 };
 
-__device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& cx) {
+// Item (chunk gc, q/k head kh), v-heads g_lo .. g_hi-1 of the group (a whole item takes
+// 0 .. G-1; the first chunk of a call is split into one item per v-head so that the chains
+// can start sooner).
+__device__ void item(const PrefillParams& p, int gc, int kh, int g_lo, int g_hi, uint8_t* sm, Ctx& cx) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hk = p.Hk, Hv = p.Hv, C = p.C;
 
@@ -173,7 +177,7 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
         for (int bx = 0; bx < 4; ++bx)
             tc::tma_load_2d(sm + kXqk + bx * kXBoxStride, &p.xmap, (bx >> 1) * Hk * kD + kh * kD + 64 * (bx & 1), y0,
                             cx.xbar);
-        stage_v_rows(kh);
+        stage_v_rows(kh + g_lo * Hk);
     }
     static_assert(kPrepThreads == 256, "one q/k channel's taps per thread");
     tc::cp_async16(sm + kTb + 16 * tid,
@@ -183,7 +187,7 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
         for (int c = idx; c < kD; c += cnt)
             tc::cp_async16(sm + taps_v_off(G) + 16 * c, reinterpret_cast<const float4*>(p.conv_w) + (2 * Hk * kD + h * kD + c));
     };
-    stage_v_taps(kh, tid, kPrepThreads);
+    stage_v_taps(kh + g_lo * Hk, tid, kPrepThreads);
     // wait for v-head h's raw rows (all threads), then its left context in a first chunk
     auto land_v_rows = [&](int h) {
         if (!tc::mbar_wait(cx.vbar, cx.vphase, kWaitLimit)) atomicExch(err_s, 1);
@@ -296,7 +300,7 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
                 // group -> fp16 hi/lo records (the gates are known by now)
                 const uint32_t go = tc::cl_off(t, ch, 64);
 #pragma unroll 1
-                for (int g = 0; g < G; ++g) {
+                for (int g = g_lo; g < g_hi; ++g) {
                     const float e = gate(g, sec == 0 ? kEgam : kElast)[t];
                     float sv[8];
 #pragma unroll
@@ -328,7 +332,7 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
     }
 
     const float* Af = reinterpret_cast<const float*>(sm + kAf);
-    for (int g = 0; g < G; ++g) {
+    for (int g = g_lo; g < g_hi; ++g) {
         const int h = kh + g * Hk;
         uint8_t* vrec = p.ws_v + (static_cast<size_t>(gc) * Hv + h) * pf::kVRec;
         land_v_rows(h);
@@ -384,7 +388,7 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
             }
         }
         pf::prep_sync();
-        if (g == 0) wait_mma();   // the [Q;K] K^T products
+        if (g == g_lo) wait_mma();   // the [Q;K] K^T products
         else tc::fence_after_sync();
         // P (rows t < 64 of the product) -> record; A (rows 64 + t) -> shared fp32
         {
@@ -424,7 +428,7 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
         // the next v-head's raw rows start loading while the diagonal blocks are solved
         pf::unit_lower_inverse<kPrepThreads>(Af, reinterpret_cast<float*>(sm + kTf), reinterpret_cast<float*>(sm + kDm),
                                              [&](int i) {
-                                                 if (g + 1 < G) {
+                                                 if (g + 1 < g_hi) {
                                                      if (i == 0) stage_v_rows(h + Hk);
                                                      stage_v_taps(h + Hk, i, kPrepThreads - 64);
                                                  }
@@ -496,14 +500,16 @@ __device__ void item(const PrefillParams& p, int gc, int kh, uint8_t* sm, Ctx& c
         }
         tc::cp_async_drain();
         tc::fence_before_sync();
-    }
-    // publish: every record write of this item is visible at GPU scope before the
-    // ready flag is (the chain role acquires the flag before reading the records)
-    __threadfence();
-    pf::prep_sync();
-    if (tid == 0) {
-        if (p.dev_status && *err_s) atomicOr(p.dev_status + s * Hv + kh, 16);
-        pf::st_release(p.ready + static_cast<size_t>(gc) * Hk + kh, 1);
+        // publish v-head h: its records (this head's part and the Q', K' written before the
+        // loop) are complete once every thread is through the barrier; one thread then
+        // makes them visible at GPU scope (cumulative through the barrier) before the
+        // head's ready flag, which the chain role acquires before reading them
+        pf::prep_sync();
+        if (tid == 0) {
+            __threadfence();
+            if (p.dev_status && *err_s) atomicOr(p.dev_status + s * Hv + h, 16);
+            pf::st_release(p.ready + static_cast<size_t>(gc) * Hv + h, 1);
+        }
     }
 }
 

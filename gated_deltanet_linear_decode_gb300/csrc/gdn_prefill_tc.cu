@@ -1,9 +1,10 @@
 // gdn_prefill_tc.cu -- the tensor-core chunked prefill (bf16 activations) as
 // one persistent kernel with two roles that run side by side:
 //   * preparation CTAs (gdn_prefill_prep.cuh) take (chunk, q/k head) items in
-//     chunk order from a global counter and write, for every v-head of the
-//     q/k head's group, the chunk's state-independent record (W^T, U, Q', K',
-//     P, decay vectors), then set the item's ready flag;
+//     chunk order from a global counter (the first chunk as one item per
+//     v-head) and write, for every v-head of the q/k head's group, the chunk's
+//     state-independent record (W^T, U, Q', K', P, decay vectors), setting each
+//     v-head's ready flag as soon as its record is complete;
 //   * chain CTAs (gdn_prefill_chain.cuh) each walk the chunks of one
 //     (sequence, v-head) at a time, the state on chip, reading every record as
 //     soon as its flag is set -- while it is still in L2 -- and dropping it from
@@ -122,14 +123,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
     pf::prep_sync();
     tc::fence_after_sync();
     prep::Ctx cx{*tslot, mbar, 0u, err_s, false, xbar, vbar, 0u, 0u};
-    const int n_items = p.n_chunks * p.Hk;
+    // items in chunk order, so every chain finds its next chunk among the earliest: first the
+    // call's chunk 0 as one item per v-head (its chains start after one head's work), then
+    // (chunk, q/k head) items of all the v-heads of the group
+    const int G = p.Hv / p.Hk;
+    const int n_first = p.Hv;
+    const int n_items = n_first + (p.n_chunks - 1) * p.Hk;
     for (;;) {
-        // items in chunk order: every chain finds its next chunk among the earliest
         if (tid == 0) item_s = atomicAdd(counter, 1);
         pf::prep_sync();
         const int it = item_s;   // read by all before thread 0 can write the next one (the item syncs first)
         if (it >= n_items) break;
-        prep::item(p, it / p.Hk, it % p.Hk, smp, cx);
+        if (it < n_first)
+            prep::item(p, 0, it % p.Hk, it / p.Hk, it / p.Hk + 1, smp, cx);
+        else
+            prep::item(p, 1 + (it - n_first) / p.Hk, (it - n_first) % p.Hk, 0, G, smp, cx);
     }
     tc::fence_before_sync();
     pf::prep_sync();
@@ -146,7 +154,7 @@ size_t flags_bytes(size_t n_chunks_bound, int Hk) { return (n_chunks_bound * Hk 
 // chunks bound every packing of T tokens.
 size_t tc_prefill_workspace_bytes(int Hk, int Hv, int n_seq, long long T) {
     const size_t nc = static_cast<size_t>((T + kChunk - 1) / kChunk) + static_cast<size_t>(n_seq);
-    return pf::table_bytes(n_seq) + 2 * flags_bytes(nc, Hk) + 256 +
+    return pf::table_bytes(n_seq) + flags_bytes(nc, Hv) + flags_bytes(nc, Hk) + 256 +
            nc * static_cast<size_t>(Hv) * pf::kVRec;
 }
 
@@ -156,7 +164,7 @@ void tc_prefill_bind_workspace(PrefillParams& p) {
     p.chunk_base = reinterpret_cast<int*>(base);
     base += pf::table_bytes(p.n_seq);
     p.ready = reinterpret_cast<int*>(base);
-    base += flags_bytes(nc, p.Hk);
+    base += flags_bytes(nc, p.Hv);
     p.consumed = reinterpret_cast<int*>(base);
     base += flags_bytes(nc, p.Hk);
     p.ws_v = base + 256;   // the item counter and the abort flag sit in the 256 bytes before the records
@@ -176,7 +184,7 @@ cudaError_t launch_tensor_core_prefill(const PrefillParams& p0, int out_dtype, c
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess) return e;
     const int n_chains = p.n_seq * p.Hv;
-    const int n_items = p.n_chunks * p.Hk;
+    const int n_items = p.Hv + (p.n_chunks - 1) * p.Hk;
     // One chain per CTA while the chains take at most half the SMs; beyond that, one
     // v-head per chain CTA (every CTA then walks every sequence once), or a third of
     // the SMs.  The preparation role takes the rest, and at least one SM.
@@ -201,7 +209,7 @@ cudaError_t launch_tensor_core_prefill(const PrefillParams& p0, int out_dtype, c
     } else {
         p.ahead = p.n_chunks;   // gc < n_chunks: never gated
     }
-    chunk_table_kernel<<<1, 256, 0, stream>>>(p.cu_seqlens, p.n_seq, p.chunk_base, p.ready, p.n_chunks * p.Hk,
+    chunk_table_kernel<<<1, 256, 0, stream>>>(p.cu_seqlens, p.n_seq, p.chunk_base, p.ready, p.n_chunks * p.Hv,
                                               p.consumed, p.n_chunks * p.Hk, counter);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
