@@ -49,6 +49,8 @@ constexpr int kCtrlWarp = kConvWarps + kEpiWarps;   // MMA issue
 constexpr int kCopyWarp = kCtrlWarp + 1;            // bulk copies of the records
 constexpr int kStateThreads = (kConvWarps + kEpiWarps + 2) * 32;
 constexpr int kConvThreads = kConvWarps * 32, kEpiThreads = kEpiWarps * 32;
+// The chain role's barrier: its 14 warps (named barrier 5; the CTA may hold idle warps too).
+__device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 5, %0;" ::"n"(kStateThreads) : "memory"); }
 
 // shared memory map (bytes)
 constexpr uint32_t kQs = 0;           // Q' hi +0, lo +16384       (64 t x 128 i, canonical 64 rows)
@@ -107,7 +109,7 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
     if (cb >= ce) {
         // an empty sequence ends with its initial state: zeros under zero_init (written by the first launch)
         if (nch_s == 0 && p.zero_init && p.chunk_lo == 0)
-            for (int e = tid; e < kD * kD * ss / 16; e += blockDim.x) reinterpret_cast<uint4*>(Sg)[e] = make_uint4(0, 0, 0, 0);
+            for (int e = tid; e < kD * kD * ss / 16; e += kStateThreads) reinterpret_cast<uint4*>(Sg)[e] = make_uint4(0, 0, 0, 0);
         return;
     }
     const bool zero_init = p.zero_init && cb == 0;
@@ -121,7 +123,7 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
     const uint32_t sb = tc::smem_u32(sm);
     const int kh = h % p.Hk;
 
-    __syncthreads();   // the previous chain of this CTA is done with every barrier
+    chain_sync();   // the previous chain of this CTA is done with every barrier
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t cnt = 1;
@@ -135,7 +137,7 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tc::fence_before_sync();
-    __syncthreads();
+    chain_sync();
     tc::fence_after_sync();
 
     // Bounded wait that also gives up as soon as another role has timed out.
@@ -248,7 +250,7 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
     // test hook: a wait that nothing ends, so every role takes its give-up path at once
     if (tid == 0 && (p.flags & kFlagTestStall) && !tc::mbar_wait(bars + kNever, 0, 1 << 12)) *err_s = 1;
     tc::fence_before_sync();
-    __syncthreads();
+    chain_sync();
     tc::fence_after_sync();
 
     bool bad = false;
@@ -532,7 +534,7 @@ __device__ void run(const PrefillParams& p, int s, int h, uint8_t* sm, uint32_t 
     }
 
     tc::fence_before_sync();
-    __syncthreads();
+    chain_sync();
     if (tid == 0 && *err_s) atomicExch(p.abort_flag, 1);   // no preparation CTA waits on this chain any more
     if (p.dev_status) {
         int st = 0;

@@ -28,7 +28,7 @@
 namespace gdn {
 namespace prep {
 
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 512;   // 16 warps
 
 // shared memory map (bytes)
 constexpr uint32_t kQKs = 0;           // [Q;K] hi +0, lo +32768   (128 rows x 128, canonical)
@@ -137,7 +137,7 @@ __device__ void item(const PrefillParams& p, int gc, int kh, int g_lo, int g_hi,
     int* err_s = cx.err_s;
     const uint32_t sb = tc::smem_u32(sm);
     const uint32_t tmem = cx.tmem;
-    const int quarter = warp & 3, chalf = warp >> 2;
+    const int quarter = warp & 3, cq = warp >> 2;   // TMEM lane quarter; column quarter of a 64-wide tile
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float* ghi_s = nullptr;
@@ -179,9 +179,9 @@ __device__ void item(const PrefillParams& p, int gc, int kh, int g_lo, int g_hi,
                             cx.xbar);
         stage_v_rows(kh + g_lo * Hk);
     }
-    static_assert(kPrepThreads == 256, "one q/k channel's taps per thread");
-    tc::cp_async16(sm + kTb + 16 * tid,
-                   reinterpret_cast<const float4*>(p.conv_w) + ((tid >> 7) * Hk * kD + kh * kD + (tid & 127)));
+    if (tid < 256)   // one q/k channel's taps per thread
+        tc::cp_async16(sm + kTb + 16 * tid,
+                       reinterpret_cast<const float4*>(p.conv_w) + ((tid >> 7) * Hk * kD + kh * kD + (tid & 127)));
     // v-head h's conv taps, by threads idx = 0 .. cnt-1
     auto stage_v_taps = [&](int h, int idx, int cnt) {
         for (int c = idx; c < kD; c += cnt)
@@ -248,18 +248,18 @@ __device__ void item(const PrefillParams& p, int gc, int kh, int g_lo, int g_hi,
     pf::prep_sync();
 
     // ---- q_hat, k_hat: conv, SiLU, clamp L2 -> [Q;K] hi/lo in shared memory.
-    // Warp w owns staged channel groups 4w .. 4w+3 (q for w < 4, k for w >= 4;
+    // Warp w owns staged channel groups 2w, 2w+1 (q for w < 8, k for w >= 8;
     // their conv taps held in registers), lanes = tokens lane and 32 + lane; the
-    // four warps of a section meet in shared memory (the decay-matrix area,
+    // eight warps of a section meet in shared memory (the decay-matrix area,
     // unused until later) to form each token's norm.
     {
-        const int sec = warp >> 2;
-        float* ssq = reinterpret_cast<float*>(sm + kDm);   // [8 warps][64 tokens]
-        float val[2][4][8];
+        const int sec = warp >> 3;
+        float* ssq = reinterpret_cast<float*>(sm + kDm);   // [16 warps][64 tokens]
+        float val[2][2][8];
         float ss[2] = {0.f, 0.f};
 #pragma unroll
-        for (int gq = 0; gq < 4; ++gq) {
-            const int cg = 4 * warp + gq;   // 0..31
+        for (int gq = 0; gq < 2; ++gq) {
+            const int cg = 2 * warp + gq;   // 0..31
             float4 w[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) w[i] = taps_qk[sec * kD + 8 * (cg & 15) + i];
@@ -284,15 +284,16 @@ __device__ void item(const PrefillParams& p, int gc, int kh, int g_lo, int g_hi,
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             const int t = 32 * hf + lane;
-            const float* q4 = ssq + 4 * sec * 64 + t;
-            const float inv = rsqrtf(fmaxf((q4[0] + q4[64]) + (q4[128] + q4[192]), p.eps * p.eps));   // 1 / max(||x||, eps)
+            const float* q8 = ssq + 8 * sec * 64 + t;
+            const float sum = ((q8[0] + q8[64]) + (q8[128] + q8[192])) + ((q8[256] + q8[320]) + (q8[384] + q8[448]));
+            const float inv = rsqrtf(fmaxf(sum, p.eps * p.eps));   // 1 / max(||x||, eps)
 #pragma unroll
-            for (int gq = 0; gq < 4; ++gq) {
+            for (int gq = 0; gq < 2; ++gq) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) val[hf][gq][i] *= inv;
                 uint4 vh, vl;
                 tc::split8(val[hf][gq], vh, vl);
-                const int ch = 8 * ((4 * warp + gq) & 15);
+                const int ch = 8 * ((2 * warp + gq) & 15);
                 const uint32_t so = tc::cl_off(64 * sec + t, ch, 128);
                 *reinterpret_cast<uint4*>(sm + kQKs + so) = vh;
                 *reinterpret_cast<uint4*>(sm + kQKs + 32768 + so) = vl;
@@ -342,11 +343,10 @@ __device__ void item(const PrefillParams& p, int gc, int kh, int g_lo, int g_hi,
         const float* elast_s = gate(g, kElast);
         ghi_s = gate(g, kGhi);
         glo_s = gate(g, kGlo);
-        // v: conv, SiLU -> V hi/lo (64 r x 128 j); warp w: channel groups 2w, 2w+1
+        // v: conv, SiLU -> V hi/lo (64 r x 128 j); warp w: channel group w
         // (taps in registers), lanes = tokens lane and 32 + lane
-#pragma unroll
-        for (int gq = 0; gq < 2; ++gq) {
-            const int cg = 2 * warp + gq;
+        {
+            const int cg = warp;
             float4 w[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) w[i] = taps_v[8 * cg + i];
@@ -374,10 +374,10 @@ __device__ void item(const PrefillParams& p, int gc, int kh, int g_lo, int g_hi,
         // e^Gam and e^{Gam_last - Gam_t} -> record
         {
             float* Dm = reinterpret_cast<float*>(sm + kDm);
-            const int tt = tid & 63, r0 = (tid >> 6) * 16, rs = min(r0 + 15, tt);
+            const int tt = tid & 63, r0 = (tid >> 6) * 8, rs = min(r0 + 7, tt);
             float val = rs >= r0 ? __expf(dgam(tt, rs)) : 0.f;
 #pragma unroll
-            for (int i = 15; i >= 0; --i) {
+            for (int i = 7; i >= 0; --i) {
                 const int r = r0 + i;
                 Dm[tt * 65 + r] = r <= rs ? val : 0.f;
                 if (r <= rs) val *= eg_s[r];
@@ -394,32 +394,32 @@ __device__ void item(const PrefillParams& p, int gc, int kh, int g_lo, int g_hi,
         {
             const float* Dm = reinterpret_cast<const float*>(sm + kDm);
             float* Afw = reinterpret_cast<float*>(sm + kAf);
-            float v[32];
+            float v[16];
             const int t = row & 63;
-            tc::tmem_ld32(tl + kColQK + 32 * chalf, v);
+            tc::tmem_ld16(tl + kColQK + 16 * cq, v);
             if (row < 64) {
 #pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
+                for (int g8 = 0; g8 < 2; ++g8) {
                     float pv[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) pv[i] = Dm[t * 65 + 32 * chalf + 8 * g8 + i] * v[8 * g8 + i];
+                    for (int i = 0; i < 8; ++i) pv[i] = Dm[t * 65 + 16 * cq + 8 * g8 + i] * v[8 * g8 + i];
                     uint4 ph, pl;
                     tc::split8(pv, ph, pl);
-                    const uint32_t o = tc::cl_off(t, 32 * chalf + 8 * g8, 64);
+                    const uint32_t o = tc::cl_off(t, 16 * cq + 8 * g8, 64);
                     *reinterpret_cast<uint4*>(vrec + pf::kRecPhi + o) = ph;
                     *reinterpret_cast<uint4*>(vrec + pf::kRecPlo + o) = pl;
                 }
             } else {
                 const float bt = beta_s[t];
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {   // 16-byte stores: a row per lane, no bank conflicts
+                for (int i = 0; i < 16; i += 4) {   // 16-byte stores: a row per lane, no bank conflicts
                     float a4[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const int r = 32 * chalf + i + k;
+                        const int r = 16 * cq + i + k;
                         a4[k] = r < t ? bt * Dm[t * 65 + r] * v[i + k] : 0.f;
                     }
-                    *reinterpret_cast<float4*>(Afw + t * pf::kTS + 32 * chalf + i) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+                    *reinterpret_cast<float4*>(Afw + t * pf::kTS + 16 * cq + i) = make_float4(a4[0], a4[1], a4[2], a4[3]);
                 }
             }
         }
@@ -436,9 +436,9 @@ __device__ void item(const PrefillParams& p, int gc, int kh, int g_lo, int g_hi,
         // T diag(beta) and T diag(beta e^Gam): thread -> row tid%64, 16 columns
         {
             const float* Tf = reinterpret_cast<const float*>(sm + kTf);
-            const int tr = tid & 63, r0 = (tid >> 6) * 16;
-#pragma unroll
-            for (int g8 = 0; g8 < 2; ++g8) {
+            const int tr = tid & 63, r0 = (tid >> 6) * 8;
+            {
+                constexpr int g8 = 0;
                 float a8[8], b8[8];
                 const bool lower = (r0 >> 4) <= (tr >> 4);   // T is block lower triangular
                 float t8[8] = {};
@@ -484,19 +484,19 @@ __device__ void item(const PrefillParams& p, int gc, int kh, int g_lo, int g_hi,
         wait_mma();
         // W^T -> fp16 hi (rows i) and U^T -> fp32 (rows j) into the record
         {
-            float v[32];
-            tc::tmem_ld32(tl + kColW + 32 * chalf, v);
+            float v[16];
+            tc::tmem_ld16(tl + kColW + 16 * cq, v);
 #pragma unroll
-            for (int g8 = 0; g8 < 4; ++g8) {
+            for (int g8 = 0; g8 < 2; ++g8) {
                 uint4 wh, wl;
                 tc::split8(v + 8 * g8, wh, wl);
-                *reinterpret_cast<uint4*>(vrec + pf::kRecW + tc::cl_off(row, 32 * chalf + 8 * g8, 128)) = wh;
+                *reinterpret_cast<uint4*>(vrec + pf::kRecW + tc::cl_off(row, 16 * cq + 8 * g8, 128)) = wh;
             }
-            tc::tmem_ld32(tl + kColU + 32 * chalf, v);
+            tc::tmem_ld16(tl + kColU + 16 * cq, v);
             float4* U4 = reinterpret_cast<float4*>(vrec + pf::kRecU);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                U4[(8 * chalf + q) * kD + row] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int q = 0; q < 4; ++q)
+                U4[(4 * cq + q) * kD + row] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
         tc::cp_async_drain();
         tc::fence_before_sync();

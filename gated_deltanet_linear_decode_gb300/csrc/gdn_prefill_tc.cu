@@ -71,8 +71,9 @@ __global__ void chunk_table_kernel(const int* cu_seqlens, int n_seq, int* chunk_
     if (tid == 0) chunk_base[n_seq] = carry_s;
 }
 
-constexpr int kThreads = chain::kStateThreads;
-static_assert(kThreads >= prep::kPrepThreads, "the preparation role needs 8 warps");
+// 512 threads: the preparation role's 16 warps; the chain role uses the first 14.
+constexpr int kThreads = 512;
+static_assert(kThreads >= prep::kPrepThreads && kThreads >= chain::kStateThreads, "the roles' warps");
 
 // The preparation role bases its map on the next 1024-byte boundary (the 128-byte swizzle
 // of its TMA boxes repeats every 1024 bytes), hence the extra 1024 bytes.
@@ -89,16 +90,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
     __shared__ int item_s;
     const int tid = threadIdx.x, warp = tid >> 5;
     if (static_cast<int>(blockIdx.x) < n_chain) {
+        if (warp >= chain::kStateThreads / 32) return;   // the chain role runs on warps 0-13
         uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + chain::kBar + 8 * chain::kNumBars);
         if (warp == 0) tc::tmem_alloc(tslot, chain::kTmemCols);
         tc::fence_before_sync();
-        __syncthreads();
+        chain::chain_sync();
         tc::fence_after_sync();
         const uint32_t tmem = *tslot;
         const int n_chains = p.n_seq * p.Hv;
         for (int j = blockIdx.x; j < n_chains; j += n_chain) chain::run<Tout>(p, j / p.Hv, j % p.Hv, sm, tmem);
         tc::fence_before_sync();
-        __syncthreads();
+        chain::chain_sync();
         tc::fence_after_sync();
         if (warp == 0) tc::tmem_dealloc(tmem, chain::kTmemCols);
         return;

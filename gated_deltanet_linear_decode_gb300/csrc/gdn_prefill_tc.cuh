@@ -44,7 +44,8 @@ __host__ __device__ inline size_t table_bytes(int n_seq) {
 // ---------------------------------------------------------------- role synchronisation
 // The preparation role runs on warps 0-7 of its CTA and meets at named barrier
 // 1 (the CTA's other warps have left), never at the CTA-wide barrier 0.
-__device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// The preparation role's barrier: its 16 warps (named barrier 1, never the CTA-wide one).
+__device__ __forceinline__ void prep_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 // Ready flags: a release store by the producer after its records are written,
 // an acquire load by the consumer before it reads them.
@@ -159,11 +160,11 @@ __device__ __forceinline__ void mac16x2x4(const float* a0, const float* a1, cons
 // them as zero).  Hf is fp32 scratch for nine 16 x 16 blocks of row stride 20
 // (11520 bytes).  While threads 0-63 solve the diagonal blocks, threads
 // 64 .. kThreads-1 run side(i) with i = tid - 64 (work of the caller's that
-// needs no barrier of its own).  Ends with a barrier of the 256 threads.
+// needs no barrier of its own).  Ends with a barrier of the role's threads.
 constexpr int kTS = 68;
 template <int kThreads, typename Side>
 __device__ void unit_lower_inverse(const float* Af, float* Tf, float* Hf, Side&& side) {
-    static_assert(kThreads == 256, "tilings below assume 256 threads");
+    static_assert(kThreads >= 256, "tilings below use threads 0-255");
     constexpr int kHS = 20;                  // row stride of a scratch block
     const int tid = threadIdx.x;
     if (tid < 64) {
