@@ -162,6 +162,6 @@ constexpr int kProjStreamMaxRows = 256;   // the weight-streaming kernel takes T
 // one CTA per 128-row tile.  status: optional, bit 4.
 size_t proj_stream_workspace_bytes(const int* rows, int n_gemm, int T, int K);
 cudaError_t launch_proj_stream(const ProjGemm* g, int n_gemm, const void* in, int T, int K, void* workspace,
-                               size_t workspace_bytes, int* status, cudaStream_t stream);
+                               size_t workspace_bytes, int* status, bool test_stall, cudaStream_t stream);
 
 }  // namespace gdn

@@ -167,7 +167,8 @@ gdn_status gdn_in_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* h
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (T <= gdn::kProjStreamMaxRows) {
         const gdn::ProjGemm g[4] = {{w->W_qkv, x, C}, {w->W_z, z, HvD}, {w->W_a, a_raw, Hv}, {w->W_b, b_raw, Hv}};
-        return gdn::launch_proj_stream(g, 4, hidden, T, H, workspace, workspace_bytes, dev_status, st) == cudaSuccess
+        return gdn::launch_proj_stream(g, 4, hidden, T, H, workspace, workspace_bytes, dev_status,
+                                       (dims->flags & GDN_FLAG_TEST_STALL) != 0, st) == cudaSuccess
                    ? GDN_OK
                    : GDN_E_CUDA;
     }
@@ -196,6 +197,7 @@ gdn_status gdn_out_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* 
     if (T <= gdn::kProjStreamMaxRows) {
         const gdn::ProjGemm g[1] = {{W_out, out, H}};
         return gdn::launch_proj_stream(g, 1, y, T, HvD, workspace, workspace_bytes, dev_status,
+                                       (dims->flags & GDN_FLAG_TEST_STALL) != 0,
                                        reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                    ? GDN_OK
                    : GDN_E_CUDA;

@@ -62,7 +62,10 @@ struct alignas(64) ProjParams {
     int* counter;                 // [tiles] (workspace, zero at launch), or null
     int max_parts;
     int* status;                  // optional: bit 4 when a wait gave up
+    int test_stall;               // GDN_FLAG_TEST_STALL: the MMA thread first waits on a barrier nothing arrives on
 };
+
+constexpr int kStallLimit = 1 << 12;   // polls of the test stall
 
 __device__ __forceinline__ long long first_block(long long c, long long total, int G) { return c * total / G; }
 // The CTA whose range holds k-block x: the largest c with first_block(c) <= x.
@@ -84,7 +87,8 @@ __global__ void __launch_bounds__(kThreads, 1) proj_stream_kernel(const __grid_c
     uint64_t* done = empty + stages;    // [2]: accumulator b of a segment is complete
     uint64_t* freed = done + 2;         // [2]: the read-out is done with accumulator b
     uint64_t* drain = freed + 2;        // every MMA of this CTA has completed
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* never = drain + 1;        // test stall: nothing arrives
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(never + 1);
     int* bad = reinterpret_cast<int*>(tslot + 1);
     int* last_s = bad + 1;
 
@@ -112,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_stream_kernel(const __grid_c
         tc::mbar_init(freed, 128);
         tc::mbar_init(freed + 1, 128);
         tc::mbar_init(drain, 1);
+        tc::mbar_init(never, 1);
         *bad = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         // the first stages' copies go out before the CTA-wide set-up below
@@ -126,11 +131,16 @@ __global__ void __launch_bounds__(kThreads, 1) proj_stream_kernel(const __grid_c
     if (producer) {
         // refill each stage as soon as the MMAs have read it
         for (int i = issued; i < nk; ++i) {
-            if (!tc::mbar_wait(empty + i % stages, ((i / stages) & 1) ^ 1, kWaitLimit)) {
+            // wait for the stage in short polls, stopping as soon as another role gave up
+            bool got = false;
+            for (int k = 0; k < kWaitLimit / 256 && !got; ++k) {
+                if (*reinterpret_cast<volatile int*>(bad)) break;
+                got = tc::mbar_wait(empty + i % stages, ((i / stages) & 1) ^ 1, 256);
+            }
+            if (!got) {
                 atomicExch(bad, 1);
                 break;
             }
-            if (*reinterpret_cast<volatile int*>(bad)) break;
             issue(i);
             issued = i + 1;
         }
@@ -144,6 +154,12 @@ __global__ void __launch_bounds__(kThreads, 1) proj_stream_kernel(const __grid_c
         const uint32_t idesc = tc::idesc_bf16(kRowsPerTile, p.npad);
         int i = 0, j = 0;
         bool fail = false;
+        if (p.test_stall && !tc::mbar_wait(never, 0, kStallLimit)) {
+            atomicExch(bad, 1);   // before the read-out can see segment 0 complete
+            __threadfence_block();
+            tc::mma_commit(done);
+            fail = true;
+        }
         while (i < nk && !fail) {
             const long long x = b0 + i;
             const int kb = static_cast<int>(x % n_kb);
@@ -350,7 +366,7 @@ size_t proj_stream_workspace_bytes(const int* rows, int n_gemm, int T, int K) {
 }
 
 cudaError_t launch_proj_stream(const ProjGemm* g, int n_gemm, const void* in, int T, int K, void* workspace,
-                               size_t workspace_bytes, int* status, cudaStream_t stream) {
+                               size_t workspace_bytes, int* status, bool test_stall, cudaStream_t stream) {
     if (n_gemm < 1 || n_gemm > kMaxSegs || T < 1 || T > kProjStreamMaxRows || K < 8 || K % 8 != 0)
         return cudaErrorInvalidValue;
     const int sms = sm_count();
@@ -374,6 +390,7 @@ cudaError_t launch_proj_stream(const ProjGemm* g, int n_gemm, const void* in, in
     p.total = q.total;
     p.max_parts = q.max_parts;
     p.status = status;
+    p.test_stall = test_stall ? 1 : 0;
     int tiles = 0;
     for (int i = 0; i < n_gemm; ++i) {
         p.seg[i].out = g[i].out;
@@ -397,7 +414,7 @@ cudaError_t launch_proj_stream(const ProjGemm* g, int n_gemm, const void* in, in
     int cols = 32;
     while (cols < 2 * p.npad) cols *= 2;   // two accumulators of npad columns
     p.tmem_cols = cols;
-    const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + (2 * p.stages + 5) * 8 + 16;
+    const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + (2 * p.stages + 6) * 8 + 16;
     if ((e = cudaFuncSetAttribute(proj_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(smem))) != cudaSuccess)
         return e;

@@ -111,9 +111,11 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
  * dev_status for every (sequence, v-head) it did not finish, and returns, so
  * the CUDA context stays usable.  With this flag the kernels that carry the
  * hook -- the streaming recurrent kernel that gdn_decode_step / gdn_verify_k
- * use when B*H_k is at least twice the SM count, and the chain role (the
+ * use when B*H_k is at least twice the SM count, the chain role (the
  * chunk-to-chunk state recurrence) of the bf16 tensor-core
- * gdn_prefill_chunked -- first wait on a barrier that nothing arrives
+ * gdn_prefill_chunked, and the weight-streaming kernel of gdn_in_proj /
+ * gdn_out_proj (include/gdn_proj.h, T <= 256; its status word is the one
+ * given to those calls) -- first wait on a barrier that nothing arrives
  * on, so that wait gives up after a few microseconds and the path above runs
  * with none of the call's work done: every (sequence, v-head) they own
  * reports bit 4 and S, conv_state and out keep their previous contents. */

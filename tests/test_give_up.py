@@ -96,3 +96,52 @@ def test_prefill_wait_gives_up_and_reports():
     assert torch.count_nonzero(st) == 0
     G.assert_out_close(out, ref.out, c.act_dtype)
     G.assert_state_close(S, ref.S, c.act_dtype)
+
+
+def test_projection_wait_gives_up_and_reports():
+    """The weight-streaming projection kernel (gdn_in_proj at the B=64 decode batch, 35B dims,
+    with its workspace): the status word reports bit 4, no output is written, and a normal
+    call in the same context then matches the oracle."""
+    T, H, Hk, Hv = 64, 2048, 16, 32
+    c = gdn_inputs.make_proj_case(T=T, H=H, Hk=Hk, Hv=Hv, seed=4511)
+    dv = lambda t: t.cuda().contiguous()
+    bf = dict(device="cuda", dtype=torch.bfloat16)
+    outs = [torch.full((T, 128 * (2 * Hk + Hv)), 7.0, **bf), torch.full((T, 128 * Hv), 7.0, **bf),
+            torch.full((T, Hv), 7.0, **bf), torch.full((T, Hv), 7.0, **bf)]
+    st = torch.zeros(1, device="cuda", dtype=torch.int32)
+    ins = [dv(c.hidden), dv(c.W_qkv), dv(c.W_z), dv(c.W_a), dv(c.W_b)]
+
+    def call(stall):
+        d = gdn.make_dims(Hk, Hv, torch.bfloat16, torch.bfloat16, test_stall=stall)
+        ws = torch.empty(max(16, gdn.gdn_proj_workspace_bytes(d, T, H)), device="cuda", dtype=torch.uint8)
+        gdn.gdn_in_proj(d, *ins, *outs, workspace=ws, dev_status=st)
+        torch.cuda.synchronize()
+
+    call(True)
+    assert int(st.item()) == BIT_GAVE_UP
+    assert all(torch.all(o == 7.0) for o in outs)
+    st.zero_()
+    call(False)
+    assert int(st.item()) == 0
+    refs = oracle.in_proj(c.hidden, c.W_qkv, c.W_z, c.W_a, c.W_b)
+    for got, ref in zip(outs, refs):
+        err = np.abs(got.float().cpu().numpy().astype(np.float64) - ref)
+        assert np.all(err <= G.half_ulp_bf16(ref) + 1e-4)
+
+
+def test_decode_with_folded_projections_gives_up_and_reports():
+    """gdn_decode_step_ab at B=64 (the streaming kernel with the ssm_alpha / ssm_beta operands
+    in its stages): every (sequence, v-head) reports bit 4 and nothing is written."""
+    c = gdn_inputs.decode_b64()
+    pc = gdn_inputs.make_proj_case(T=c.N, H=2048, Hk=c.Hk, Hv=c.Hv, seed=4512)
+    d = gdn.make_dims(c.Hk, c.Hv, c.act_dtype, torch.float32, test_stall=True)
+    conv, S = G.dev(c.conv0), G.dev(c.S0)
+    conv0, S0 = conv.clone(), S.clone()
+    out = torch.full((c.N, c.Hv * 128), 7.0, device="cuda")
+    st = torch.zeros(c.N * c.Hv, device="cuda", dtype=torch.int32)
+    gdn.gdn_decode_step_ab(d, G.weights(c), G.dev(c.x), G.dev(c.z), G.dev(pc.hidden), G.dev(pc.W_a), G.dev(pc.W_b),
+                           conv, S, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert torch.all(st == BIT_GAVE_UP), st.unique()
+    assert torch.equal(S, S0) and torch.equal(conv, conv0)
+    assert torch.all(out == 7.0)
