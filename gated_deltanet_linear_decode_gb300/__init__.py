@@ -26,7 +26,7 @@ __all__ = [
     "gdn_verify_k", "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked",
     "gdn_prefill_chunked_static", "gdn_verify_k_ring", "gdn_commit_ring", "gdn_decode_step_ring",
     "gdn_state_faults", "gdn_state_reset", "GdnInProjWeights", "gdn_in_proj", "gdn_out_proj",
-    "gdn_proj_workspace_bytes", "PREFILL_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "HEAD_DIM",
+    "PREFILL_STATIC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "HEAD_DIM",
 ]
 
 HEAD_DIM = 128
@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "gdn_status_string", "gdn_version", "gdn_conv_state_init", "gdn_decode_step", "gdn_decode_step_ab",
     "gdn_verify_k", "gdn_commit", "gdn_prefill_workspace_bytes", "gdn_prefill_chunked",
     "gdn_prefill_chunked_static", "gdn_verify_k_ring", "gdn_commit_ring", "gdn_decode_step_ring",
-    "gdn_state_faults", "gdn_state_reset", "gdn_in_proj", "gdn_out_proj", "gdn_proj_workspace_bytes",
+    "gdn_state_faults", "gdn_state_reset", "gdn_in_proj", "gdn_out_proj",
 )
 
 
@@ -100,7 +100,6 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
         "gdn_state_reset": (ctypes.c_int, [D, I32, I32, P, P, P, P, P]),
         "gdn_in_proj": (ctypes.c_int, [D, I32, I32, P, ctypes.POINTER(GdnInProjWeights), P, P, P, P, P, SZ, P, P]),
         "gdn_out_proj": (ctypes.c_int, [D, I32, I32, P, P, P, P, SZ, P, P]),
-        "gdn_proj_workspace_bytes": (SZ, [D, I32, I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -366,11 +365,6 @@ def gdn_in_proj(dims: GdnDims, hidden, W_qkv, W_z, W_a, W_b, x, z, a_raw, b_raw,
     _check("gdn_in_proj", library().gdn_in_proj(ctypes.byref(dims), T, H, _ptr(hidden), ctypes.byref(w), _ptr(x),
                                                 _ptr(z), _ptr(a_raw), _ptr(b_raw), _ptr(workspace), nws,
                                                 _ptr(dev_status), _stream(stream)))
-
-
-def gdn_proj_workspace_bytes(dims: GdnDims, T: int, H: int) -> int:
-    """Workspace that lets the projections at T <= 256 rows spread over every SM."""
-    return int(library().gdn_proj_workspace_bytes(ctypes.byref(dims), T, H))
 
 
 def gdn_out_proj(dims: GdnDims, y, W_out, out, workspace=None, dev_status=None, stream=None) -> None:

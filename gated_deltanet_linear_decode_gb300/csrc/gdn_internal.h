@@ -157,11 +157,9 @@ struct ProjGemm {
     int rows;
 };
 constexpr int kProjStreamMaxRows = 256;   // the weight-streaming kernel takes T <= this
-// Up to 4 GEMMs sharing `in`, one launch (gdn_proj_stream.cu).  With a workspace of at least
-// proj_stream_workspace_bytes() every SM streams an equal share of the weights; without,
-// one CTA per 128-row tile.  status: optional, bit 4.
-size_t proj_stream_workspace_bytes(const int* rows, int n_gemm, int T, int K);
-cudaError_t launch_proj_stream(const ProjGemm* g, int n_gemm, const void* in, int T, int K, void* workspace,
-                               size_t workspace_bytes, int* status, bool test_stall, cudaStream_t stream);
+// Up to 4 GEMMs sharing `in`, one launch (gdn_proj_stream.cu): a CTA per 128-row tile, or a
+// cluster of 2 or 4 CTAs splitting its K when there are few tiles.  status: optional, bit 4.
+cudaError_t launch_proj_stream(const ProjGemm* g, int n_gemm, const void* in, int T, int K, int* status,
+                               bool test_stall, cudaStream_t stream);
 
 }  // namespace gdn

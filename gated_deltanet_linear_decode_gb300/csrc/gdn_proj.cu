@@ -3,8 +3,8 @@
 // page, "Architecture cheat sheet", "Gated DeltaNet layer").  They are dense GEMMs.  At
 // decode-size batches (T <= 256) they are bound by the weight stream and run in the
 // library's own weight-streaming kernel (gdn_proj_stream.cu: TMA + tcgen05, the four
-// input GEMMs in one launch); larger T is tensor-bound and runs through cuBLASLt (bf16
-// operands, fp32 accumulation).  This file is host code only: validation, dispatch, one
+// input GEMMs in one launch, K split over a cluster when there are few tiles); larger T
+// is tensor-bound and runs through cuBLASLt (bf16 operands, fp32 accumulation).  This file is host code only: validation, dispatch, one
 // cached cuBLASLt handle per device, and a cache of the chosen algorithm per shape.
 #include <cublasLt.h>
 #include <cuda_runtime.h>
@@ -126,15 +126,6 @@ gdn_status gemm_bf16(const void* A, const void* W, void* C, int T, int N, int K,
 
 extern "C" {
 
-size_t gdn_proj_workspace_bytes(const gdn_dims* dims, int32_t T, int32_t H) {
-    if (check_proj_dims(dims, T, H) != GDN_OK || T == 0 || T > gdn::kProjStreamMaxRows) return 0;
-    const int C = kD * (2 * dims->H_k + dims->H_v), HvD = kD * dims->H_v, Hv = dims->H_v;
-    const int in_rows[4] = {C, HvD, Hv, Hv}, out_rows[1] = {H};
-    const size_t a = gdn::proj_stream_workspace_bytes(in_rows, 4, T, H);
-    const size_t b = gdn::proj_stream_workspace_bytes(out_rows, 1, T, HvD);
-    return a > b ? a : b;
-}
-
 gdn_status gdn_in_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* hidden, const gdn_in_proj_weights* w,
                        void* x, void* z, void* a_raw, void* b_raw, void* workspace, size_t workspace_bytes,
                        int32_t* dev_status, gdn_stream_t stream) {
@@ -167,8 +158,8 @@ gdn_status gdn_in_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* h
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (T <= gdn::kProjStreamMaxRows) {
         const gdn::ProjGemm g[4] = {{w->W_qkv, x, C}, {w->W_z, z, HvD}, {w->W_a, a_raw, Hv}, {w->W_b, b_raw, Hv}};
-        return gdn::launch_proj_stream(g, 4, hidden, T, H, workspace, workspace_bytes, dev_status,
-                                       (dims->flags & GDN_FLAG_TEST_STALL) != 0, st) == cudaSuccess
+        return gdn::launch_proj_stream(g, 4, hidden, T, H, dev_status, (dims->flags & GDN_FLAG_TEST_STALL) != 0, st) ==
+                       cudaSuccess
                    ? GDN_OK
                    : GDN_E_CUDA;
     }
@@ -196,8 +187,7 @@ gdn_status gdn_out_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* 
         return GDN_E_INVALID_ARG;
     if (T <= gdn::kProjStreamMaxRows) {
         const gdn::ProjGemm g[1] = {{W_out, out, H}};
-        return gdn::launch_proj_stream(g, 1, y, T, HvD, workspace, workspace_bytes, dev_status,
-                                       (dims->flags & GDN_FLAG_TEST_STALL) != 0,
+        return gdn::launch_proj_stream(g, 1, y, T, HvD, dev_status, (dims->flags & GDN_FLAG_TEST_STALL) != 0,
                                        reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                    ? GDN_OK
                    : GDN_E_CUDA;

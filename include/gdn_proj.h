@@ -16,8 +16,11 @@
  * by few rows, so the time is the weight stream) they run in the library's
  * own weight-streaming kernel: 128-row tiles of W and the input streamed by
  * TMA into shared memory, tcgen05 MMAs into tensor memory, K split over a
- * cluster of up to 8 CTAs whose partial sums meet in distributed shared
- * memory; gdn_in_proj's four GEMMs share one launch.  For T > 256 they run
+ * cluster of 2 or 4 CTAs whose partial sums meet in distributed shared
+ * memory when there are fewer tiles than SMs; gdn_in_proj's four GEMMs share
+ * one launch.  The kernel is launched as a programmatic dependent of the
+ * previous kernel in the stream: it starts streaming the weights while that
+ * kernel finishes, and reads the input and writes the outputs only after it.  For T > 256 they run
  * through cuBLASLt (tensor-bound; one cuBLASLt handle per device is created
  * on first use and kept for the life of the process).  The order in which
  * the fp32 sums are formed differs between the two paths.
@@ -25,14 +28,9 @@
  * Conventions as in gdn.h: caller-owned, 16-byte aligned device buffers,
  * asynchronous on `stream`, errors returned, outputs must not overlap inputs.
  * Requires act_dtype = out_dtype = GDN_BF16 (GDN_E_UNSUPPORTED otherwise).
- * The workspace is optional (NULL / 0 allowed; the library allocates no
- * device memory).  For T <= 256, one of at least gdn_proj_workspace_bytes()
- * lets the streaming kernel give every SM an equal share of the weights (runs
- * of a 128-row tile's K split between CTAs add fp32 partial sums through it);
- * without it each CTA streams whole tiles, which leaves SMs idle when there
- * are fewer tiles than SMs.  For T > 256 it is cuBLASLt's scratch (a few MiB
- * lets it pick faster kernels).  Calls that share a workspace must not
- * overlap on the GPU.
+ * The workspace is optional scratch for cuBLASLt at T > 256 (NULL / 0
+ * allowed; a few MiB lets it pick faster kernels; the streaming kernel needs
+ * none); the library allocates no device memory.
  * dev_status (optional, may be NULL) is one int32: the weight-streaming kernel
  * ORs bit 4 into it when one of its bounded waits gave up (its outputs are
  * then not written); the caller zeroes it and reads it after synchronising.
@@ -62,14 +60,6 @@ typedef struct {
  * (dev_status: 4); GDN_E_CUDA if a launch fails, or cuBLASLt fails or finds
  * no kernel.
  */
-/*
- * gdn_proj_workspace_bytes -- workspace that lets gdn_in_proj and gdn_out_proj
- * with these dims, T and H spread their weight streams over every SM of the
- * current device (the larger of the two needs); 0 for T > 256 or invalid
- * arguments.  Host-only query.
- */
-size_t gdn_proj_workspace_bytes(const gdn_dims* dims, int32_t T, int32_t H);
-
 gdn_status gdn_in_proj(const gdn_dims* dims, int32_t T, int32_t H, const void* hidden,
                        const gdn_in_proj_weights* w, void* x, void* z, void* a_raw, void* b_raw,
                        void* workspace, size_t workspace_bytes, int32_t* dev_status,

@@ -99,8 +99,8 @@ def test_prefill_wait_gives_up_and_reports():
 
 
 def test_projection_wait_gives_up_and_reports():
-    """The weight-streaming projection kernel (gdn_in_proj at the B=64 decode batch, 35B dims,
-    with its workspace): the status word reports bit 4, no output is written, and a normal
+    """The weight-streaming projection kernel (gdn_in_proj at the B=64 decode batch, 35B dims):
+    the status word reports bit 4, no output is written, and a normal
     call in the same context then matches the oracle."""
     T, H, Hk, Hv = 64, 2048, 16, 32
     c = gdn_inputs.make_proj_case(T=T, H=H, Hk=Hk, Hv=Hv, seed=4511)
@@ -113,8 +113,7 @@ def test_projection_wait_gives_up_and_reports():
 
     def call(stall):
         d = gdn.make_dims(Hk, Hv, torch.bfloat16, torch.bfloat16, test_stall=stall)
-        ws = torch.empty(max(16, gdn.gdn_proj_workspace_bytes(d, T, H)), device="cuda", dtype=torch.uint8)
-        gdn.gdn_in_proj(d, *ins, *outs, workspace=ws, dev_status=st)
+        gdn.gdn_in_proj(d, *ins, *outs, dev_status=st)
         torch.cuda.synchronize()
 
     call(True)

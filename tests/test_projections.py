@@ -3,12 +3,12 @@ gdn_out_proj) against the fp64 oracle on the same bf16 inputs.  Each output
 is one fp32 sum of exact bf16 products rounded once to bf16, so the bound is
 half a bf16 ulp of the reference plus 1e-4 for the fp32 accumulation.
 
-T <= 256 runs the library's weight-streaming kernel: with a workspace of
-gdn_proj_workspace_bytes() every SM takes an equal run of k-blocks and tiles
-split between CTAs meet through fp32 partial sums; without one, a CTA per
-whole tile.  Both are run, with zero fill past the last weight row and past
-the last multiple of 64 in K.  Larger T runs cuBLASLt.  The status word of
-the streaming kernel must stay clear."""
+T <= 256 runs the library's weight-streaming kernel: a CTA per 128-row tile
+when there are about as many tiles as SMs, else clusters of 2 or 4 CTAs that
+split a tile's K and add their partial sums in distributed shared memory (both
+are run: the input GEMMs take the first, ssm_out the second), with zero fill
+past the last weight row and past the last multiple of 64 in K.  Larger T runs
+cuBLASLt.  The status word of the streaming kernel must stay clear."""
 import numpy as np
 import pytest
 import torch
@@ -30,9 +30,6 @@ def _close(got, ref):
 
 def _run(c, T, rows=None, ws_bytes=0):
     d = gdn.make_dims(c.Hk, c.Hv, torch.bfloat16, torch.bfloat16)
-    if ws_bytes == "auto":
-        ws_bytes = gdn.gdn_proj_workspace_bytes(d, T, c.H)
-        assert ws_bytes > 0
     dv = lambda t: t.cuda().contiguous()
     C, HvD = 128 * (2 * c.Hk + c.Hv), 128 * c.Hv
     x = torch.empty(T, C, device="cuda", dtype=torch.bfloat16)
@@ -54,8 +51,8 @@ def _run(c, T, rows=None, ws_bytes=0):
     _close(out[sel], oracle.out_proj(c.y[sel], c.W_out))
 
 
-@pytest.mark.parametrize("T,ws", [(300, 0), (257, 4 << 20), (256, "auto"), (192, 0), (129, "auto"), (64, "auto"),
-                                  (64, 0), (48, "auto"), (17, 1 << 20), (1, "auto"), (1, 0)])
+@pytest.mark.parametrize("T,ws", [(300, 0), (257, 4 << 20), (256, 0), (192, 0), (129, 1 << 20), (64, 4 << 20),
+                                  (64, 0), (48, 0), (17, 1 << 20), (1, 0)])
 def test_projections_35b_dims(T, ws):
     """Hidden 2048, 16/32 heads: ragged prefills either side of the 256-row switch to cuBLASLt,
     the B=64 K=3 verify batch, the B=64 decode batch, 48 and 17 rows, and a single token, with
@@ -74,10 +71,10 @@ def test_projections_27b_dims_full_size_sampled():
 
 @pytest.mark.parametrize("T", [64, 192])
 def test_projections_27b_dims_decode_batches(T):
-    """Hidden 5120, 16/48 heads at the decode and verify batch sizes (the streaming kernel splits
-    K of the input GEMMs two ways and of ssm_out four ways)."""
+    """Hidden 5120, 16/48 heads at the decode and verify batch sizes (130 tiles of input GEMMs, a
+    CTA each; ssm_out's 40 tiles split two ways)."""
     c = gdn_inputs.make_proj_case(T=T, H=5120, Hk=16, Hv=48, seed=220 + T)
-    _run(c, T, ws_bytes="auto")
+    _run(c, T)
 
 
 @pytest.mark.parametrize("T", [5, 100])
@@ -85,5 +82,4 @@ def test_projections_ragged_hidden(T):
     """H = 2056: K ends 8 past a multiple of 64 (zero-filled copies), ssm_out's 2056 rows end 8
     into their last 128-row tile, and ssm_alpha / ssm_beta are 4-row GEMMs."""
     c = gdn_inputs.make_proj_case(T=T, H=2056, Hk=2, Hv=4, seed=230 + T)
-    _run(c, T, ws_bytes="auto")
     _run(c, T)
