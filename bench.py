@@ -304,10 +304,12 @@ class Workload:
         T = self.pc.T
         seg = T // n_seg
         assert seg * n_seg == T and seg % 64 == 0
-        if getattr(self, "cu_seg_len", None) != seg:
-            self.cu_seg_h = torch.tensor([0, seg], dtype=torch.int32)
-            self.cu_seg_d = self.cu_seg_h.to(self.p_out.device)
-            self.cu_seg_len = seg
+        if not hasattr(self, "cu_seg"):
+            self.cu_seg = {}
+        if seg not in self.cu_seg:   # one segment table per length, made outside the timed steps
+            h = torch.tensor([0, seg], dtype=torch.int32)
+            self.cu_seg[seg] = (h, h.to(self.p_out.device))
+        cu_seg_h, cu_seg_d = self.cu_seg[seg]
         ev_in = [torch.cuda.Event() for _ in range(n_seg + 1)]
         ev_done = [torch.cuda.Event() for _ in range(n_seg + 1)]
         self.s_in.wait_stream(cur)
@@ -336,7 +338,7 @@ class Workload:
         for i in range(n_seg):
             cur.wait_event(ev_in[i])
             sl = slice(i * seg, (i + 1) * seg)
-            self.gdn.gdn_prefill_chunked(self.p_dims, self.p_w, self.cu_seg_h, self.cu_seg_d, pi["x"][sl], pi["z"][sl],
+            self.gdn.gdn_prefill_chunked(self.p_dims, self.p_w, cu_seg_h, cu_seg_d, pi["x"][sl], pi["z"][sl],
                                          pi["a_raw"][sl], pi["b_raw"][sl], self.p_conv, self.p_S, self.p_out[sl],
                                          zero_init=(i == 0), workspace=self.p_ws)
             n += 3
