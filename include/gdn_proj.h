@@ -20,7 +20,9 @@
  * memory when there are fewer tiles than SMs; gdn_in_proj's four GEMMs share
  * one launch.  The kernel is launched as a programmatic dependent of the
  * previous kernel in the stream: it starts streaming the weights while that
- * kernel finishes, and reads the input and writes the outputs only after it.  For T > 256 they run
+ * kernel finishes, and reads the input and writes the outputs only after it
+ * (so the weights must not be written by the kernel just before the call in
+ * the stream; a copy or any earlier kernel is ordered as usual).  For T > 256 they run
  * through cuBLASLt (tensor-bound; one cuBLASLt handle per device is created
  * on first use and kept for the life of the process).  The order in which
  * the fp32 sums are formed differs between the two paths.
