@@ -152,6 +152,15 @@ __device__ __forceinline__ void st_f4(float* p, float4 v) {
 // pattern); fp32 -> bf16 rounds to nearest even.  round() gives the value a
 // store followed by a load would give, so a walk that keeps the state in
 // registers continues from exactly what a later call would read back.
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start before the previous kernel in its stream has finished:
+// grid_dependency_wait() returns once that kernel has completed and its writes are
+// visible (at once when there is none), and grid_launch_dependents() lets the next
+// such kernel start.  Kernels here wait before their first global access and let the
+// next one start only after that, so at most two grids are resident at a time.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 template <typename Ts>
 struct StateIO;
 

@@ -29,6 +29,7 @@
 #include <cstdint>
 #include <cstring>
 
+#include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "gdn_tc.cuh"
 
@@ -86,12 +87,6 @@ __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
     asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
-// Programmatic dependent launch: wait until the grids this one depends on have completed
-// and their writes are visible (returns at once when launched without such a dependence);
-// let the grids that depend on this one be scheduled.
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
 __global__ void __launch_bounds__(kThreads, 1) proj_stream_kernel(const __grid_constant__ ProjParams p) {
     extern __shared__ __align__(1024) uint8_t sm_raw[];
     // the 128-byte swizzle pattern repeats every 1024 bytes: base the stages there

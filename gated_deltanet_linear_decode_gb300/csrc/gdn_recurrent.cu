@@ -69,6 +69,10 @@ recurrent_kernel(const RecParams p) {
     __shared__ float abp[NW][2];   // folded a/b: the warps' partial dot products
     __shared__ float rms_part[kMaxK];
 
+    // launched as a programmatic dependent: nothing global is touched before the previous
+    // kernel in the stream is done (it may have written the state, the conv state or the inputs)
+    grid_dependency_wait();
+    grid_launch_dependents();
     // ---- state rows: issue the 128-bit loads before anything else
     const Ts* Sin = rec_state_in<Ts>(p, b) + static_cast<size_t>(h) * kD * kD + static_cast<size_t>(j0) * kD;
     float4 s[8];
@@ -345,13 +349,15 @@ __global__ void state_reset_kernel(const ResetParams p) {
 template <typename Tact, typename Tout, typename Ts>
 cudaError_t launch_rec_t(const RecParams& p, int rpc, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = p.CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see grid_dependency_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cfg.gridDim = dim3(static_cast<unsigned>(p.B) * p.Hk * p.CS);
     cfg.blockDim = dim3(rpc * 4);
     cfg.dynamicSmemBytes = 0;

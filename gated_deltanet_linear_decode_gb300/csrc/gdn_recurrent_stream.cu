@@ -127,9 +127,13 @@ recurrent_stream_kernel(const RecParams p) {
         tc::mbar_init(never, 1);
         *abort_s = 0;
     }
+    // launched as a programmatic dependent: nothing global is touched before the previous
+    // kernel in the stream is done (it may have written the state, the conv state or the inputs)
+    grid_dependency_wait();
     if (tid < kD) nw_s[tid] = p.norm_w[tid];
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
+    grid_launch_dependents();
 
     // item i of this CTA -> (group, m)
     const int G = gridDim.x;
@@ -390,8 +394,17 @@ cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_d
     auto go = [&](auto kernel) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        kernel<<<grid, kLaunchThreads, smem, stream>>>(p);
-        return cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(kLaunchThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see grid_dependency_wait
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kernel, p);
     };
     using bf = __nv_bfloat16;
     if (sbf)   // bf16 activations only (checked by the API)
