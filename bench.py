@@ -289,71 +289,89 @@ class Workload:
         g.gdn_commit_ring(self.d_dims, self.vc.K, self.vc.K + 1, self.acc, self.v_ckc, self.r_conv, self.r_cur)
         return 2
 
-    def e2e_step(self, n_seg=4, small_first=True):
+    @staticmethod
+    def e2e_segments(T):
+        """Prefill segments of the e2e step: 2048 tokens each, the last 2048 cut into 1024 + 768 +
+        256 (T = 8192: 2048, 2048, 2048, 1024, 768, 256 -- the fastest of the splits measured:
+        short last segments leave little compute and copying once the last inputs land, while
+        every call costs a fixed ~60 us of start-up); one segment when T is not a multiple of 64."""
+        if T % 64 or T < 1024:
+            return (T,)
+        segs = [2048] * (T // 2048) + ([T % 2048] if T % 2048 else [])
+        last = segs.pop()
+        if last == 2048:
+            tail = [1024, 768, 256]
+        elif last >= 512:
+            tail = [last - 256, 256]
+        else:
+            tail = [last]
+        return tuple(segs + tail)
+
+    def e2e_step(self, segs=None):
         """One step from host buffers to host buffers through the C ABI, with the transfers
         pipelined against the compute on two side streams.  The decode and verify inputs (a few
         MB) go first, so those two calls run while the prefill's inputs are still arriving; the
-        prefill's tokens then go through gdn_prefill_chunked in n_seg segments (the conv and
-        recurrent state carried on the device from one call to the next, the chunk grid
-        unchanged, so the results are those of one call), segment i+1's inputs copied in while
-        segment i computes and each segment's outputs copied out as soon as it is done.
+        prefill's tokens then go through gdn_prefill_chunked in segments of `segs` tokens
+        (multiples of 64: the conv and recurrent state carried on the device from one call to
+        the next, the chunk grid unchanged, so the results are those of one call), segment i+1's
+        inputs copied in while segment i computes and each segment's outputs copied out as soon
+        as it is done.  The host enqueues the copies one segment ahead of the compute (so the
+        copy engine never waits for the host, and no launch waits behind the host issuing all
+        the copies); the last segments are short, so little compute and copying is left once
+        the last inputs land.
         Returns the number of library kernels launched."""
         cur = torch.cuda.current_stream()
         if not hasattr(self, "s_in"):
             self.s_in, self.s_out = torch.cuda.Stream(self.p_out.device), torch.cuda.Stream(self.p_out.device)
-        T = self.pc.T
-        seg = T // n_seg
-        assert seg * n_seg == T and seg % 64 == 0
+        segs = self.e2e_segments(self.pc.T) if segs is None else tuple(segs)
+        assert sum(segs) == self.pc.T and (len(segs) == 1 or all(L > 0 and L % 64 == 0 for L in segs))
         if not hasattr(self, "cu_seg"):
             self.cu_seg = {}
-        if seg not in self.cu_seg:   # one segment table per length, made outside the timed steps
-            h = torch.tensor([0, seg], dtype=torch.int32)
-            self.cu_seg[seg] = (h, h.to(self.p_out.device))
-        cu_seg_h, cu_seg_d = self.cu_seg[seg]
-        ev_in = [torch.cuda.Event() for _ in range(n_seg + 1)]
-        ev_done = [torch.cuda.Event() for _ in range(n_seg + 1)]
+        for L in segs:
+            if L not in self.cu_seg:   # one segment table per length, made outside the timed steps
+                h = torch.tensor([0, L], dtype=torch.int32)
+                self.cu_seg[L] = (h, h.to(self.p_out.device))
         self.s_in.wait_stream(cur)
         self.s_out.wait_stream(cur)
-        def small_in():
+        starts = [sum(segs[:i]) for i in range(len(segs))]
+        pi = self.p_in
+        ev_in = [torch.cuda.Event() for _ in segs]
+
+        def copy_in(i):   # segment i's inputs, on the input stream
+            sl = slice(starts[i], starts[i] + segs[i])
+            with torch.cuda.stream(self.s_in):
+                for k in self.h:
+                    pi[k][sl].copy_(self.h[k][sl], non_blocking=True)
+                ev_in[i].record(self.s_in)
+
+        ev_small, ev_dv = torch.cuda.Event(), torch.cuda.Event()
+        with torch.cuda.stream(self.s_in):
             for src, dst in ((self.hd, self.d_in), (self.hv, self.v_in)):
                 for k in src:
                     dst[k].copy_(src[k], non_blocking=True)
-            ev_in[n_seg].record(self.s_in)
-
-        with torch.cuda.stream(self.s_in):
-            if small_first:
-                small_in()
-            for i in range(n_seg):
-                for k in self.h:
-                    self.p_in[k][i * seg:(i + 1) * seg].copy_(self.h[k][i * seg:(i + 1) * seg], non_blocking=True)
-                ev_in[i].record(self.s_in)
-            if not small_first:
-                small_in()
-        n = 0
-        if small_first:
-            cur.wait_event(ev_in[n_seg])
-            n += self.decode() + self.verify()
-            ev_done[n_seg].record(cur)
-        pi = self.p_in
-        for i in range(n_seg):
+            ev_small.record(self.s_in)
+        copy_in(0)   # the copy engine keeps one segment queued ahead of the compute
+        cur.wait_event(ev_small)
+        n = self.decode() + self.verify()
+        ev_dv.record(cur)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(ev_dv)
+            self.h_dout.copy_(self.d_out, non_blocking=True)
+            self.h_vout.copy_(self.v_out, non_blocking=True)
+        for i, L in enumerate(segs):
+            if i + 1 < len(segs):
+                copy_in(i + 1)
+            sl = slice(starts[i], starts[i] + L)
             cur.wait_event(ev_in[i])
-            sl = slice(i * seg, (i + 1) * seg)
-            self.gdn.gdn_prefill_chunked(self.p_dims, self.p_w, cu_seg_h, cu_seg_d, pi["x"][sl], pi["z"][sl],
+            cu_h, cu_d = self.cu_seg[L]
+            self.gdn.gdn_prefill_chunked(self.p_dims, self.p_w, cu_h, cu_d, pi["x"][sl], pi["z"][sl],
                                          pi["a_raw"][sl], pi["b_raw"][sl], self.p_conv, self.p_S, self.p_out[sl],
                                          zero_init=(i == 0), workspace=self.p_ws)
             n += 3
-            ev_done[i].record(cur)
-        if not small_first:
-            cur.wait_event(ev_in[n_seg])
-            n += self.decode() + self.verify()
-            ev_done[n_seg].record(cur)
-        with torch.cuda.stream(self.s_out):
-            self.s_out.wait_event(ev_done[n_seg])
-            self.h_dout.copy_(self.d_out, non_blocking=True)
-            self.h_vout.copy_(self.v_out, non_blocking=True)
-            for i in range(n_seg):
-                self.s_out.wait_event(ev_done[i])
-                sl = slice(i * seg, (i + 1) * seg)
+            ev_done = torch.cuda.Event()
+            ev_done.record(cur)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(ev_done)
                 self.h_pout[sl].copy_(self.p_out[sl], non_blocking=True)
         cur.wait_stream(self.s_out)
         cur.wait_stream(self.s_in)
