@@ -170,6 +170,7 @@ struct StateIO<float> {
     __device__ static __forceinline__ float4 ld(const void* p) { return *static_cast<const float4*>(p); }
     __device__ static __forceinline__ float4 round(float4 v) { return v; }
     __device__ static __forceinline__ void st(float* p, float4 v) { st_f4(p, v); }
+    __device__ static __forceinline__ void st_shared(void* p, float4 v) { *static_cast<float4*>(p) = v; }
 };
 
 template <>
@@ -194,6 +195,9 @@ struct StateIO<__nv_bfloat16> {
     __device__ static __forceinline__ float4 round(float4 v) { return unpack(pack(v.x, v.y), pack(v.z, v.w)); }
     __device__ static __forceinline__ void st(__nv_bfloat16* p, float4 v) {
         asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(pack(v.x, v.y)), "r"(pack(v.z, v.w)) : "memory");
+    }
+    __device__ static __forceinline__ void st_shared(void* p, float4 v) {
+        *static_cast<uint2*>(p) = make_uint2(pack(v.x, v.y), pack(v.z, v.w));
     }
 };
 

@@ -92,9 +92,15 @@ struct StageLayout {
     }
 };
 
-template <typename Tact, typename Tout, typename Ts>
-__global__ void __launch_bounds__(kLaunchThreads, 1)
-recurrent_stream_kernel(const RecParams p) {
+// With a bf16 state the tile stays in its shared-memory stage while it is updated (read
+// there for S.k, S.q and again for the update) instead of moving to registers: the kernel
+// then fits 96 registers, and two CTAs per SM keep two tiles' latency chains in flight
+// (2 x 9 warps leave 5 warps on some of the SM's four sub-partitions, whose 16,384
+// registers allow 96 a thread).  The stage goes back to the producer once the item is done.
+constexpr int kMaxRegsSmemState = 96;
+
+template <typename Tact, typename Tout, typename Ts, bool kSmemState>
+__device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
     extern __shared__ __align__(128) uint8_t sm[];
     constexpr int es = sizeof(Tact), ss = sizeof(Ts);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -208,7 +214,7 @@ recurrent_stream_kernel(const RecParams p) {
         return;
     }
 
-    float4 sreg[16];
+    float4 sreg[kSmemState ? 1 : 16];
     for (int i = 0; i < n_items; ++i) {
         const int g = item_group(i), m = i % r;
         const int b = g / p.Hk, kh = g % p.Hk, h = kh + m * p.Hk;
@@ -222,10 +228,12 @@ recurrent_stream_kernel(const RecParams p) {
         }
         const float a_dt = p.dt_bias[h], a_ssm = p.ssm_a[h];
         const bool landed = stage_wait(&full[i % kStages], (i / kStages) & 1, abort_s);
-        // state rows -> registers; small inputs -> private area
+        // state rows -> registers (or left in the stage); small inputs -> private area
+        uint8_t* const srow = const_cast<uint8_t*>(stg) + ((warp * 16) * kD + 4 * lane) * ss;   // my rows in the stage
+        if constexpr (!kSmemState) {
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr)
-            sreg[rr] = StateIO<Ts>::ld(stg + ((warp * 16 + rr) * kD + 4 * lane) * ss);
+            for (int rr = 0; rr < 16; ++rr) sreg[rr] = StateIO<Ts>::ld(srow + rr * kD * ss);
+        }
         for (uint32_t e = tid * 16; e < cur_bytes; e += kSThreads * 16)
             *reinterpret_cast<uint4*>(cur + e) = *reinterpret_cast<const uint4*>(stg + L.cw + e);
         if (tid < K && !H) {
@@ -252,7 +260,7 @@ recurrent_stream_kernel(const RecParams p) {
             report_from(i, tid, kSThreads);
             break;
         }
-        if (tid == 0) tc::mbar_arrive(&empty[i % kStages]);   // the stage may be refilled
+        if (!kSmemState && tid == 0) tc::mbar_arrive(&empty[i % kStages]);   // the stage may be refilled
         if (H > 0 && tid < K) {
             // the folded a_raw, b_raw: the warps' partial sums (the next barrier orders them
             // before step 7)
@@ -313,7 +321,7 @@ recurrent_stream_kernel(const RecParams p) {
             float pv[32];
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
-                const float4 sv = sreg[rr];
+                const float4 sv = kSmemState ? StateIO<Ts>::ld(srow + rr * kD * ss) : sreg[rr];
                 pv[2 * rr] = fmaf(sv.w, kk.w, fmaf(sv.z, kk.z, fmaf(sv.y, kk.y, sv.x * kk.x)));
                 pv[2 * rr + 1] = fmaf(sv.w, qq.w, fmaf(sv.z, qq.z, fmaf(sv.y, qq.y, sv.x * qq.x)));
             }
@@ -328,14 +336,18 @@ recurrent_stream_kernel(const RecParams p) {
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
                 const float d = __shfl_sync(0xffffffffu, d_even, 2 * rr);
-                const float4 sv = sreg[rr];
+                const float4 sv = kSmemState ? StateIO<Ts>::ld(srow + rr * kD * ss) : sreg[rr];
                 float4 nv;
                 nv.x = fmaf(d, kk.x, eg * sv.x);
                 nv.y = fmaf(d, kk.y, eg * sv.y);
                 nv.z = fmaf(d, kk.z, eg * sv.z);
                 nv.w = fmaf(d, kk.w, eg * sv.w);
                 nv = StateIO<Ts>::round(nv);   // the next token continues from what a later call reads
-                sreg[rr] = nv;
+                if constexpr (kSmemState) {
+                    if (t + 1 < K) StateIO<Ts>::st_shared(srow + rr * kD * ss, nv);
+                } else {
+                    sreg[rr] = nv;
+                }
                 StateIO<Ts>::st(Sout + rr * kD + 4 * lane, nv);
                 if (status && (nonfinite_bits(nv.x) | nonfinite_bits(nv.y) | nonfinite_bits(nv.z) | nonfinite_bits(nv.w)))
                     atomicOr(status, 1);
@@ -374,7 +386,23 @@ recurrent_stream_kernel(const RecParams p) {
             }
             compute_sync();
         }
+        if constexpr (kSmemState) {
+            // the item is done with its stage: hand it back (the generic writes of the state
+            // above are ordered before the producer's next bulk copy into it)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            compute_sync();
+            if (tid == 0) tc::mbar_arrive(&empty[i % kStages]);
+        }
     }
+}
+
+template <typename Tact, typename Tout>
+__global__ void __launch_bounds__(kLaunchThreads, 1) recurrent_stream_kernel(const RecParams p) {
+    recurrent_stream_body<Tact, Tout, float, false>(p);
+}
+template <typename Tout>
+__global__ void __maxnreg__(kMaxRegsSmemState) recurrent_stream_bf16s_kernel(const RecParams p) {
+    recurrent_stream_body<__nv_bfloat16, Tout, __nv_bfloat16, true>(p);
 }
 
 }  // namespace
@@ -394,8 +422,14 @@ cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_d
     auto go = [&](auto kernel) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
+        int per_sm = 1;
+        if (sbf) {   // as many CTAs per SM as fit (the bf16-state kernel is built for two)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kLaunchThreads, smem);
+            if (e != cudaSuccess) return e;
+            per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
+        }
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.gridDim = dim3(static_cast<unsigned>(grid * per_sm));
         cfg.blockDim = dim3(kLaunchThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
@@ -408,10 +442,10 @@ cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_d
     };
     using bf = __nv_bfloat16;
     if (sbf)   // bf16 activations only (checked by the API)
-        return out_dtype == 1 ? go(recurrent_stream_kernel<bf, bf, bf>) : go(recurrent_stream_kernel<bf, float, bf>);
+        return out_dtype == 1 ? go(recurrent_stream_bf16s_kernel<bf>) : go(recurrent_stream_bf16s_kernel<float>);
     if (act_dtype == 1)
-        return out_dtype == 1 ? go(recurrent_stream_kernel<bf, bf, float>) : go(recurrent_stream_kernel<bf, float, float>);
-    return out_dtype == 1 ? go(recurrent_stream_kernel<float, bf, float>) : go(recurrent_stream_kernel<float, float, float>);
+        return out_dtype == 1 ? go(recurrent_stream_kernel<bf, bf>) : go(recurrent_stream_kernel<bf, float>);
+    return out_dtype == 1 ? go(recurrent_stream_kernel<float, bf>) : go(recurrent_stream_kernel<float, float>);
 }
 
 }  // namespace gdn
