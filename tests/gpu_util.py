@@ -67,6 +67,17 @@ def assert_state_close(S, ref, act_dtype):
     return r
 
 
+def assert_state_one_rounding(S, ref):
+    """A bf16 state: every element within one bf16 rounding of the oracle,
+    |S - S_ref| <= 2^-8 |S_ref| + 1e-5 max|S_ref| (half a bf16 ulp is at most
+    2^-8 of the value; the second term covers the fp32 arithmetic)."""
+    S = S.float().cpu().numpy().astype(np.float64)
+    ref = np.asarray(ref, dtype=np.float64).reshape(S.shape)
+    err = np.abs(S - ref)
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-5 * np.abs(ref).max()
+    assert np.all(err <= bound), f"worst excess {float((err - bound).max()):.3e}"
+
+
 def conv_bits_equal(conv_dev, conv_ref_f32, act_dtype):
     got = conv_dev.cpu()
     want = torch.from_numpy(np.ascontiguousarray(conv_ref_f32)).to(act_dtype)

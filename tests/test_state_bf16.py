@@ -26,12 +26,7 @@ pytestmark = pytest.mark.gpu
 BF = torch.bfloat16
 
 
-def assert_one_rounding(S, ref):
-    S = S.float().cpu().numpy().astype(np.float64)
-    ref = np.asarray(ref, dtype=np.float64).reshape(S.shape)
-    err = np.abs(S - ref)
-    bound = 2.0 ** -8 * np.abs(ref) + 1e-5 * np.abs(ref).max()
-    assert np.all(err <= bound), f"worst excess {float((err - bound).max()):.3e}"
+assert_one_rounding = G.assert_state_one_rounding
 
 
 def _dims(c, out=torch.float32, **kw):
