@@ -200,6 +200,25 @@ class ClockSampler:
 class Workload:
     """Device-resident inputs/outputs of one step, plus pinned host copies for e2e."""
 
+    @staticmethod
+    def _packed(named, dev):
+        """One pinned host buffer and one device buffer holding the tensors of `named` (a list of
+        (dict, key, tensor)), each at a 256-byte aligned offset, so that all of them move in one
+        copy; returns (host buffer, device buffer, [(dict, key, host view, device view)])."""
+        off, place = 0, []
+        for d, k, t in named:
+            nb = t.numel() * t.element_size()
+            place.append((d, k, t, off, nb))
+            off = (off + nb + 255) // 256 * 256
+        hbuf = torch.empty(off, dtype=torch.uint8).pin_memory()
+        dbuf = torch.empty(off, dtype=torch.uint8, device=dev)
+        views = []
+        for d, k, t, o, nb in place:
+            hv = hbuf[o:o + nb].view(t.dtype).view(t.shape)
+            hv.copy_(t)
+            views.append((d, k, hv, dbuf[o:o + nb].view(t.dtype).view(t.shape)))
+        return hbuf, dbuf, views
+
     def __init__(self, device, prefill_tokens=8192):
         import gated_deltanet_linear_decode_gb300 as gdn
         self.gdn = gdn
@@ -218,12 +237,18 @@ class Workload:
         # host (pinned) inputs for the e2e leg
         pin = lambda t: t.contiguous().pin_memory()
         self.h = {k: pin(getattr(pc, k)) for k in ("x", "z", "a_raw", "b_raw")}
-        self.hd = {k: pin(getattr(dc, k)) for k in ("x", "z", "a_raw", "b_raw")}
-        self.hv = {k: pin(getattr(vc, k)) for k in ("x", "z", "a_raw", "b_raw")}
-        # device copies
+        # the decode and verify inputs (a few MB in eight tensors) packed in one pinned buffer and
+        # one device buffer, so that the e2e leg moves them in one copy
+        self.hd, self.hv, self.d_in, self.v_in = {}, {}, {}, {}
+        self.h_small, self.d_small, views = self._packed(
+            [(0, k, getattr(dc, k).contiguous()) for k in ("x", "z", "a_raw", "b_raw")] +
+            [(1, k, getattr(vc, k).contiguous()) for k in ("x", "z", "a_raw", "b_raw")], dev)
+        for which, k, hview, dview in views:
+            (self.hd if which == 0 else self.hv)[k] = hview
+            (self.d_in if which == 0 else self.v_in)[k] = dview
+        self.d_small.copy_(self.h_small)
+        # device copies of the prefill inputs
         self.p_in = {k: v.to(dev, non_blocking=True) for k, v in self.h.items()}
-        self.d_in = {k: v.to(dev, non_blocking=True) for k, v in self.hd.items()}
-        self.v_in = {k: v.to(dev, non_blocking=True) for k, v in self.hv.items()}
         self.cu_h = pc.cu_seqlens.to(torch.int32)
         self.cu_d = self.cu_h.to(dev)
         self.p_conv = torch.zeros(1, 3, pc.C, device=dev, dtype=torch.bfloat16)
@@ -233,11 +258,15 @@ class Workload:
         self.p_ws = torch.empty(max(nws, 16), device=dev, dtype=torch.uint8) if nws else None
         self.d_conv = dc.conv0.to(dev)
         self.d_S = dc.S0.to(dev)
-        self.d_out = torch.empty(dc.N, dc.Hv * 128, device=dev, dtype=torch.bfloat16)
+        # decode and verify outputs: one device buffer and one pinned host buffer (one copy out)
+        n_d, n_v = dc.N * dc.Hv * 128, vc.N * vc.K * vc.Hv * 128
+        self.d_small_out = torch.empty(n_d + n_v, device=dev, dtype=torch.bfloat16)
+        self.h_small_out = torch.empty(n_d + n_v, dtype=torch.bfloat16).pin_memory()
+        self.d_out = self.d_small_out[:n_d].view(dc.N, dc.Hv * 128)
         B, K = vc.N, vc.K
         self.v_ckc = torch.empty(B, K, 3, vc.C, device=dev, dtype=torch.bfloat16)
         self.v_ckS = torch.empty(B, K, vc.Hv, 128, 128, device=dev)
-        self.v_out = torch.empty(B * K, vc.Hv * 128, device=dev, dtype=torch.bfloat16)
+        self.v_out = self.d_small_out[n_d:].view(B * K, vc.Hv * 128)
         self.acc = vc.accept_len.to(dev)
         # the same verify + commit on a state ring (R = K + 1 slots, slot 0 live at the start)
         self.r_S = torch.zeros(B, K + 1, vc.Hv, 128, 128, device=dev)
@@ -245,8 +274,8 @@ class Workload:
         self.r_cur = torch.zeros(B, device=dev, dtype=torch.int32)
         self.r_conv = vc.conv0.to(dev)
         self.h_pout = torch.empty(self.p_out.shape, dtype=torch.bfloat16).pin_memory()
-        self.h_dout = torch.empty(self.d_out.shape, dtype=torch.bfloat16).pin_memory()
-        self.h_vout = torch.empty(self.v_out.shape, dtype=torch.bfloat16).pin_memory()
+        self.h_dout = self.h_small_out[:n_d].view(self.d_out.shape)
+        self.h_vout = self.h_small_out[n_d:].view(self.v_out.shape)
         self.flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
         self.launches_per_step = 0
 
@@ -346,9 +375,7 @@ class Workload:
 
         ev_small, ev_dv = torch.cuda.Event(), torch.cuda.Event()
         with torch.cuda.stream(self.s_in):
-            for src, dst in ((self.hd, self.d_in), (self.hv, self.v_in)):
-                for k in src:
-                    dst[k].copy_(src[k], non_blocking=True)
+            self.d_small.copy_(self.h_small, non_blocking=True)   # the decode and verify inputs
             ev_small.record(self.s_in)
         copy_in(0)   # the copy engine keeps one segment queued ahead of the compute
         cur.wait_event(ev_small)
@@ -356,8 +383,7 @@ class Workload:
         ev_dv.record(cur)
         with torch.cuda.stream(self.s_out):
             self.s_out.wait_event(ev_dv)
-            self.h_dout.copy_(self.d_out, non_blocking=True)
-            self.h_vout.copy_(self.v_out, non_blocking=True)
+            self.h_small_out.copy_(self.d_small_out, non_blocking=True)   # the decode and verify outputs
         for i, L in enumerate(segs):
             if i + 1 < len(segs):
                 copy_in(i + 1)
@@ -378,8 +404,8 @@ class Workload:
         return n
 
     def io_bytes(self):
-        h2d = sum(t.numel() * t.element_size() for d in (self.h, self.hd, self.hv) for t in d.values())
-        d2h = sum(t.numel() * t.element_size() for t in (self.h_pout, self.h_dout, self.h_vout))
+        h2d = sum(t.numel() * t.element_size() for t in self.h.values()) + self.h_small.numel()
+        d2h = sum(t.numel() * t.element_size() for t in (self.h_pout, self.h_small_out))
         return h2d, d2h
 
     def flush_l2(self):
