@@ -264,6 +264,9 @@ prefill_simt_kernel(const PrefillParams p) {
 // Runs after the main kernel so every CTA has read the old rows first.
 template <typename Tact>
 __global__ void conv_state_finalize_kernel(const PrefillParams p) {
+    // launched as a programmatic dependent of the prefill kernel, which reads the old rows
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int s = blockIdx.y;
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= p.C) return;
@@ -330,11 +333,17 @@ cudaError_t launch_prefill(const PrefillParams& p, int act_dtype, int out_dtype,
     if (e != cudaSuccess) return e;
     // the test hook leaves every state of the tensor-core path as it was
     if ((p.flags & kFlagTestStall) && use_tensor_cores(act_dtype, p.flags)) return cudaSuccess;
-    if (act_dtype == 1)
-        conv_state_finalize_kernel<__nv_bfloat16><<<dim3((p.C + 255) / 256, p.n_seq), 256, 0, stream>>>(p);
-    else
-        conv_state_finalize_kernel<float><<<dim3((p.C + 255) / 256, p.n_seq), 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.C + 255) / 256, p.n_seq);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see grid_dependency_wait
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return act_dtype == 1 ? cudaLaunchKernelEx(&cfg, conv_state_finalize_kernel<__nv_bfloat16>, p)
+                          : cudaLaunchKernelEx(&cfg, conv_state_finalize_kernel<float>, p);
 }
 
 }  // namespace gdn

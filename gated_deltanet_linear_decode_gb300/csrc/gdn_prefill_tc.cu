@@ -29,6 +29,10 @@ namespace {
 // the item counter and abort flag of this call.
 __global__ void chunk_table_kernel(const int* cu_seqlens, int n_seq, int* chunk_base, int* ready, int n_flags,
                                    int* consumed, int n_consumed, int* counter) {
+    // launched as a programmatic dependent: the previous kernel (a prefill of the same
+    // workspace, for one) is done before anything is cleared
+    grid_dependency_wait();
+    grid_launch_dependents();
     __shared__ int carry_s;
     __shared__ int warp_s[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
@@ -89,6 +93,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_fused_kernel(const __grid
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ int item_s;
     const int tid = threadIdx.x, warp = tid >> 5;
+    // launched as a programmatic dependent of the chunk-table kernel: nothing global (nor the
+    // tensor memory) is touched before it is done
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (static_cast<int>(blockIdx.x) < n_chain) {
         if (warp >= chain::kStateThreads / 32) return;   // the chain role runs on warps 0-13
         uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + chain::kBar + 8 * chain::kNumBars);
@@ -211,17 +219,46 @@ cudaError_t launch_tensor_core_prefill(const PrefillParams& p0, int out_dtype, c
     } else {
         p.ahead = p.n_chunks;   // gc < n_chunks: never gated
     }
-    chunk_table_kernel<<<1, 256, 0, stream>>>(p.cu_seqlens, p.n_seq, p.chunk_base, p.ready, p.n_chunks * p.Hv,
-                                              p.consumed, p.n_chunks * p.Hk, counter);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see grid_dependency_wait
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, chunk_table_kernel, static_cast<const int*>(p.cu_seqlens), p.n_seq,
+                                    p.chunk_base, p.ready, p.n_chunks * p.Hv, p.consumed, p.n_chunks * p.Hk,
+                                    counter)) != cudaSuccess)
+            return e;
+    }
 
     auto go = [&](auto kernel) -> cudaError_t {
         cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (r != cudaSuccess) return r;
-        int nc = n_chain;
-        void* args[] = {const_cast<PrefillParams*>(&p), &nc, &counter};
-        return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(kThreads), args, smem,
-                                           stream);
+        // cooperative (every CTA resident at once: chains wait on preparation CTAs) and a
+        // programmatic dependent of the chunk-table kernel
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        r = cudaLaunchKernelEx(&cfg, kernel, p, n_chain, counter);
+        if (r == cudaErrorInvalidValue || r == cudaErrorNotSupported) {   // the pair refused: a plain cooperative launch
+            (void)cudaGetLastError();
+            cfg.numAttrs = 1;
+            r = cudaLaunchKernelEx(&cfg, kernel, p, n_chain, counter);
+        }
+        return r;
     };
     return out_dtype == 1 ? go(prefill_fused_kernel<__nv_bfloat16>) : go(prefill_fused_kernel<float>);
 }
