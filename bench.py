@@ -749,6 +749,18 @@ def proj_part(dev):
     return run
 
 
+def decode_bf16_part(dev):
+    """The B=64 decode step (16/32 heads) with the state stored as bf16, as timed in `extras`."""
+    import gated_deltanet_linear_decode_gb300 as gdn
+    c = gdn_inputs.decode_b64()
+    d = gdn.make_dims(c.Hk, c.Hv, torch.bfloat16, torch.bfloat16, state_dtype=torch.bfloat16)
+    w = gdn.make_weights(c.conv_w, c.dt_bias, c.ssm_a, c.norm_w, device=dev)
+    i = {k: getattr(c, k).to(dev) for k in ("x", "z", "a_raw", "b_raw")}
+    conv, S = c.conv0.to(dev), c.S0.to(dev).to(torch.bfloat16)
+    o = torch.empty(c.N, c.Hv * 128, device=dev, dtype=torch.bfloat16)
+    return lambda: gdn.gdn_decode_step(d, w, i["x"], i["z"], i["a_raw"], i["b_raw"], conv, S, o)
+
+
 def run_part(args):
     """Warm-up then timed launches of one part only (profiling aid)."""
     dev = torch.device("cuda", 0)
@@ -757,6 +769,8 @@ def run_part(args):
     fn = {"prefill": wl.prefill, "decode": wl.decode, "verify": wl.verify}.get(args.only)
     if args.only == "proj":
         fn = proj_part(dev)
+    elif args.only == "decode-bf16":
+        fn = decode_bf16_part(dev)
     for _ in range(args.warmup + args.steps):
         wl.flush_l2()
         fn()
@@ -885,7 +899,7 @@ def main():
                     help="skip the batch-1 graph decode and the varlen T=65536 prefill (timed outside the step)")
     ap.add_argument("--prefill-tokens", type=int, default=8192,
                     help="with --only prefill: the sequence length (a smaller case for profiling)")
-    ap.add_argument("--only", choices=["prefill", "decode", "verify", "proj"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "verify", "proj", "decode-bf16"], default=None,
                     help="run only one part of the step (for profiling); no JSON line")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
