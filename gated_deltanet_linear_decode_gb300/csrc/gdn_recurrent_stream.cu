@@ -31,25 +31,8 @@ namespace gdn {
 
 namespace {
 
-constexpr int kSThreads = 256;     // compute: 8 warps x 16 rows
-constexpr int kProducerWarp = kSThreads / 32;
-constexpr int kLaunchThreads = kSThreads + 32;
-constexpr int kStages = 2;
-
-// Barrier among the compute warps only (the producer warp never joins it).
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSThreads) : "memory"); }
-// The same barrier, returning whether any compute thread passed a nonzero v
-// (one decision for all of them).
-__device__ __forceinline__ bool compute_sync_any(int v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(v), "n"(kSThreads)
-        : "memory");
-    return r != 0;
-}
+constexpr int kSThreads = 256;     // a compute group: 8 warps x 16 rows
+constexpr int kLaunchThreads = kSThreads + 32;   // one compute group and the producer warp
 constexpr int kWaitLimit = 1 << 22;   // polls of one stage wait before it gives up
 constexpr int kStallLimit = 1 << 12;  // polls of the test stall (a barrier nothing arrives on)
 
@@ -97,36 +80,72 @@ struct StageLayout {
 // then fits 96 registers, and two CTAs per SM keep two tiles' latency chains in flight
 // (2 x 9 warps leave 5 warps on some of the SM's four sub-partitions, whose 16,384
 // registers allow 96 a thread).  The stage goes back to the producer once the item is done.
+// An fp32 tile does not fit twice per SM that way, so the fp32 decode step (one token, no
+// folded projections) runs two compute groups of 8 warps in one CTA instead, each holding
+// one tile in a shared-memory stage, with three stages (the third one loading).
 constexpr int kMaxRegsSmemState = 96;
 
-template <typename Tact, typename Tout, typename Ts, bool kSmemState>
+// Stages of a CTA: three for two compute groups, else two.
+__host__ __device__ constexpr int stage_count(int groups) { return groups > 1 ? 3 : 2; }
+
+// Per-compute-group scratch after the stages (floats): q_hat|k_hat [K][256], v [K][128],
+// o [128], norm partials [16], RMS partials [8], gates [K][2], folded a/b partials [K][8][2].
+__host__ __device__ inline int group_scratch_floats(int K) { return (K * (256 + 128 + 2 + 16) + 152 + 3) & ~3; }
+
+// Shared-memory bytes: the stages, the copy of the small inputs (when the tile goes to
+// registers and its stage is handed back at once), norm_w, each group's scratch, barriers.
+__host__ __device__ inline size_t stream_smem_bytes(const StageLayout& L, int K, int groups, bool copy_inputs) {
+    const size_t cur = copy_inputs ? ((L.ab - L.cw + 15) & ~static_cast<size_t>(15)) : 0;
+    return static_cast<size_t>(stage_count(groups)) * L.bytes + cur +
+           4 * (128 + static_cast<size_t>(groups) * group_scratch_floats(K)) + (2 * stage_count(groups) + 1) * 8 + 16;
+}
+
+template <typename Tact, typename Tout, typename Ts, bool kSmemState, int kGroups>
 __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
     extern __shared__ __align__(128) uint8_t sm[];
     constexpr int es = sizeof(Tact), ss = sizeof(Ts);
+    constexpr int kStg = stage_count(kGroups);
+    constexpr int kProducer = kGroups * kSThreads / 32;   // the producer warp
+    static_assert(kSmemState || kGroups == 1, "two compute groups hold their tiles in shared memory");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // compute group cg (warps 8cg .. 8cg+7) and the thread's place in it
+    const int cg = kGroups > 1 ? (warp < kProducer ? tid / kSThreads : 0) : 0;
+    const int ctid = tid - cg * kSThreads, cwarp = ctid >> 5;
     const int K = p.K, C = p.C, HvD = p.Hv * kD;
     const int r = p.Hv / p.Hk;
     const int n_groups = p.B * p.Hk;
     const int H = p.ab_hidden ? p.ab_H : 0;
     const StageLayout L(K, es, ss, H);
-    // private copy of the current item's small inputs, after the stages
-    uint8_t* cur = sm + kStages * L.bytes;
+    // a private copy of the current item's small inputs (register form only), after the stages
+    uint8_t* cur = sm + kStg * L.bytes;
     const uint32_t cur_bytes = L.ab - L.cw;
-    float* qk_s = reinterpret_cast<float*>(cur + ((cur_bytes + 15) & ~15u));   // [K][256] q_hat | k_hat
-    float* v_s = qk_s + K * 256;                                                  // [K][128]
-    float* o_s = v_s + K * 128;                                                   // [128]
-    float* red = o_s + 128;                                                       // [2][8]
-    float* part = red + 16;                                                       // [8]
-    float* gates = part + 8;                                                      // [K][2]
-    float* nw_s = gates + 2 * kMaxK;                                              // [128]
-    float* abp = nw_s + 128;                                  // [K][8 warps][2] folded a/b partial sums
-    uint64_t* full = reinterpret_cast<uint64_t*>(abp + 16 * kMaxK);               // [kStages] stage landed
-    uint64_t* empty = full + kStages;                                              // [kStages] stage copied out
-    uint64_t* never = empty + kStages;                                             // test stall: no arrivals
-    volatile int* abort_s = reinterpret_cast<volatile int*>(never + 1);           // a wait gave up
+    float* nw_s = reinterpret_cast<float*>(cur + (kSmemState ? 0u : ((cur_bytes + 15) & ~15u)));   // [128]
+    float* qk_s = nw_s + 128 + cg * group_scratch_floats(K);                      // [K][256] q_hat | k_hat
+    float* v_s = qk_s + K * 256;                                                   // [K][128]
+    float* o_s = v_s + K * 128;                                                    // [128]
+    float* red = o_s + 128;                                                        // [2][8]
+    float* part = red + 16;                                                        // [8]
+    float* gates = part + 8;                                                       // [K][2]
+    float* abp = gates + 2 * K;                               // [K][8 warps][2] folded a/b partial sums
+    uint64_t* full = reinterpret_cast<uint64_t*>(nw_s + 128 + kGroups * group_scratch_floats(K));   // stage landed
+    uint64_t* empty = full + kStg;                                                 // stage copied out
+    uint64_t* never = empty + kStg;                                                // test stall: no arrivals
+    volatile int* abort_s = reinterpret_cast<volatile int*>(never + 1);            // a wait gave up
+    // the compute group's barrier (named barrier 1 + cg, its 256 threads only)
+    auto group_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + cg), "n"(kSThreads) : "memory"); };
+    auto group_sync_any = [&](int v) {   // the same, returning whether any thread of the group passed v != 0
+        uint32_t res;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(res)
+            : "r"(v), "r"(1 + cg), "n"(kSThreads)
+            : "memory");
+        return res != 0;
+    };
 
     if (tid == 0) {
-        for (int st = 0; st < kStages; ++st) {
+        for (int st = 0; st < kStg; ++st) {
             tc::mbar_init(&full[st], 1);
             tc::mbar_init(&empty[st], 1);
         }
@@ -141,17 +160,18 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
     __syncthreads();
     grid_launch_dependents();
 
-    // item i of this CTA -> (group, m)
+    // item i of this CTA -> (group, m); the items of a (sequence, q/k head) group are
+    // consecutive, and compute group cg takes the CTA's groups cg, cg + kGroups, ...
     const int G = gridDim.x;
     const int my_groups = blockIdx.x < n_groups ? (n_groups - 1 - blockIdx.x) / G + 1 : 0;
     const int n_items = my_groups * r;
     auto item_group = [&](int i) { return blockIdx.x + (i / r) * G; };
 
-    auto issue = [&](int i) {      // one thread: load item i into stage i % kStages
+    auto issue = [&](int i) {      // one thread: load item i into stage i % kStg
         const int g = item_group(i), m = i % r;
         const int b = g / p.Hk, kh = g % p.Hk, h = kh + m * p.Hk;
-        uint64_t* mb = &full[i % kStages];
-        const uint32_t base = tc::smem_u32(sm + (i % kStages) * L.bytes);
+        uint64_t* mb = &full[i % kStg];
+        const uint32_t base = tc::smem_u32(sm + (i % kStg) * L.bytes);
         const uint32_t seg = 128 * es;   // one head's channels of one row
         mbar_expect_tx(mb, L.bytes);
         const Ts* Sh = rec_state_in<Ts>(p, b) + static_cast<size_t>(h) * kD * kD;
@@ -180,19 +200,21 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
         }
     };
 
-    // Bit 4 of dev_status marks every (sequence, v-head) of item i and later
-    // items of this CTA: a wait gave up, so their states and outputs were not
-    // (fully) written.
-    auto report_from = [&](int i0, int idx, int cnt) {
+    // Bit 4 of dev_status marks every (sequence, v-head) of item i0 and the compute group's
+    // later items: a wait gave up, so their states and outputs were not (fully) written.
+    auto report_from = [&](int i0) {
         if (!p.dev_status) return;
-        for (int i = i0 + idx; i < n_items; i += cnt) {
+        int k = 0;
+        for (int i = i0; i < n_items; ++i) {
+            if ((i / r) % kGroups != cg) continue;
+            if (k++ % kSThreads != ctid) continue;
             const int g = item_group(i);
             atomicOr(p.dev_status + (g / p.Hk) * p.Hv + g % p.Hk + (i % r) * p.Hk, 16);
         }
     };
 
-    if (warp == kProducerWarp) {
-        // ================= producer: item i into stage i % kStages once item i - kStages has left it.
+    if (warp == kProducer) {
+        // ================= producer: item i into stage i % kStg once item i - kStg has left it.
         // On a wait that gives up it issues nothing more, and it returns only once
         // every copy it issued has landed (none may land in a released CTA).
         if (lane == 0) {
@@ -200,111 +222,117 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
             bool ok = true;
             if (p.flags & kFlagTestStall) ok = tc::mbar_wait(never, 0, kStallLimit);   // never completes
             for (int i = 0; i < n_items && ok; ++i) {
-                const int st = i % kStages;
-                if (i >= kStages && !(ok = stage_wait(&empty[st], ((i / kStages) - 1) & 1, abort_s))) break;
+                const int st = i % kStg;
+                if (i >= kStg && !(ok = stage_wait(&empty[st], ((i / kStg) - 1) & 1, abort_s))) break;
                 issue(i);
                 issued = i + 1;
             }
             if (!ok) {
                 *abort_s = 1;
-                for (int i = max(0, issued - kStages); i < issued; ++i)
-                    tc::mbar_wait(&full[i % kStages], (i / kStages) & 1, kWaitLimit);
+                for (int i = max(0, issued - kStg); i < issued; ++i)
+                    tc::mbar_wait(&full[i % kStg], (i / kStg) & 1, kWaitLimit);
             }
         }
         return;
     }
 
     float4 sreg[kSmemState ? 1 : 16];
-    for (int i = 0; i < n_items; ++i) {
-        const int g = item_group(i), m = i % r;
+    bool go_on = true;
+    for (int j = cg; j < my_groups && go_on; j += kGroups) {
+      for (int m = 0; m < r; ++m) {
+        const int i = j * r + m;
+        const int g = item_group(i);
         const int b = g / p.Hk, kh = g % p.Hk, h = kh + m * p.Hk;
-        const uint8_t* stg = sm + (i % kStages) * L.bytes;
+        const uint8_t* stg = sm + (i % kStg) * L.bytes;
         // gates for the item's tokens: plain loads, issued before the wait
         float a_raw = 0.f, b_raw = 0.f;
-        if (tid < K && !p.ab_hidden) {
-            const size_t gi = (static_cast<size_t>(b) * K + tid) * p.Hv + h;
+        if (ctid < K && !p.ab_hidden) {
+            const size_t gi = (static_cast<size_t>(b) * K + ctid) * p.Hv + h;
             a_raw = ld_act(static_cast<const Tact*>(p.a_raw) + gi);
             b_raw = ld_act(static_cast<const Tact*>(p.b_raw) + gi);
         }
         const float a_dt = p.dt_bias[h], a_ssm = p.ssm_a[h];
-        const bool landed = stage_wait(&full[i % kStages], (i / kStages) & 1, abort_s);
-        // state rows -> registers (or left in the stage); small inputs -> private area
-        uint8_t* const srow = const_cast<uint8_t*>(stg) + ((warp * 16) * kD + 4 * lane) * ss;   // my rows in the stage
+        const bool landed = stage_wait(&full[i % kStg], (i / kStg) & 1, abort_s);
+        // state rows -> registers (or left in the stage); small inputs -> private area (or read
+        // in the stage, which the item then holds)
+        uint8_t* const srow = const_cast<uint8_t*>(stg) + ((cwarp * 16) * kD + 4 * lane) * ss;   // my rows in the stage
         if constexpr (!kSmemState) {
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) sreg[rr] = StateIO<Ts>::ld(srow + rr * kD * ss);
+            for (uint32_t e = ctid * 16; e < cur_bytes; e += kSThreads * 16)
+                *reinterpret_cast<uint4*>(cur + e) = *reinterpret_cast<const uint4*>(stg + L.cw + e);
         }
-        for (uint32_t e = tid * 16; e < cur_bytes; e += kSThreads * 16)
-            *reinterpret_cast<uint4*>(cur + e) = *reinterpret_cast<const uint4*>(stg + L.cw + e);
-        if (tid < K && !H) {
-            gates[2 * tid] = sigmoidf_(b_raw);
-            gates[2 * tid + 1] = a_ssm * softplusf_(a_raw + a_dt);
+        const uint8_t* in = kSmemState ? stg + L.cw : cur;
+        if (ctid < K && !H) {
+            gates[2 * ctid] = sigmoidf_(b_raw);
+            gates[2 * ctid + 1] = a_ssm * softplusf_(a_raw + a_dt);
         }
         if (H > 0) {
             // ssm_alpha / ssm_beta folded in: each compute thread's share of the dot products of
             // the token's hidden row with W_a[h], W_b[h] (all in the stage), summed over warps below
             const __nv_bfloat16* sab = reinterpret_cast<const __nv_bfloat16*>(stg + L.ab);
             for (int t = 0; t < K; ++t) {
-                const float2 pr = ab_dot_part<false>(sab + t * H, sab + K * H, sab + (K + 1) * H, H, tid, kSThreads);
+                const float2 pr = ab_dot_part<false>(sab + t * H, sab + K * H, sab + (K + 1) * H, H, ctid, kSThreads);
                 const float sa = warp_sum(pr.x), sb = warp_sum(pr.y);
                 if (lane == 0) {
-                    abp[(t * 8 + warp) * 2] = sa;
-                    abp[(t * 8 + warp) * 2 + 1] = sb;
+                    abp[(t * 8 + cwarp) * 2] = sa;
+                    abp[(t * 8 + cwarp) * 2 + 1] = sb;
                 }
             }
         }
-        // one decision for all compute warps, before anything is written: stop at the
+        // one decision for the group's warps, before anything is written: stop at the
         // first item whose stage did not land (what was read from it is discarded)
-        if (compute_sync_any(!landed)) {
+        if (group_sync_any(!landed)) {
             *abort_s = 1;
-            report_from(i, tid, kSThreads);
+            report_from(i);
+            go_on = false;
             break;
         }
-        if (!kSmemState && tid == 0) tc::mbar_arrive(&empty[i % kStages]);   // the stage may be refilled
-        if (H > 0 && tid < K) {
+        if (!kSmemState && ctid == 0) tc::mbar_arrive(&empty[i % kStg]);   // the stage may be refilled
+        if (H > 0 && ctid < K) {
             // the folded a_raw, b_raw: the warps' partial sums (the next barrier orders them
             // before step 7)
             float sa = 0.f, sb = 0.f;
 #pragma unroll
             for (int w8 = 0; w8 < 8; ++w8) {
-                sa += abp[(tid * 8 + w8) * 2];
-                sb += abp[(tid * 8 + w8) * 2 + 1];
+                sa += abp[(ctid * 8 + w8) * 2];
+                sb += abp[(ctid * 8 + w8) * 2 + 1];
             }
-            gates[2 * tid] = sigmoidf_(sb);
-            gates[2 * tid + 1] = a_ssm * softplusf_(sa + a_dt);
+            gates[2 * ctid] = sigmoidf_(sb);
+            gates[2 * ctid + 1] = a_ssm * softplusf_(sa + a_dt);
         }
 
-        const float4* cw = reinterpret_cast<const float4*>(cur);                      // [384] taps
-        const Tact* xr = reinterpret_cast<const Tact*>(cur + (L.xr - L.cw));           // [K+3][384]
-        const Tact* zr = reinterpret_cast<const Tact*>(cur + (L.zr - L.cw));           // [K][128]
+        const float4* cw = reinterpret_cast<const float4*>(in);                       // [384] taps
+        const Tact* xr = reinterpret_cast<const Tact*>(in + (L.xr - L.cw));            // [K+3][384]
+        const Tact* zr = reinterpret_cast<const Tact*>(in + (L.zr - L.cw));            // [K][128]
         // ---- steps 1-4 for every token of the item: thread c < 256 owns q/k channel c, c < 128 v channel c.
         // q_hat and k_hat belong to the group: the group's first head computes them, the others reuse them.
         if (m > 0) {
-            if (tid < kD) {
-                const float4 wv = cw[256 + tid];
+            if (ctid < kD) {
+                const float4 wv = cw[256 + ctid];
                 for (int t = 0; t < K; ++t)
-                    v_s[t * kD + tid] =
-                        siluf_(conv4(wv, to_f(xr[t * 384 + 256 + tid]), to_f(xr[(t + 1) * 384 + 256 + tid]),
-                                     to_f(xr[(t + 2) * 384 + 256 + tid]), to_f(xr[(t + 3) * 384 + 256 + tid])));
+                    v_s[t * kD + ctid] =
+                        siluf_(conv4(wv, to_f(xr[t * 384 + 256 + ctid]), to_f(xr[(t + 1) * 384 + 256 + ctid]),
+                                     to_f(xr[(t + 2) * 384 + 256 + ctid]), to_f(xr[(t + 3) * 384 + 256 + ctid])));
             }
-            compute_sync();
+            group_sync();
         } else {
-            const float4 w = cw[tid];
-            const float4 wv = tid < kD ? cw[256 + tid] : make_float4(0, 0, 0, 0);
+            const float4 w = cw[ctid];
+            const float4 wv = ctid < kD ? cw[256 + ctid] : make_float4(0, 0, 0, 0);
             for (int t = 0; t < K; ++t) {
-                const float val = siluf_(conv4(w, to_f(xr[t * 384 + tid]), to_f(xr[(t + 1) * 384 + tid]),
-                                               to_f(xr[(t + 2) * 384 + tid]), to_f(xr[(t + 3) * 384 + tid])));
-                const float ss = warp_sum(val * val);
-                if (lane == 0) red[(warp >> 2) * 8 + (warp & 3)] = ss;
-                if (tid < kD)
-                    v_s[t * kD + tid] =
-                        siluf_(conv4(wv, to_f(xr[t * 384 + 256 + tid]), to_f(xr[(t + 1) * 384 + 256 + tid]),
-                                     to_f(xr[(t + 2) * 384 + 256 + tid]), to_f(xr[(t + 3) * 384 + 256 + tid])));
-                compute_sync();
-                const float* rd = red + (warp >> 2) * 8;
+                const float val = siluf_(conv4(w, to_f(xr[t * 384 + ctid]), to_f(xr[(t + 1) * 384 + ctid]),
+                                               to_f(xr[(t + 2) * 384 + ctid]), to_f(xr[(t + 3) * 384 + ctid])));
+                const float sq = warp_sum(val * val);
+                if (lane == 0) red[(cwarp >> 2) * 8 + (cwarp & 3)] = sq;
+                if (ctid < kD)
+                    v_s[t * kD + ctid] =
+                        siluf_(conv4(wv, to_f(xr[t * 384 + 256 + ctid]), to_f(xr[(t + 1) * 384 + 256 + ctid]),
+                                     to_f(xr[(t + 2) * 384 + 256 + ctid]), to_f(xr[(t + 3) * 384 + 256 + ctid])));
+                group_sync();
+                const float* rd = red + (cwarp >> 2) * 8;
                 const float nrm = sqrtf((rd[0] + rd[1]) + (rd[2] + rd[3]));
-                qk_s[t * 256 + tid] = val / fmaxf(nrm, p.eps);
-                compute_sync();
+                qk_s[t * 256 + ctid] = val / fmaxf(nrm, p.eps);
+                group_sync();
             }
         }
 
@@ -316,7 +344,7 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
             const float kq = warp_sum(fmaf(kk.w, qq.w, fmaf(kk.z, qq.z, fmaf(kk.y, qq.y, kk.x * qq.x))));
             const float beta = gates[2 * t];
             const float eg = expf(gates[2 * t + 1]);
-            Ts* Sout = rec_state_out<Ts>(p, b, t) + (static_cast<size_t>(h) * kD + warp * 16) * kD;
+            Ts* Sout = rec_state_out<Ts>(p, b, t) + (static_cast<size_t>(h) * kD + cwarp * 16) * kD;
             // partial S.k and S.q of my 16 rows: slot 2rr = row rr . k, slot 2rr+1 = row rr . q
             float pv[32];
 #pragma unroll
@@ -328,7 +356,7 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
             const float full_sum = reduce32_transposed(pv);   // lane 2rr: (S k)_rr, lane 2rr+1: (S q)_rr
             const int my_row = lane >> 1;
             // d = (v - e^g S.k) beta in the even lane; the odd lane forms o from it
-            const float d_even = (v_s[t * kD + warp * 16 + my_row] - eg * full_sum) * beta;
+            const float d_even = (v_s[t * kD + cwarp * 16 + my_row] - eg * full_sum) * beta;
             const float d_pair = __shfl_xor_sync(0xffffffffu, d_even, 1);
             const float o = fmaf(d_pair, kq, eg * full_sum) * kInvSqrtD;   // meaningful in odd lanes
             const float o_mine = (lane & 1) ? o : 0.f;
@@ -352,19 +380,19 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
                 if (status && (nonfinite_bits(nv.x) | nonfinite_bits(nv.y) | nonfinite_bits(nv.z) | nonfinite_bits(nv.w)))
                     atomicOr(status, 1);
             }
-            if (lane & 1) o_s[warp * 16 + my_row] = o;
-            if (lane == 0) part[warp] = ps;
-            compute_sync();
+            if (lane & 1) o_s[cwarp * 16 + my_row] = o;
+            if (lane == 0) part[cwarp] = ps;
+            group_sync();
             // ---- step 8: gated RMSNorm, thread c < 128 -> output j = c
             const size_t row = static_cast<size_t>(b) * K + t;
-            if (tid < kD) {
+            if (ctid < kD) {
                 float tot = 0.f;
 #pragma unroll
                 for (int w = 0; w < 8; ++w) tot += part[w];
                 const float rs = 1.0f / sqrtf(tot * (1.0f / kD) + p.eps);
-                const float ov = o_s[tid];
-                const float y = ov * rs * nw_s[tid] * siluf_(to_f(zr[t * kD + tid]));
-                const size_t oi = row * HvD + h * kD + tid;
+                const float ov = o_s[ctid];
+                const float y = ov * rs * nw_s[ctid] * siluf_(to_f(zr[t * kD + ctid]));
+                const size_t oi = row * HvD + h * kD + ctid;
                 st_out(static_cast<Tout*>(p.out) + oi, y);
                 if (p.prenorm) p.prenorm[oi] = ov;
                 if (status && nonfinite_bits(y)) atomicOr(status, 2);
@@ -374,63 +402,80 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
             // group has its inputs staged before that head runs).
             Tact* cout = static_cast<Tact*>(p.conv_out) + static_cast<size_t>(b) * p.conv_out_b +
                          static_cast<size_t>(t) * p.conv_out_p;
-            if (tid < kD) {
-                const int cv = 2 * p.Hk * kD + h * kD + tid;
+            if (ctid < kD) {
+                const int cv = 2 * p.Hk * kD + h * kD + ctid;
 #pragma unroll
-                for (int q = 0; q < 3; ++q) cout[q * C + cv] = xr[(t + 1 + q) * 384 + 256 + tid];
+                for (int q = 0; q < 3; ++q) cout[q * C + cv] = xr[(t + 1 + q) * 384 + 256 + ctid];
             }
             if (m == r - 1) {
-                const int ch = tid < kD ? kh * kD + tid : p.Hk * kD + kh * kD + (tid - kD);
+                const int ch = ctid < kD ? kh * kD + ctid : p.Hk * kD + kh * kD + (ctid - kD);
 #pragma unroll
-                for (int q = 0; q < 3; ++q) cout[q * C + ch] = xr[(t + 1 + q) * 384 + tid];
+                for (int q = 0; q < 3; ++q) cout[q * C + ch] = xr[(t + 1 + q) * 384 + ctid];
             }
-            compute_sync();
+            group_sync();
         }
         if constexpr (kSmemState) {
             // the item is done with its stage: hand it back (the generic writes of the state
             // above are ordered before the producer's next bulk copy into it)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            compute_sync();
-            if (tid == 0) tc::mbar_arrive(&empty[i % kStages]);
+            group_sync();
+            if (ctid == 0) tc::mbar_arrive(&empty[i % kStg]);
         }
+      }
     }
 }
 
 template <typename Tact, typename Tout>
 __global__ void __launch_bounds__(kLaunchThreads, 1) recurrent_stream_kernel(const RecParams p) {
-    recurrent_stream_body<Tact, Tout, float, false>(p);
+    recurrent_stream_body<Tact, Tout, float, false, 1>(p);
 }
 template <typename Tout>
 __global__ void __maxnreg__(kMaxRegsSmemState) recurrent_stream_bf16s_kernel(const RecParams p) {
-    recurrent_stream_body<__nv_bfloat16, Tout, __nv_bfloat16, true>(p);
+    recurrent_stream_body<__nv_bfloat16, Tout, __nv_bfloat16, true, 1>(p);
+}
+// fp32 state, two compute groups of 8 warps and the producer warp (17 warps: 96 registers)
+constexpr int kLaunchThreads2 = 2 * kSThreads + 32;
+template <typename Tact, typename Tout>
+__global__ void __maxnreg__(kMaxRegsSmemState) recurrent_stream_2g_kernel(const RecParams p) {
+    recurrent_stream_body<Tact, Tout, float, true, 2>(p);
 }
 
 }  // namespace
 
+// Shared memory of the form launch_recurrent_stream falls back to (one compute group): what
+// the caller checks against the device's limit before choosing the streaming kernel.
 size_t recurrent_stream_smem(int K, int act_dtype, bool state_bf16, int ab_H) {
     const int es = act_dtype == 1 ? 2 : 4;
     const StageLayout L(K, es, state_bf16 ? 2 : 4, ab_H);
-    const size_t cur = ((L.ab - L.cw + 15) & ~static_cast<size_t>(15));
-    const size_t misc = (static_cast<size_t>(K) * 384 + 128 + 16 + 8 + 2 * kMaxK + 128 + 16 * kMaxK) * 4 +
-                        2 * kStages * 8 + 16;
-    return kStages * static_cast<size_t>(L.bytes) + cur + misc;
+    return stream_smem_bytes(L, K, 1, !state_bf16);
 }
 
 cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_dtype, int grid, cudaStream_t stream) {
     const bool sbf = (p.flags & kFlagStateBf16) != 0;
-    const size_t smem = recurrent_stream_smem(p.K, act_dtype, sbf, p.ab_hidden ? p.ab_H : 0);
-    auto go = [&](auto kernel) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
+    const int es = act_dtype == 1 ? 2 : 4;
+    const int H = p.ab_hidden ? p.ab_H : 0;
+    const StageLayout L(p.K, es, sbf ? 2 : 4, H);
+    int dev = 0, optin = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+    // an fp32 decode step without folded projections: two compute groups when their three
+    // stages fit
+    const size_t smem2 = stream_smem_bytes(L, p.K, 2, false);
+    const bool two_groups = !sbf && p.K == 1 && H == 0 && smem2 <= static_cast<size_t>(optin);
+    const size_t smem = two_groups ? smem2 : stream_smem_bytes(L, p.K, 1, !sbf);
+    auto go = [&](auto kernel, int threads) {
+        cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (r != cudaSuccess) return r;
         int per_sm = 1;
         if (sbf) {   // as many CTAs per SM as fit (the bf16-state kernel is built for two)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kLaunchThreads, smem);
-            if (e != cudaSuccess) return e;
+            r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+            if (r != cudaSuccess) return r;
             per_sm = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
         }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(grid * per_sm));
-        cfg.blockDim = dim3(kLaunchThreads);
+        cfg.blockDim = dim3(static_cast<unsigned>(threads));
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
@@ -442,10 +487,20 @@ cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_d
     };
     using bf = __nv_bfloat16;
     if (sbf)   // bf16 activations only (checked by the API)
-        return out_dtype == 1 ? go(recurrent_stream_bf16s_kernel<bf>) : go(recurrent_stream_bf16s_kernel<float>);
+        return out_dtype == 1 ? go(recurrent_stream_bf16s_kernel<bf>, kLaunchThreads)
+                              : go(recurrent_stream_bf16s_kernel<float>, kLaunchThreads);
+    if (two_groups) {
+        if (act_dtype == 1)
+            return out_dtype == 1 ? go(recurrent_stream_2g_kernel<bf, bf>, kLaunchThreads2)
+                                  : go(recurrent_stream_2g_kernel<bf, float>, kLaunchThreads2);
+        return out_dtype == 1 ? go(recurrent_stream_2g_kernel<float, bf>, kLaunchThreads2)
+                              : go(recurrent_stream_2g_kernel<float, float>, kLaunchThreads2);
+    }
     if (act_dtype == 1)
-        return out_dtype == 1 ? go(recurrent_stream_kernel<bf, bf>) : go(recurrent_stream_kernel<bf, float>);
-    return out_dtype == 1 ? go(recurrent_stream_kernel<float, bf>) : go(recurrent_stream_kernel<float, float>);
+        return out_dtype == 1 ? go(recurrent_stream_kernel<bf, bf>, kLaunchThreads)
+                              : go(recurrent_stream_kernel<bf, float>, kLaunchThreads);
+    return out_dtype == 1 ? go(recurrent_stream_kernel<float, bf>, kLaunchThreads)
+                          : go(recurrent_stream_kernel<float, float>, kLaunchThreads);
 }
 
 }  // namespace gdn
