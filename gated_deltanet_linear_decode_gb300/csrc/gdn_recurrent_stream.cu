@@ -85,26 +85,27 @@ struct StageLayout {
 // one tile in a shared-memory stage, with three stages (the third one loading).
 constexpr int kMaxRegsSmemState = 96;
 
-// Stages of a CTA: three for two compute groups, else two.
-__host__ __device__ constexpr int stage_count(int groups) { return groups > 1 ? 3 : 2; }
+// Stages of a CTA: two, or three for two compute groups where they fit (one loading while
+// both groups update theirs).
+__host__ __device__ constexpr int stage_count(int groups, bool third) { return groups > 1 && third ? 3 : 2; }
 
 // Per-compute-group scratch after the stages (floats): q_hat|k_hat [K][256], v [K][128],
 // o [128], norm partials [16], RMS partials [8], gates [K][2], folded a/b partials [K][8][2].
 __host__ __device__ inline int group_scratch_floats(int K) { return (K * (256 + 128 + 2 + 16) + 152 + 3) & ~3; }
 
 // Shared-memory bytes: the stages, the copy of the small inputs (when the tile goes to
-// registers and its stage is handed back at once), norm_w, each group's scratch, barriers.
-__host__ __device__ inline size_t stream_smem_bytes(const StageLayout& L, int K, int groups, bool copy_inputs) {
+// registers and its stage is handed back at once), norm_w, each group's scratch, barriers
+// ("full" per stage and compute group, "empty" per stage, the test-stall barrier).
+__host__ __device__ inline size_t stream_smem_bytes(const StageLayout& L, int K, int groups, int stages, bool copy_inputs) {
     const size_t cur = copy_inputs ? ((L.ab - L.cw + 15) & ~static_cast<size_t>(15)) : 0;
-    return static_cast<size_t>(stage_count(groups)) * L.bytes + cur +
-           4 * (128 + static_cast<size_t>(groups) * group_scratch_floats(K)) + (2 * stage_count(groups) + 1) * 8 + 16;
+    return static_cast<size_t>(stages) * L.bytes + cur +
+           4 * (128 + static_cast<size_t>(groups) * group_scratch_floats(K)) + ((groups + 1) * stages + 1) * 8 + 16;
 }
 
-template <typename Tact, typename Tout, typename Ts, bool kSmemState, int kGroups>
+template <typename Tact, typename Tout, typename Ts, bool kSmemState, int kGroups, int kStg>
 __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
     extern __shared__ __align__(128) uint8_t sm[];
     constexpr int es = sizeof(Tact), ss = sizeof(Ts);
-    constexpr int kStg = stage_count(kGroups);
     constexpr int kProducer = kGroups * kSThreads / 32;   // the producer warp
     static_assert(kSmemState || kGroups == 1, "two compute groups hold their tiles in shared memory");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -127,8 +128,11 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
     float* part = red + 16;                                                        // [8]
     float* gates = part + 8;                                                       // [K][2]
     float* abp = gates + 2 * K;                               // [K][8 warps][2] folded a/b partial sums
-    uint64_t* full = reinterpret_cast<uint64_t*>(nw_s + 128 + kGroups * group_scratch_floats(K));   // stage landed
-    uint64_t* empty = full + kStg;                                                 // stage copied out
+    // full[s * kGroups + g]: stage s landed with an item of compute group g.  Each group waits
+    // only on its own barriers, so it sees every phase of them in order (a group that skipped
+    // the other group's fills of a shared stage could not tell one phase from the next but one).
+    uint64_t* full = reinterpret_cast<uint64_t*>(nw_s + 128 + kGroups * group_scratch_floats(K));
+    uint64_t* empty = full + kStg * kGroups;                                       // stage s handed back
     uint64_t* never = empty + kStg;                                                // test stall: no arrivals
     volatile int* abort_s = reinterpret_cast<volatile int*>(never + 1);            // a wait gave up
     // the compute group's barrier (named barrier 1 + cg, its 256 threads only)
@@ -146,7 +150,7 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
 
     if (tid == 0) {
         for (int st = 0; st < kStg; ++st) {
-            tc::mbar_init(&full[st], 1);
+            for (int gg = 0; gg < kGroups; ++gg) tc::mbar_init(&full[st * kGroups + gg], 1);
             tc::mbar_init(&empty[st], 1);
         }
         tc::mbar_init(never, 1);
@@ -170,7 +174,7 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
     auto issue = [&](int i) {      // one thread: load item i into stage i % kStg
         const int g = item_group(i), m = i % r;
         const int b = g / p.Hk, kh = g % p.Hk, h = kh + m * p.Hk;
-        uint64_t* mb = &full[i % kStg];
+        uint64_t* mb = &full[(i % kStg) * kGroups + (i / r) % kGroups];
         const uint32_t base = tc::smem_u32(sm + (i % kStg) * L.bytes);
         const uint32_t seg = 128 * es;   // one head's channels of one row
         mbar_expect_tx(mb, L.bytes);
@@ -220,17 +224,23 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
         if (lane == 0) {
             int issued = 0;
             bool ok = true;
+            uint32_t fills = 0;      // parity of the fills of each full barrier so far (bit s * kGroups + g)
+            uint32_t last_par = 0;   // parity of the fill of the last item issued into each stage (bit s)
             if (p.flags & kFlagTestStall) ok = tc::mbar_wait(never, 0, kStallLimit);   // never completes
             for (int i = 0; i < n_items && ok; ++i) {
-                const int st = i % kStg;
+                const int st = i % kStg, fb = st * kGroups + (i / r) % kGroups;
                 if (i >= kStg && !(ok = stage_wait(&empty[st], ((i / kStg) - 1) & 1, abort_s))) break;
                 issue(i);
+                last_par = (last_par & ~(1u << st)) | (((fills >> fb) & 1u) << st);
+                fills ^= 1u << fb;
                 issued = i + 1;
             }
             if (!ok) {
                 *abort_s = 1;
-                for (int i = max(0, issued - kStg); i < issued; ++i)
-                    tc::mbar_wait(&full[i % kStg], (i / kStg) & 1, kWaitLimit);
+                for (int i = max(0, issued - kStg); i < issued; ++i) {
+                    const int st = i % kStg;
+                    tc::mbar_wait(&full[st * kGroups + (i / r) % kGroups], (last_par >> st) & 1u, kWaitLimit);
+                }
             }
         }
         return;
@@ -238,6 +248,7 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
 
     float4 sreg[kSmemState ? 1 : 16];
     bool go_on = true;
+    uint32_t phase = 0;   // parity of the next fill of full[s * kGroups + cg] this group waits for (bit s)
     for (int j = cg; j < my_groups && go_on; j += kGroups) {
       for (int m = 0; m < r; ++m) {
         const int i = j * r + m;
@@ -252,7 +263,9 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
             b_raw = ld_act(static_cast<const Tact*>(p.b_raw) + gi);
         }
         const float a_dt = p.dt_bias[h], a_ssm = p.ssm_a[h];
-        const bool landed = stage_wait(&full[i % kStg], (i / kStg) & 1, abort_s);
+        const int st = i % kStg;
+        const bool landed = stage_wait(&full[st * kGroups + cg], (phase >> st) & 1u, abort_s);
+        phase ^= 1u << st;
         // state rows -> registers (or left in the stage); small inputs -> private area (or read
         // in the stage, which the item then holds)
         uint8_t* const srow = const_cast<uint8_t*>(stg) + ((cwarp * 16) * kD + 4 * lane) * ss;   // my rows in the stage
@@ -427,17 +440,17 @@ __device__ __forceinline__ void recurrent_stream_body(const RecParams& p) {
 
 template <typename Tact, typename Tout>
 __global__ void __launch_bounds__(kLaunchThreads, 1) recurrent_stream_kernel(const RecParams p) {
-    recurrent_stream_body<Tact, Tout, float, false, 1>(p);
+    recurrent_stream_body<Tact, Tout, float, false, 1, 2>(p);
 }
 template <typename Tout>
 __global__ void __maxnreg__(kMaxRegsSmemState) recurrent_stream_bf16s_kernel(const RecParams p) {
-    recurrent_stream_body<__nv_bfloat16, Tout, __nv_bfloat16, true, 1>(p);
+    recurrent_stream_body<__nv_bfloat16, Tout, __nv_bfloat16, true, 1, 2>(p);
 }
 // fp32 state, two compute groups of 8 warps and the producer warp (17 warps: 96 registers)
 constexpr int kLaunchThreads2 = 2 * kSThreads + 32;
-template <typename Tact, typename Tout>
+template <typename Tact, typename Tout, int kStg>
 __global__ void __maxnreg__(kMaxRegsSmemState) recurrent_stream_2g_kernel(const RecParams p) {
-    recurrent_stream_body<Tact, Tout, float, true, 2>(p);
+    recurrent_stream_body<Tact, Tout, float, true, 2, kStg>(p);
 }
 
 }  // namespace
@@ -447,7 +460,7 @@ __global__ void __maxnreg__(kMaxRegsSmemState) recurrent_stream_2g_kernel(const 
 size_t recurrent_stream_smem(int K, int act_dtype, bool state_bf16, int ab_H) {
     const int es = act_dtype == 1 ? 2 : 4;
     const StageLayout L(K, es, state_bf16 ? 2 : 4, ab_H);
-    return stream_smem_bytes(L, K, 1, !state_bf16);
+    return stream_smem_bytes(L, K, 1, 2, !state_bf16);
 }
 
 cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_dtype, int grid, cudaStream_t stream) {
@@ -459,11 +472,12 @@ cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_d
     cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
-    // an fp32 decode step without folded projections: two compute groups when their three
-    // stages fit
-    const size_t smem2 = stream_smem_bytes(L, p.K, 2, false);
-    const bool two_groups = !sbf && p.K == 1 && H == 0 && smem2 <= static_cast<size_t>(optin);
-    const size_t smem = two_groups ? smem2 : stream_smem_bytes(L, p.K, 1, !sbf);
+    // an fp32 state without folded projections: two compute groups, with three stages where
+    // they fit (the decode step), else two (the verify walk)
+    const size_t smem3 = stream_smem_bytes(L, p.K, 2, 3, false), smem22 = stream_smem_bytes(L, p.K, 2, 2, false);
+    const bool two_groups = !sbf && H == 0 && smem22 <= static_cast<size_t>(optin);
+    const bool third = smem3 <= static_cast<size_t>(optin);
+    const size_t smem = two_groups ? (third ? smem3 : smem22) : stream_smem_bytes(L, p.K, 1, 2, !sbf);
     auto go = [&](auto kernel, int threads) {
         cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (r != cudaSuccess) return r;
@@ -489,12 +503,19 @@ cudaError_t launch_recurrent_stream(const RecParams& p, int act_dtype, int out_d
     if (sbf)   // bf16 activations only (checked by the API)
         return out_dtype == 1 ? go(recurrent_stream_bf16s_kernel<bf>, kLaunchThreads)
                               : go(recurrent_stream_bf16s_kernel<float>, kLaunchThreads);
+    if (two_groups && third) {
+        if (act_dtype == 1)
+            return out_dtype == 1 ? go(recurrent_stream_2g_kernel<bf, bf, 3>, kLaunchThreads2)
+                                  : go(recurrent_stream_2g_kernel<bf, float, 3>, kLaunchThreads2);
+        return out_dtype == 1 ? go(recurrent_stream_2g_kernel<float, bf, 3>, kLaunchThreads2)
+                              : go(recurrent_stream_2g_kernel<float, float, 3>, kLaunchThreads2);
+    }
     if (two_groups) {
         if (act_dtype == 1)
-            return out_dtype == 1 ? go(recurrent_stream_2g_kernel<bf, bf>, kLaunchThreads2)
-                                  : go(recurrent_stream_2g_kernel<bf, float>, kLaunchThreads2);
-        return out_dtype == 1 ? go(recurrent_stream_2g_kernel<float, bf>, kLaunchThreads2)
-                              : go(recurrent_stream_2g_kernel<float, float>, kLaunchThreads2);
+            return out_dtype == 1 ? go(recurrent_stream_2g_kernel<bf, bf, 2>, kLaunchThreads2)
+                                  : go(recurrent_stream_2g_kernel<bf, float, 2>, kLaunchThreads2);
+        return out_dtype == 1 ? go(recurrent_stream_2g_kernel<float, bf, 2>, kLaunchThreads2)
+                              : go(recurrent_stream_2g_kernel<float, float, 2>, kLaunchThreads2);
     }
     if (act_dtype == 1)
         return out_dtype == 1 ? go(recurrent_stream_kernel<bf, bf>, kLaunchThreads)
