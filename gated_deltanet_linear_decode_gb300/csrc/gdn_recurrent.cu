@@ -250,6 +250,9 @@ recurrent_kernel(const RecParams p) {
 
 // Commit: copy checkpoint accept_len[b]-1 into the live state (bit-exact).
 __global__ void commit_kernel(const CommitParams p) {
+    // launched as a programmatic dependent of the verify walk, whose checkpoints it reads
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int b = blockIdx.y;
     const int n = p.accept_len[b];
     if (n < 1 || n > p.K) return;
@@ -397,8 +400,16 @@ cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream) {
     unsigned bx = static_cast<unsigned>((per + 255) / 256);
     if (bx > 64) bx = 64;
     if (bx < 1) bx = 1;
-    commit_kernel<<<dim3(bx, p.B), 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(bx, static_cast<unsigned>(p.B));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see grid_dependency_wait
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, commit_kernel, p);
 }
 
 cudaError_t launch_conv_init(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
