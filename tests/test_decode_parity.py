@@ -180,6 +180,42 @@ def test_large_batch_verify_bitexact_vs_decode(K, act):
     assert G.conv_bits_equal(ck_conv, c_ck_ref, act)
 
 
+@pytest.mark.parametrize("B,Hk,Hv,K", [(19, 16, 32, 1), (23, 16, 32, 1), (37, 16, 48, 1), (23, 16, 32, 3), (41, 8, 24, 2)])
+def test_streaming_kernel_uneven_groups(B, Hk, Hv, K):
+    """Batches just above the streaming kernel's threshold: each CTA gets two or three
+    (sequence, q/k head) groups, so its two compute groups carry unequal loads and share
+    the stages unevenly.  The decode step against the oracle; the verify walk's
+    checkpoints against decode replays bit for bit and the oracle."""
+    c = gdn_inputs.make_case("ug", Hk=Hk, Hv=Hv, B=B, K=K, seed=5100 + B * K + Hv)
+    d, w = G.dims(c), G.weights(c)
+    conv0, S0 = G.dev(c.conv0), G.dev(c.S0)
+    if K == 1:
+        out, _, conv, S, _ = _decode(c)
+        ref = oracle.forward(c.Hk, c.Hv, c.x, c.z, c.a_raw, c.b_raw, c.conv_w, c.dt_bias, c.ssm_a, c.norm_w,
+                             c.conv0, c.S0, cu_seqlens=np.arange(B + 1))
+        G.assert_out_close(out, ref.out, c.act_dtype)
+        G.assert_state_close(S, ref.S, c.act_dtype)
+        assert G.conv_bits_equal(conv, ref.conv_state, c.act_dtype)
+        return
+    ck_conv = torch.empty(B, K, 3, c.C, device="cuda", dtype=c.act_dtype)
+    ck_S = torch.empty(B, K, c.Hv, 128, 128, device="cuda")
+    out = torch.empty(B * K, c.Hv * 128, device="cuda")
+    gdn.gdn_verify_k(d, w, K, G.dev(c.x), G.dev(c.z), G.dev(c.a_raw), G.dev(c.b_raw), conv0, S0, ck_conv, ck_S, out)
+    conv, S = conv0.clone(), S0.clone()
+    xs = c.x.view(B, K, -1); zs = c.z.view(B, K, -1); as_ = c.a_raw.view(B, K, -1); bs = c.b_raw.view(B, K, -1)
+    for p in range(K):
+        o = torch.empty(B, c.Hv * 128, device="cuda")
+        gdn.gdn_decode_step(d, w, G.dev(xs[:, p]), G.dev(zs[:, p]), G.dev(as_[:, p]), G.dev(bs[:, p]), conv, S, o)
+        torch.cuda.synchronize()
+        assert torch.equal(ck_S[:, p], S) and torch.equal(ck_conv[:, p], conv)
+        assert torch.equal(out.view(B, K, -1)[:, p], o)
+    o_ref, _, S_ck_ref, c_ck_ref = oracle.verify_checkpoints(c.Hk, c.Hv, c.x, c.z, c.a_raw, c.b_raw, c.conv_w,
+                                                             c.dt_bias, c.ssm_a, c.norm_w, c.conv0, c.S0, K)
+    G.assert_out_close(out, o_ref, c.act_dtype)
+    G.assert_state_close(ck_S, S_ck_ref, c.act_dtype)
+    assert G.conv_bits_equal(ck_conv, c_ck_ref, c.act_dtype)
+
+
 def test_large_batch_nonfinite_reported():
     c = gdn_inputs.make_case("lnan", Hk=16, Hv=32, B=64, K=1, seed=13)
     c.x[7, 2 * 16 * 128 + 3 * 128 + 9] = float("nan")     # sequence 7, v-head 3, row 9
