@@ -761,6 +761,22 @@ def decode_bf16_part(dev):
     return lambda: gdn.gdn_decode_step(d, w, i["x"], i["z"], i["a_raw"], i["b_raw"], conv, S, o)
 
 
+def varlen_part(dev):
+    """The packed varlen prefill (8 sequences, T=65536, nonzero initial state), as timed in `extras`."""
+    import gated_deltanet_linear_decode_gb300 as gdn
+    c = gdn_inputs.varlen_t65536()
+    d = gdn.make_dims(c.Hk, c.Hv, torch.bfloat16, torch.bfloat16)
+    w = gdn.make_weights(c.conv_w, c.dt_bias, c.ssm_a, c.norm_w, device=dev)
+    i = {k: getattr(c, k).to(dev) for k in ("x", "z", "a_raw", "b_raw")}
+    cu_h = c.cu_seqlens.to(torch.int32)
+    cu_d = cu_h.to(dev)
+    conv, S = c.conv0.to(dev), c.S0.to(dev)
+    po = torch.empty(c.T, c.Hv * 128, device=dev, dtype=torch.bfloat16)
+    ws = torch.empty(max(gdn.gdn_prefill_workspace_bytes(d, c.N, c.T), 16), device=dev, dtype=torch.uint8)
+    return lambda: gdn.gdn_prefill_chunked(d, w, cu_h, cu_d, i["x"], i["z"], i["a_raw"], i["b_raw"], conv, S, po,
+                                           zero_init=False, workspace=ws)
+
+
 def run_part(args):
     """Warm-up then timed launches of one part only (profiling aid)."""
     dev = torch.device("cuda", 0)
@@ -771,6 +787,8 @@ def run_part(args):
         fn = proj_part(dev)
     elif args.only == "decode-bf16":
         fn = decode_bf16_part(dev)
+    elif args.only == "varlen":
+        fn = varlen_part(dev)
     for _ in range(args.warmup + args.steps):
         wl.flush_l2()
         fn()
@@ -899,7 +917,7 @@ def main():
                     help="skip the batch-1 graph decode and the varlen T=65536 prefill (timed outside the step)")
     ap.add_argument("--prefill-tokens", type=int, default=8192,
                     help="with --only prefill: the sequence length (a smaller case for profiling)")
-    ap.add_argument("--only", choices=["prefill", "decode", "verify", "proj", "decode-bf16"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "verify", "proj", "decode-bf16", "varlen"], default=None,
                     help="run only one part of the step (for profiling); no JSON line")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
